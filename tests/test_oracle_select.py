@@ -1,0 +1,84 @@
+"""Pins of the oracle's two-level selection ("DeepSeek-V4.1-Flash-NVFP4" §3.3:
+blocks of 8 positions scored by their best position, top-2048 blocks with the
+block holding the newest position always kept, then top-512 positions; config
+walkthrough §2.1 for the sizes). Ties go to the lower index (reading stated in
+the design doc). Checked by brute force on tiny inputs with many ties."""
+import itertools
+
+import numpy as np
+
+from oracle import oracle as orc
+
+
+def brute_select(scores, blk, Kb, Kp):
+    n = len(scores)
+    if n == 0:
+        return []
+    nb = -(-n // blk)
+    bm = [max(scores[b * blk:(b + 1) * blk]) for b in range(nb)]
+    if nb <= Kb:
+        kept = set(range(nb))
+    else:
+        newest = (n - 1) // blk
+        others = sorted((b for b in range(nb) if b != newest), key=lambda b: (-bm[b], b))
+        kept = set(others[:Kb - 1]) | {newest}
+    cand = [t for t in range(n) if t // blk in kept]
+    best = sorted(cand, key=lambda t: (-scores[t], t))[:Kp]
+    return sorted(best)
+
+
+def test_matches_brute_force_with_ties():
+    rng = np.random.default_rng(0)
+    for trial in range(400):
+        n = int(rng.integers(0, 70))
+        levels = rng.integers(1, 6)
+        s = rng.integers(0, levels, n).astype(np.float32) * np.float32(0.5)
+        blk, Kb, Kp = 8, int(rng.integers(1, 5)), int(rng.integers(1, 12))
+        idx, m = orc.select(s, blk, Kb, Kp)
+        ref = brute_select(list(s), blk, Kb, Kp)
+        assert m == len(ref)
+        assert list(idx[:m]) == ref and np.all(idx[m:] == -1), (trial, n, Kb, Kp)
+
+
+def test_exhaustive_tiny():
+    for n in range(1, 11):
+        for s in itertools.product([0.0, 1.0], repeat=min(n, 6)):
+            s = np.array(list(s) + [0.5] * (n - len(s)), np.float32)
+            idx, m = orc.select(s, 2, 2, 3)
+            assert list(idx[:m]) == brute_select(list(s), 2, 2, 3)
+
+
+def test_newest_block_always_kept_even_when_worst():
+    s = np.ones(8 * 40, np.float32)
+    s[-8:] = -5.0  # the newest block has the lowest scores
+    idx, m = orc.select(s, 8, 4, 32)
+    kept_blocks = set(int(t) // 8 for t in idx[:m])
+    assert 39 in kept_blocks and len(kept_blocks) == 4
+    assert m == 32  # 4 blocks x 8 positions, all kept
+
+
+def test_block_stage_is_identity_when_few_blocks():
+    rng = np.random.default_rng(1)
+    s = rng.standard_normal(2048).astype(np.float32)  # 256 blocks <= 2048
+    idx, m = orc.select(s, 8, 2048, 512)
+    ref = np.sort(np.argsort(-s, kind="stable")[:512])
+    assert m == 512 and np.array_equal(idx, ref)
+
+
+def test_short_context_keeps_everything():
+    s = np.arange(100, dtype=np.float32)
+    idx, m = orc.select(s, 8, 2048, 512)
+    assert m == 100 and np.array_equal(idx[:100], np.arange(100)) and np.all(idx[100:] == -1)
+    idx, m = orc.select(np.zeros(0, np.float32), 8, 2048, 512)
+    assert m == 0 and np.all(idx == -1)
+
+
+def test_planted_high_scores_are_selected_and_the_block_cut_binds():
+    rng = np.random.default_rng(2)
+    n = 8 * 5000
+    s = rng.standard_normal(n).astype(np.float32)
+    plants = rng.choice(n - 8, 16, replace=False)
+    s[plants] = 100.0
+    idx, m = orc.select(s, 8, 2048, 512)
+    assert m == 512 and set(plants) <= set(idx.tolist())
+    assert len(set(int(t) // 8 for t in idx)) <= 2048
