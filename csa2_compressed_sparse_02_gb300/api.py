@@ -1,0 +1,168 @@
+"""Python binding of the CSA2 C ABI (``include/csa2.h``): argument marshalling only.
+
+Every function has the ABI call's name without the ``csa2_`` prefix, takes
+torch CUDA tensors, passes their device pointers and the current CUDA stream,
+and raises ``Csa2Error`` on a non-zero status. All arithmetic runs in the CUDA
+kernels of ``libcsa2.so``; nothing here computes on the data.
+
+``LayerCache`` and ``IndexKeyCache`` allocate one layer's per-sequence buffers
+with PyTorch (device memory is PyTorch's job) and build the device arrays of
+per-sequence base pointers the ABI takes.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from dataclasses import dataclass
+
+import torch
+
+from ._lib import Csa2Error, Params, check, lib  # noqa: F401
+
+F32, NVFP4, E4M3, BF16 = 0, 1, 2, 3
+D, H, HI, DI, W, BLK, KB, KP = 512, 64, 32, 128, 128, 8, 2048, 512
+
+
+def default_params(**over) -> Params:
+    p = Params()
+    lib().csa2_default_params(ctypes.byref(p))
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+def version() -> int:
+    return lib().csa2_version()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise Csa2Error("expected a CUDA tensor")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def ptr_array(tensors, device=None) -> torch.Tensor:
+    """Device int64 array of the base addresses of `tensors` (one per sequence)."""
+    addrs = [t.data_ptr() for t in tensors]
+    dev = device or tensors[0].device
+    return torch.tensor(addrs, dtype=torch.int64, device=dev)
+
+
+# --------------------------------------------------------------------------- calls
+def compress_append(params, kv_new, gate_new, pend_kv, pend_gate, comp_ptrs, comp_scale_ptrs,
+                    comp_cap, win_ptrs, n_tokens, dev_status=None, stream=None):
+    B = n_tokens.numel()
+    n_new = kv_new.shape[1] if kv_new.dim() == 3 else 0
+    check(lib().csa2_compress_append(
+        ctypes.byref(params), B, n_new, _ptr(kv_new), _ptr(gate_new), _ptr(pend_kv),
+        _ptr(pend_gate), _ptr(comp_ptrs), _ptr(comp_scale_ptrs), _ptr(comp_cap), _ptr(win_ptrs),
+        _ptr(n_tokens), _ptr(dev_status), _stream(stream)), "compress_append")
+
+
+def nvfp4_quantize(x, vals, scales, stream=None):
+    check(lib().csa2_nvfp4_quantize(_ptr(x), x.numel() // x.shape[-1], x.shape[-1], _ptr(vals),
+                                    _ptr(scales), _stream(stream)), "nvfp4_quantize")
+
+
+def index_scores(params, max_ncomp, q_vals, q_scales, w, key_val_ptrs, key_scale_ptrs, n_tokens,
+                 scores, block_max, dev_status=None, stream=None):
+    B = n_tokens.numel()
+    check(lib().csa2_index_scores(
+        ctypes.byref(params), B, max_ncomp, _ptr(q_vals), _ptr(q_scales), _ptr(w),
+        _ptr(key_val_ptrs), _ptr(key_scale_ptrs), _ptr(n_tokens), _ptr(scores), _ptr(block_max),
+        _ptr(dev_status), _stream(stream)), "index_scores")
+
+
+def select_topk(params, max_ncomp, scores, block_max, n_tokens, idx, n_sel=None, dev_status=None,
+                stream=None):
+    B = n_tokens.numel()
+    check(lib().csa2_select_topk(
+        ctypes.byref(params), B, max_ncomp, _ptr(scores), _ptr(block_max), _ptr(n_tokens),
+        _ptr(idx), _ptr(n_sel), _ptr(dev_status), _stream(stream)), "select_topk")
+
+
+def sparse_attn_workspace_size(params, B) -> int:
+    return lib().csa2_sparse_attn_workspace_size(ctypes.byref(params), B)
+
+
+def sparse_attn(params, q, sink, win_ptrs, n_tokens, comp_ptrs, comp_scale_ptrs, idx, out,
+                workspace, dev_status=None, stream=None):
+    B = n_tokens.numel()
+    check(lib().csa2_sparse_attn(
+        ctypes.byref(params), B, _ptr(q), _ptr(sink), _ptr(win_ptrs), _ptr(n_tokens),
+        _ptr(comp_ptrs), _ptr(comp_scale_ptrs), _ptr(idx), _ptr(out), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)),
+        "sparse_attn")
+
+
+# --------------------------------------------------------------------------- buffers
+@dataclass
+class LayerCache:
+    """One layer's per-sequence state: compressed cache (NVFP4 or fp32, absent
+    for window-only layers), ring window, pending half-pair, token counts."""
+    B: int
+    caps: list
+    params: Params
+    has_comp: bool = True
+    device: str = "cuda"
+
+    def __post_init__(self):
+        dev, B, p = self.device, self.B, self.params
+        nv = p.kv_format == NVFP4
+        self.comp, self.comp_scales = [], []
+        if self.has_comp:
+            for cap in self.caps:
+                cap = max(1, int(cap))
+                if nv:
+                    self.comp.append(torch.zeros(cap, D // 2, dtype=torch.uint8, device=dev))
+                    self.comp_scales.append(torch.zeros(cap, D // 16, dtype=torch.uint8, device=dev))
+                else:
+                    self.comp.append(torch.zeros(cap, D, dtype=torch.float32, device=dev))
+        wdt = torch.uint8 if p.win_format == E4M3 else torch.float32
+        self.win = torch.zeros(B, W, D, dtype=wdt, device=dev)
+        self.pend_kv = torch.zeros(B, D, dtype=torch.float32, device=dev)
+        self.pend_gate = torch.zeros(B, D, dtype=torch.float32, device=dev)
+        self.n_tokens = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.comp_cap = torch.tensor([max(1, int(c)) for c in self.caps], dtype=torch.int64,
+                                     device=dev)
+        self.comp_ptrs = ptr_array(self.comp) if self.has_comp else None
+        self.comp_scale_ptrs = ptr_array(self.comp_scales) if (self.has_comp and nv) else None
+        self.win_ptrs = ptr_array(list(self.win.unbind(0)))
+
+    def append(self, kv_new, gate_new=None, dev_status=None, stream=None):
+        compress_append(self.params, kv_new, gate_new if self.has_comp else None,
+                        self.pend_kv if self.has_comp else None,
+                        self.pend_gate if self.has_comp else None,
+                        self.comp_ptrs, self.comp_scale_ptrs,
+                        self.comp_cap if self.has_comp else None, self.win_ptrs, self.n_tokens,
+                        dev_status, stream)
+
+    def shares_compressed_cache_of(self, other: "LayerCache"):
+        """Point this (window-only) layer's compressed-cache arrays at `other`'s."""
+        self.comp_ptrs, self.comp_scale_ptrs = other.comp_ptrs, other.comp_scale_ptrs
+
+
+@dataclass
+class IndexKeyCache:
+    """Per-sequence FP4 index keys: values [cap, 64] and E4M3 scales [cap, 8]."""
+    caps: list
+    device: str = "cuda"
+
+    def __post_init__(self):
+        self.vals = [torch.zeros(max(1, int(c)), DI // 2, dtype=torch.uint8, device=self.device)
+                     for c in self.caps]
+        self.scales = [torch.zeros(max(1, int(c)), DI // 16, dtype=torch.uint8, device=self.device)
+                       for c in self.caps]
+        self.val_ptrs = ptr_array(self.vals)
+        self.scale_ptrs = ptr_array(self.scales)
+
+
+def n_blocks(n: int) -> int:
+    return math.ceil(n / BLK)

@@ -1,0 +1,45 @@
+// Host-side pieces of the C ABI: defaults, version, per-thread error text.
+#include <cmath>
+
+#include "common.cuh"
+
+namespace csa2 {
+
+static thread_local std::string g_last_error;
+
+void set_error(const std::string& msg) { g_last_error = msg; }
+
+int fail(int code, const std::string& msg) {
+    g_last_error = msg;
+    return code;
+}
+
+int check_launch(const char* what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return fail(CSA2_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+    return CSA2_OK;
+}
+
+}  // namespace csa2
+
+extern "C" void csa2_default_params(csa2_params* p) {
+    if (!p) return;
+    p->heads = csa2::kH;
+    p->head_dim = csa2::kD;
+    p->index_heads = csa2::kHi;
+    p->index_dim = csa2::kDi;
+    p->window = csa2::kW;
+    p->block_size = csa2::kBlk;
+    p->topk_blocks = csa2::kKb;
+    p->topk_pos = csa2::kKp;
+    p->compress_ratio = 2;
+    p->kv_format = CSA2_NVFP4;
+    p->win_format = CSA2_E4M3;
+    p->q_format = CSA2_BF16;
+    p->softmax_scale = 1.0f / std::sqrt((float)csa2::kD);
+}
+
+extern "C" int csa2_version(void) { return 100; }
+
+extern "C" const char* csa2_last_error(void) { return csa2::g_last_error.c_str(); }

@@ -1,0 +1,80 @@
+// Internal helpers shared by the CSA2 kernels (sm_103a). Not part of the ABI.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "../../include/csa2.h"
+
+namespace csa2 {
+
+// Pages' sizes the kernels are specialised for ("CSA2稀疏注意力、384专家MoE与1M上下文"
+// config walkthrough §2.1, §一; "DeepSeek-V4.1-Flash-NVFP4" §3.1-§3.3).
+constexpr int kD = 512;       // KV latent dim
+constexpr int kH = 64;        // query heads
+constexpr int kHi = 32;       // index heads
+constexpr int kDi = 128;      // index head dim
+constexpr int kW = 128;       // window slots
+constexpr int kBlk = 8;       // candidate block size
+constexpr int kKb = 2048;     // blocks kept
+constexpr int kKp = 512;      // positions kept
+constexpr int kGroup = 16;    // NVFP4 group
+
+void set_error(const std::string& msg);
+int fail(int code, const std::string& msg);
+int check_launch(const char* what);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Raise a status bit on the device (NULL status pointer = ignore).
+__device__ __forceinline__ void raise_status(int32_t* st, int bit) {
+    if (st) atomicOr(st, bit);
+}
+
+// E2M1 code of y: round to nearest, ties to the even code, |y| > 6 -> 6, sign
+// bit from y. Thresholds are the midpoints of the E2M1 grid
+// {0, .5, 1, 1.5, 2, 3, 4, 6}; at a midpoint the code with mantissa bit 0 wins,
+// hence the alternation of > and >=.
+__device__ __forceinline__ uint32_t e2m1_code_rne(float y) {
+    float a = fabsf(y);
+    uint32_t c = (a > 0.25f) + (a >= 0.75f) + (a > 1.25f) + (a >= 1.75f) + (a > 2.5f) +
+                 (a >= 3.5f) + (a > 5.0f);
+    return c | ((__float_as_uint(y) >> 28) & 8u);
+}
+
+// E4M3 byte of a float (hardware convert: RNE, saturating to +-448).
+__device__ __forceinline__ uint8_t e4m3_byte(float x) {
+    return (uint8_t)__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3);
+}
+
+// Value of an E4M3 byte (exact).
+__device__ __forceinline__ float e4m3_value(uint8_t b) {
+    __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)b, __NV_E4M3);
+    return __half2float(__half(h));
+}
+
+// Two E2M1 codes (one byte, element 0 in the low nibble) -> two halves, exact.
+__device__ __forceinline__ uint32_t e2m1x2_to_half2(uint32_t byte) {
+    uint32_t out;
+    asm("{\n .reg .b8 t;\n cvt.u8.u32 t, %1;\n cvt.rn.f16x2.e2m1x2 %0, t;\n}"
+        : "=r"(out) : "r"(byte));
+    return out;
+}
+
+// Order-preserving u32 key of an fp32 score (larger value -> larger key;
+// -0 is folded onto +0 so that equal values tie).
+__device__ __forceinline__ uint32_t score_key(float x) {
+    uint32_t u = __float_as_uint(x + 0.0f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+}  // namespace csa2
+
+#define CSA2_CHECK_PARAMS(p)                                                    \
+    do {                                                                        \
+        if (!(p)) return csa2::fail(CSA2_ERR_INVALID_ARG, "params is NULL");    \
+    } while (0)

@@ -140,3 +140,28 @@ def plant_row(q_vals: np.ndarray, w: np.ndarray):
     weight (first such head), with group scale 4 (E4M3 0x48) on every group."""
     h = int(np.argmax(w))
     return q_vals[h].copy(), np.full(q_vals.shape[1] // 8, E4M3_FOUR, np.uint8)
+
+
+# ----------------------------------------------------------------------------- device twin
+G_NORMAL_F32, G_NORMAL_BF16, G_E2M1_BYTES, G_SCALE_POW2_BYTES, G_W_POW2_F32 = range(5)
+
+
+def gpu_fill(kind: int, keys, counter0: int, n_per_stream: int, out, stride: int | None = None,
+             stream=None):
+    """Fill out[s * stride + i] = value(keys[s], counter0 + i) on the device with the
+    same definitions as the host functions above (libcsa2synth.so)."""
+    import ctypes
+
+    import torch
+
+    from ._lib import synth_lib
+    keys = [int(k) & M64 for k in keys]
+    for s0 in range(0, len(keys), 64):
+        chunk = keys[s0:s0 + 64]
+        arr = (ctypes.c_uint64 * len(chunk))(*chunk)
+        st = n_per_stream if stride is None else stride
+        base = out.data_ptr() + s0 * st * out.element_size()
+        s = (torch.cuda.current_stream() if stream is None else stream).cuda_stream
+        rc = synth_lib().csa2synth_fill(kind, arr, len(chunk), counter0, n_per_stream, base, st, s)
+        if rc != 0:
+            raise RuntimeError("csa2synth_fill failed (%d)" % rc)

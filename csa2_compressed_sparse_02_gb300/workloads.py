@@ -1,0 +1,226 @@
+"""Device side of the CSA2 decode configurations: builds a configuration's
+caches and per-step inputs on the GPU from the seeded generator (the recipe is
+in ``inputs.py``) and enqueues decode steps through the C ABI (``api.py``).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field
+
+import numpy as np
+
+from . import synth
+from .inputs import CONFIGS, D, DI, H, HI, W, DecodeConfig, plants  # noqa: F401
+
+# =============================================================================== device side
+@dataclass
+class DecodeRun:
+    """Device state of one decode configuration, ready to run `n_steps` steps."""
+    cfg: DecodeConfig
+    n_steps: int
+    device: str = "cuda"
+    step_done: int = 0
+    groups: list = field(default_factory=list)
+
+    def __post_init__(self):
+        import torch
+
+        from . import api
+        self.torch, self.api = torch, api
+        cfg, dev = self.cfg, self.device
+        self.T0 = cfg.first_lengths()
+        self.B = cfg.B
+        if cfg.quant:
+            self.params = api.default_params()
+        else:
+            self.params = api.default_params(kv_format=api.F32, win_format=api.F32,
+                                             q_format=api.F32)
+        last = [T + self.n_steps - 1 for T in self.T0]          # T after the last step
+        self.comp_caps = [t // 2 + 1 for t in last]
+        self.n_c_max = max(t // 2 for t in last)
+        self.key_rows = [max(1, t // 2) for t in last]
+        self.max_ncomp = self.n_c_max
+        self.n_b_max = math.ceil(self.max_ncomp / 8)
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        ws = api.sparse_attn_workspace_size(self.params, self.B)
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+        qdt = torch.bfloat16 if cfg.quant else torch.float32
+        for g in range(cfg.groups):
+            grp = {}
+            grp["src"] = api.LayerCache(self.B, self.comp_caps, self.params, device=dev)
+            if cfg.readers > 1:
+                grp["rd"] = api.LayerCache(self.B * (cfg.readers - 1), [1] * (self.B * (cfg.readers - 1)),
+                                           self.params, has_comp=False, device=dev)
+            grp["keys"] = api.IndexKeyCache(self.key_rows, device=dev)
+            grp["scores"] = torch.empty(self.B, self.max_ncomp, dtype=torch.float32, device=dev)
+            grp["bmax"] = torch.empty(self.B, self.n_b_max, dtype=torch.float32, device=dev)
+            grp["idx"] = torch.empty(self.B, 512, dtype=torch.int32, device=dev)
+            grp["n_sel"] = torch.empty(self.B, dtype=torch.int32, device=dev)
+            grp["out"] = [torch.empty(self.B, H, D, dtype=qdt, device=dev) for _ in range(cfg.readers)]
+            grp["sink"] = [torch.empty(H, dtype=torch.float32, device=dev) for _ in range(cfg.readers)]
+            # per-step inputs, resident before timing
+            grp["kv"] = torch.empty(self.n_steps, self.B, 1, D, dtype=torch.float32, device=dev)
+            grp["gate"] = torch.empty(self.n_steps, self.B, 1, D, dtype=torch.float32, device=dev)
+            if cfg.readers > 1:
+                grp["kv_rd"] = torch.empty(self.n_steps, self.B * (cfg.readers - 1), 1, D,
+                                           dtype=torch.float32, device=dev)
+            grp["q"] = torch.empty(self.n_steps, cfg.readers, self.B, H, D, dtype=qdt, device=dev)
+            grp["iq"] = torch.empty(self.n_steps, self.B, HI, DI // 2, dtype=torch.uint8, device=dev)
+            grp["iqs"] = torch.full((self.n_steps, self.B, HI, DI // 16), synth.E4M3_ONE,
+                                    dtype=torch.uint8, device=dev)
+            grp["iw"] = torch.empty(self.n_steps, self.B, HI, dtype=torch.float32, device=dev)
+            self.groups.append(grp)
+        self._fill()
+
+    # ------------------------------------------------------------------ setup
+    def _keys(self, kind, layer):
+        return [synth.stream_key(self.cfg.seed, kind, layer, s) for s in range(self.B)]
+
+    def _prefill_source(self, g, grp, chunk=8192):
+        """Compressor over raw tokens [0, T0-1) of every sequence of the group's source."""
+        torch, cfg, src = self.torch, self.cfg, grp["src"]
+        lay = cfg.layer(g, 0)
+        for seqs in self._seq_sets():
+            n_pre = self.T0[seqs[0]] - 1
+            nb = len(seqs)
+            sl = slice(seqs[0], seqs[0] + nb)
+            view = _CacheView(src, sl)
+            kvk = [synth.stream_key(cfg.seed, synth.KV, lay, s) for s in seqs]
+            gk = [synth.stream_key(cfg.seed, synth.GATE, lay, s) for s in seqs]
+            ch = max(1, min(chunk, (1 << 29) // (nb * D * 8)))
+            kv = torch.empty(nb, ch, D, dtype=torch.float32, device=self.device)
+            gt = torch.empty_like(kv)
+            for t0 in range(0, n_pre, ch):
+                n = min(ch, n_pre - t0)
+                synth.gpu_fill(synth.G_NORMAL_F32, kvk, t0 * D, n * D, kv, stride=n * D)
+                synth.gpu_fill(synth.G_NORMAL_F32, gk, t0 * D, n * D, gt, stride=n * D)
+                self.api.compress_append(self.params, kv.view(-1)[:nb * n * D].view(nb, n, D),
+                                         gt.view(-1)[:nb * n * D].view(nb, n, D), view.pend_kv,
+                                         view.pend_gate, view.comp_ptrs, view.comp_scale_ptrs,
+                                         view.comp_cap, view.win_ptrs, view.n_tokens,
+                                         self.dev_status)
+
+    def _seq_sets(self):
+        """Sequences grouped by first length (all of them at once when uniform)."""
+        if len(set(self.T0)) == 1:
+            return [list(range(self.B))]
+        return [[s] for s in range(self.B)]
+
+    def _prefill_readers(self, g, grp):
+        """Windows of the readers: raw tokens [T0-W, T0-1) of each reader layer."""
+        torch, cfg, rd = self.torch, self.cfg, grp["rd"]
+        for r in range(1, cfg.readers):
+            lay = cfg.layer(g, r)
+            for seqs in self._seq_sets():
+                T0 = self.T0[seqs[0]]
+                t_start = max(0, T0 - W)
+                n = T0 - 1 - t_start
+                i0 = (r - 1) * self.B + seqs[0]
+                view = _CacheView(rd, slice(i0, i0 + len(seqs)))
+                view.n_tokens.fill_(t_start)
+                if n <= 0:
+                    continue
+                kv = torch.empty(len(seqs), n, D, dtype=torch.float32, device=self.device)
+                synth.gpu_fill(synth.G_NORMAL_F32,
+                               [synth.stream_key(cfg.seed, synth.KV, lay, s) for s in seqs],
+                               t_start * D, n * D, kv)
+                self.api.compress_append(self.params, kv, None, None, None, None, None, None,
+                                         view.win_ptrs, view.n_tokens, self.dev_status)
+
+    def _fill(self):
+        torch, cfg = self.torch, self.cfg
+        for g, grp in enumerate(self.groups):
+            self._prefill_source(g, grp)
+            if cfg.readers > 1:
+                self._prefill_readers(g, grp)
+            keys = grp["keys"]
+            for s in range(self.B):
+                n = self.key_rows[s]
+                synth.gpu_fill(synth.G_E2M1_BYTES, [synth.stream_key(cfg.seed, synth.IDX_K, g, s)],
+                               0, n * DI // 2, keys.vals[s])
+                if cfg.kscale_pow2:
+                    synth.gpu_fill(synth.G_SCALE_POW2_BYTES,
+                                   [synth.stream_key(cfg.seed, synth.IDX_K_SCALE, g, s)], 0,
+                                   n * DI // 16, keys.scales[s])
+                else:
+                    keys.scales[s].fill_(synth.E4M3_ONE)
+                pos, rv, rs = plants(cfg, g, s)
+                pos = pos[pos < n]
+                if pos.size:
+                    pi = torch.from_numpy(pos).to(self.device)
+                    keys.vals[s][pi] = torch.from_numpy(np.tile(rv, (pos.size, 1))).to(self.device)
+                    keys.scales[s][pi] = torch.from_numpy(np.tile(rs, (pos.size, 1))).to(self.device)
+            for r in range(cfg.readers):
+                lay = cfg.layer(g, r)
+                synth.gpu_fill(synth.G_NORMAL_F32, [synth.stream_key(cfg.seed, synth.SINK, lay, 0)],
+                               0, H, grp["sink"][r])
+            qkind = synth.G_NORMAL_BF16 if cfg.quant else synth.G_NORMAL_F32
+            for k in range(self.n_steps):
+                for seqs in self._seq_sets():
+                    tok = self.T0[seqs[0]] - 1 + k  # raw position of this step's token
+                    s0, nb = seqs[0], len(seqs)
+                    for r in range(cfg.readers):
+                        lay = cfg.layer(g, r)
+                        kk = [synth.stream_key(cfg.seed, synth.KV, lay, s) for s in seqs]
+                        if r == 0:
+                            gk = [synth.stream_key(cfg.seed, synth.GATE, lay, s) for s in seqs]
+                            synth.gpu_fill(synth.G_NORMAL_F32, kk, tok * D, D,
+                                           grp["kv"][k, s0:s0 + nb], stride=D)
+                            synth.gpu_fill(synth.G_NORMAL_F32, gk, tok * D, D,
+                                           grp["gate"][k, s0:s0 + nb], stride=D)
+                        else:
+                            i0 = (r - 1) * self.B + s0
+                            synth.gpu_fill(synth.G_NORMAL_F32, kk, tok * D, D,
+                                           grp["kv_rd"][k, i0:i0 + nb], stride=D)
+                for r in range(cfg.readers):
+                    synth.gpu_fill(qkind, self._keys(synth.Q, cfg.layer(g, r)), k * H * D, H * D,
+                                   grp["q"][k, r])
+                synth.gpu_fill(synth.G_E2M1_BYTES, [synth.stream_key(cfg.seed, synth.IDX_Q, g, s)
+                                                    for s in range(self.B)],
+                               k * HI * DI // 2, HI * DI // 2, grp["iq"][k])
+                synth.gpu_fill(synth.G_W_POW2_F32, [synth.stream_key(cfg.seed, synth.IDX_W, g, s)
+                                                    for s in range(self.B)], k * HI, HI, grp["iw"][k])
+        torch.cuda.synchronize()
+
+    # ------------------------------------------------------------------ one step
+    def step(self, stream=None):
+        """Enqueue one decode step (every group, every layer) on `stream`."""
+        api, cfg, k = self.api, self.cfg, self.step_done
+        assert k < self.n_steps, "more steps than prepared"
+        p = self.params
+        for grp in self.groups:
+            src = grp["src"]
+            src.append(grp["kv"][k], grp["gate"][k], self.dev_status, stream)
+            if cfg.readers > 1:
+                grp["rd"].append(grp["kv_rd"][k], None, self.dev_status, stream)
+            api.index_scores(p, self.max_ncomp, grp["iq"][k], grp["iqs"][k], grp["iw"][k],
+                             grp["keys"].val_ptrs, grp["keys"].scale_ptrs, src.n_tokens,
+                             grp["scores"], grp["bmax"], self.dev_status, stream)
+            api.select_topk(p, self.max_ncomp, grp["scores"], grp["bmax"], src.n_tokens,
+                            grp["idx"], grp["n_sel"], self.dev_status, stream)
+            for r in range(cfg.readers):
+                if r == 0:
+                    win_ptrs, n_tok = src.win_ptrs, src.n_tokens
+                else:
+                    sl = slice((r - 1) * self.B, r * self.B)
+                    win_ptrs, n_tok = grp["rd"].win_ptrs[sl], grp["rd"].n_tokens[sl]
+                api.sparse_attn(p, grp["q"][k, r], grp["sink"][r], win_ptrs, n_tok, src.comp_ptrs,
+                                src.comp_scale_ptrs, grp["idx"], grp["out"][r], self.workspace,
+                                self.dev_status, stream)
+        self.step_done += 1
+
+    def tokens_after(self, s: int) -> int:
+        return self.T0[s] - 1 + self.step_done
+
+
+class _CacheView:
+    """A contiguous slice of a LayerCache's sequences, addressable on its own."""
+
+    def __init__(self, cache, sl: slice):
+        self.pend_kv = cache.pend_kv[sl]
+        self.pend_gate = cache.pend_gate[sl]
+        self.n_tokens = cache.n_tokens[sl]
+        self.comp_ptrs = cache.comp_ptrs[sl] if cache.comp_ptrs is not None else None
+        self.comp_scale_ptrs = cache.comp_scale_ptrs[sl] if cache.comp_scale_ptrs is not None else None
+        self.comp_cap = cache.comp_cap[sl]
+        self.win_ptrs = cache.win_ptrs[sl]

@@ -1,0 +1,209 @@
+/*
+ * csa2.h — C ABI of the CSA2 (Compressed Sparse Attention 2) hot path on GB300.
+ *
+ * One layer's decode path, as the "DeepSeek-V4.1-Flash-NVFP4" walkthrough
+ * (lpnh.cn) describes it:
+ *   csa2_compress_append   §3.2 Compressor (2:1 softmax-gated pooling, NVFP4
+ *                          cache, pending half-pair kept in state) and §3.1
+ *                          128-slot FP8 ring window, one write per token;
+ *   csa2_index_scores      §3.3 Indexer (32 FP4 index heads, ReLU, per-head
+ *                          weights) with the block maximum over 8 positions;
+ *   csa2_select_topk       §3.3 select_candidate_blocks (top-2048 blocks of 8,
+ *                          newest block kept) then top-512 positions;
+ *   csa2_sparse_attn       §3.4 sparse_attn (gather, online softmax, attn_sink),
+ *                          §三 128 window + 512 selected = 640 positions.
+ * Sizes from the "CSA2稀疏注意力、384专家MoE与1M上下文" config walkthrough
+ * (nxmr.cn) §2.1 and §一 (64 query heads sharing one KV head of dim 512).
+ *
+ * Conventions (all calls):
+ *  - Pointers named *_dev (and every array argument unless stated otherwise)
+ *    are CUDA device pointers. The caller owns every buffer; the library
+ *    allocates nothing and keeps no per-call state. Scratch, where a call
+ *    needs it, is a caller buffer sized by a *_workspace_size query.
+ *  - Per-sequence caches are reached through device arrays of per-sequence
+ *    base pointers (ragged batches need no common stride).
+ *  - `stream` is a cudaStream_t passed as void*. Every call only enqueues work
+ *    on it and returns; nothing synchronises.
+ *  - Return value: CSA2_OK or a CSA2_ERR_* code for errors found on the host
+ *    (bad arguments, unsupported sizes, launch failures; text in
+ *    csa2_last_error(), per calling thread). Nothing is enqueued on error.
+ *  - Errors only visible on the device (an index outside the cache, a length
+ *    beyond capacity) set CSA2_DEV_* bits in the caller's int32 `dev_status`
+ *    (atomicOr; may be NULL to skip), the offending element is skipped, and
+ *    the kernel completes. The caller reads it after synchronising.
+ *  - The hot kernels are specialised for the pages' sizes (csa2_default_params);
+ *    other sizes return CSA2_ERR_UNSUPPORTED.
+ */
+#ifndef CSA2_H
+#define CSA2_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---- */
+#define CSA2_OK 0
+#define CSA2_ERR_INVALID_ARG 1 /* NULL where a buffer is required, negative size */
+#define CSA2_ERR_SHAPE 2       /* inconsistent sizes (e.g. workspace too small) */
+#define CSA2_ERR_ALIGN 3       /* pointer not 16-byte aligned where vector loads need it */
+#define CSA2_ERR_UNSUPPORTED 4 /* sizes or formats the kernels are not built for */
+#define CSA2_ERR_CUDA 5        /* a CUDA launch or attribute call failed */
+
+/* ---- device status bits (OR-ed into *dev_status) ---- */
+#define CSA2_DEV_BAD_INDEX 1   /* a selected index >= the sequence's compressed length */
+#define CSA2_DEV_BAD_LENGTH 2  /* a sequence length beyond the stated capacity, or < 0 */
+
+/* ---- formats ---- */
+#define CSA2_F32 0   /* fp32 */
+#define CSA2_NVFP4 1 /* E2M1 pairs (element 2k = low nibble of byte k) + one E4M3 scale per 16 */
+#define CSA2_E4M3 2  /* FP8 E4M3 ("fn": max 448, no inf), unit scale */
+#define CSA2_BF16 3  /* bfloat16 */
+
+typedef struct csa2_params {
+    int heads;            /* query heads sharing the KV head: 64 */
+    int head_dim;         /* KV latent / query head dim D: 512 */
+    int index_heads;      /* Indexer query heads: 32 */
+    int index_dim;        /* Indexer head dim: 128 */
+    int window;           /* ring window slots W: 128 */
+    int block_size;       /* positions per candidate block: 8 */
+    int topk_blocks;      /* blocks kept: 2048 */
+    int topk_pos;         /* positions kept: 512 */
+    int compress_ratio;   /* raw tokens per compressed position: 2 */
+    int kv_format;        /* compressed cache: CSA2_NVFP4 (or CSA2_F32, unquantised) */
+    int win_format;       /* window ring: CSA2_E4M3 (or CSA2_F32) */
+    int q_format;         /* query and output: CSA2_BF16 (or CSA2_F32) */
+    float softmax_scale;  /* logit scale: 1/sqrt(head_dim) */
+} csa2_params;
+
+/* Fills *p with the pages' configuration (64/512/32/128/128/8/2048/512/2,
+ * NVFP4 cache, E4M3 window, bf16 query, 1/sqrt(512)). */
+void csa2_default_params(csa2_params* p);
+
+/* Library ABI version (major*10000 + minor*100 + patch). */
+int csa2_version(void);
+
+/* Text of the last host-side error on the calling thread ("" if none). */
+const char* csa2_last_error(void);
+
+/*
+ * csa2_compress_append — append n_new raw tokens to B sequences of one layer.
+ * ("DeepSeek-V4.1-Flash-NVFP4" §3.2 Compressor, §3.1 window.)
+ *
+ * Before the call sequence b holds T_b = n_tokens[b] raw tokens; compressed
+ * row j pools raw tokens 2j and 2j+1; when T_b is odd, token T_b-1 waits in
+ * pend_kv/pend_gate. For every pair completed by the new tokens, per channel d:
+ *   alpha_i = softmax_{i in pair}(gate[i,d]),  c[d] = sum_i alpha_i * kv[i,d]  (fp32)
+ * and c is written to compressed row j of comp[b]:
+ *   kv_format NVFP4: per 16-channel group, S = E4M3(amax/6) (fp32 division,
+ *     round to nearest even, saturating), codes = E2M1(c/S) (IEEE fp32
+ *     division, RNE, saturating to +-6, sign kept), all codes 0 when S = 0.
+ *     Row layout: comp[b] + j*D/2 bytes (values), comp_scales[b] + j*D/16 bytes.
+ *   kv_format F32: comp[b] + j*D floats.
+ * Every new raw token p also writes ring slot p mod W of win[b] (D bytes E4M3,
+ * RNE satfinite, or D floats) — only the newest W of them, as the ring keeps.
+ * Afterwards n_tokens[b] = T_b + n_new.
+ *
+ *   kv_new, gate_new  [B, n_new, D] fp32, device. gate_new may be NULL when
+ *                     comp is NULL.
+ *   pend_kv, pend_gate [B, D] fp32, device; caller zero-initialises once.
+ *   comp              device array [B] of per-sequence row bases, or NULL for a
+ *                     window-only layer (compress ratio 0, or a layer that reads
+ *                     another layer's compressed cache).
+ *   comp_scales       device array [B] of scale-row bases (NVFP4 only).
+ *   comp_cap          [B] int64, device: rows allocated per sequence; a row
+ *                     j >= comp_cap[b] is not written and sets CSA2_DEV_BAD_LENGTH.
+ *   win               device array [B] of ring bases ([W, D]).
+ *   n_tokens          [B] int32, device, read and advanced.
+ * Constraints: D == 512; n_new >= 0; 16-byte aligned rows.
+ */
+int csa2_compress_append(const csa2_params* p, int B, int n_new,
+                         const float* kv_new, const float* gate_new,
+                         float* pend_kv, float* pend_gate,
+                         void* const* comp, uint8_t* const* comp_scales, const int64_t* comp_cap,
+                         void* const* win, int32_t* n_tokens,
+                         int32_t* dev_status, void* stream);
+
+/*
+ * csa2_nvfp4_quantize — quantise n_rows rows of row_len fp32 values to NVFP4
+ * with exactly the rule csa2_compress_append uses ("DeepSeek-V4.1-Flash-NVFP4"
+ * §3.2). Used for index keys/queries produced outside the path and to check
+ * the quantiser on identical inputs.
+ *   x      [n_rows, row_len] fp32, device;  vals [n_rows, row_len/2] bytes;
+ *   scales [n_rows, row_len/16] bytes.  row_len % 16 == 0.
+ */
+int csa2_nvfp4_quantize(const float* x, int64_t n_rows, int row_len,
+                        uint8_t* vals, uint8_t* scales, void* stream);
+
+/*
+ * csa2_index_scores — decode Indexer over every compressed position of B
+ * sequences ("DeepSeek-V4.1-Flash-NVFP4" §3.3):
+ *   s_t = sum_{h<Hi} w[h] * ReLU( sum_{d<Di} q[h,d] * k[t,d] ),  t < n_c,
+ * with q and k the NVFP4-decoded values (E2M1 code x E4M3 group scale), fp32
+ * accumulation, and the block maximum m_b = max_{t in [8b, 8b+8), t < n_c} s_t.
+ * n_c = n_tokens[b] / compress_ratio.
+ *
+ *   q_vals   [B, Hi, Di/2] bytes   q_scales [B, Hi, Di/16] bytes   w [B, Hi] fp32
+ *   key_vals, key_scales: device arrays [B] of per-sequence bases of the index
+ *            key cache, [cap, Di/2] and [cap, Di/16] bytes (row t = position t).
+ *   scores   [B, max_ncomp] fp32 out (entries >= n_c untouched)
+ *   block_max [B, ceil(max_ncomp/8)] fp32 out (entries >= ceil(n_c/8) untouched)
+ *   max_ncomp >= every n_c (else CSA2_DEV_BAD_LENGTH, and the sequence is clipped).
+ * Constraints: Hi == 32, Di == 128, block_size == 8.
+ * The fp32 result is exact (independent of summation order) when every
+ * partial sum is a multiple of a common power of two below 2^24 of it — true
+ * for E2M1 codes with power-of-two scales and weights.
+ */
+int csa2_index_scores(const csa2_params* p, int B, int64_t max_ncomp,
+                      const uint8_t* q_vals, const uint8_t* q_scales, const float* w,
+                      const uint8_t* const* key_vals, const uint8_t* const* key_scales,
+                      const int32_t* n_tokens, float* scores, float* block_max,
+                      int32_t* dev_status, void* stream);
+
+/*
+ * csa2_select_topk — two-level selection ("DeepSeek-V4.1-Flash-NVFP4" §3.3).
+ * Per sequence, with n_c = n_tokens[b]/compress_ratio and n_b = ceil(n_c/8):
+ *   if n_b > topk_blocks: keep block n_b-1 (it holds the newest position) and
+ *   the best topk_blocks-1 other blocks by (block_max desc, block asc); else
+ *   keep every block. Among the positions of kept blocks keep the best
+ *   topk_pos by (score desc, position asc).
+ *   idx   [B, topk_pos] int32 out: kept positions ascending, then -1 padding.
+ *   n_sel [B] int32 out: number of valid entries (may be NULL).
+ * Scores compare as fp32 values (-0 == +0). Ties are resolved exactly.
+ */
+int csa2_select_topk(const csa2_params* p, int B, int64_t max_ncomp,
+                     const float* scores, const float* block_max, const int32_t* n_tokens,
+                     int32_t* idx, int32_t* n_sel, int32_t* dev_status, void* stream);
+
+/* Bytes of scratch csa2_sparse_attn needs for a batch of B queries. */
+size_t csa2_sparse_attn_workspace_size(const csa2_params* p, int B);
+
+/*
+ * csa2_sparse_attn — attention of one decode query per sequence over its
+ * window and its selected compressed positions, with a per-head sink logit in
+ * the denominator ("DeepSeek-V4.1-Flash-NVFP4" §3.4, §三, §3.1):
+ *   attended set: raw positions max(0,T-W)..T-1 (ring slot p mod W of win[b],
+ *   T = n_tokens[b]) and compressed rows idx[b][k] >= 0 of comp[b];
+ *   z_j = softmax_scale * q_h . k_j;  o_h = sum_j e^{z_j} v_j / (e^{sink_h} + sum_j e^{z_j}),
+ *   with K = V = the stored latent (NVFP4/E4M3 decoded exactly).
+ *   q    [B, H, D] bf16 (or fp32)      sink [H] fp32     out [B, H, D] bf16 (or fp32)
+ *   idx  [B, topk_pos] int32 (-1 = empty); an idx >= T/compress_ratio is
+ *        skipped and sets CSA2_DEV_BAD_INDEX.
+ *   workspace: device scratch of at least csa2_sparse_attn_workspace_size(p, B)
+ *   bytes (partial outputs of the split-KV passes); contents need no init.
+ * Constraints: H == 64, D == 512, W == 128, topk_pos == 512.
+ */
+int csa2_sparse_attn(const csa2_params* p, int B,
+                     const void* q, const float* sink,
+                     const void* const* win, const int32_t* n_tokens,
+                     const void* const* comp, const uint8_t* const* comp_scales,
+                     const int32_t* idx, void* out,
+                     void* workspace, size_t ws_bytes,
+                     int32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CSA2_H */

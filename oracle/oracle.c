@@ -154,31 +154,42 @@ static int lsb_exp(double v) {
     return e - 53 + __builtin_ctzll(M);
 }
 
+/* Smallest lsb exponent over the non-zero entries of v[0..n), INT32_MAX if all zero. */
+static int min_lsb(const double* v, int n) {
+    int m = INT32_MAX;
+    for (int i = 0; i < n; ++i)
+        if (v[i] != 0.0 && lsb_exp(v[i]) < m) m = lsb_exp(v[i]);
+    return m;
+}
+
 int64_t orc_index_scores(int Hi, int Di, const uint8_t* q_vals, const uint8_t* q_scales,
                          const float* w, int64_t n_c, const uint8_t* k_vals,
                          const uint8_t* k_scales, float* scores) {
     double* q = (double*)malloc(sizeof(double) * (size_t)Hi * Di);
     double* k = (double*)malloc(sizeof(double) * (size_t)Di);
-    for (int h = 0; h < Hi; ++h)
+    int* q_lsb = (int*)malloc(sizeof(int) * (size_t)Hi);
+    for (int h = 0; h < Hi; ++h) {
         for (int d = 0; d < Di; ++d)
             q[h * Di + d] = orc_nvfp4_value(q_vals + (int64_t)h * (Di / 2),
                                             q_scales + (int64_t)h * (Di / 16), d);
+        q_lsb[h] = min_lsb(q + h * Di, Di);
+    }
     int64_t inexact = 0;
     for (int64_t t = 0; t < n_c; ++t) {
         for (int d = 0; d < Di; ++d)
             k[d] = orc_nvfp4_value(k_vals + t * (Di / 2), k_scales + t * (Di / 16), d);
+        const int k_lsb = min_lsb(k, Di);
         double s = 0.0, s_bound = 0.0;
         int s_lsb = INT32_MAX, ok = 1;
         for (int h = 0; h < Hi; ++h) {
             double dot = 0.0, d_bound = 0.0;
-            int d_lsb = INT32_MAX;
             for (int d = 0; d < Di; ++d) {
                 double p = q[h * Di + d] * k[d];
                 dot += p;
                 d_bound += fabs(p);
-                if (p != 0.0 && lsb_exp(p) < d_lsb) d_lsb = lsb_exp(p);
             }
-            if (d_lsb != INT32_MAX && d_bound > ldexp(1.0, 24 + d_lsb)) ok = 0;
+            /* every product is a multiple of 2^(q_lsb + k_lsb); so is every partial sum */
+            if (d_bound != 0.0 && d_bound > ldexp(1.0, 24 + q_lsb[h] + k_lsb)) ok = 0;
             double term = (double)w[h] * (dot > 0.0 ? dot : 0.0); /* w_h * ReLU(q_h . k_t) */
             s += term;
             s_bound += fabs(term);
@@ -188,6 +199,7 @@ int64_t orc_index_scores(int Hi, int Di, const uint8_t* q_vals, const uint8_t* q
         scores[t] = (float)s;
         if (!ok) ++inexact;
     }
+    free(q_lsb);
     free(q);
     free(k);
     return inexact;

@@ -1,0 +1,62 @@
+"""C ABI checks that need no GPU: the library loads, exports every function
+include/*.h declares, and rejects bad arguments on the host before touching
+CUDA (no compute call is made here)."""
+import ctypes
+import glob
+import os
+
+import pytest
+
+from csa2_compressed_sparse_02_gb300 import _lib, api
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(_lib.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    return _lib.lib()
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        names += _lib.header_symbols(h)
+    assert names, "no declarations found"
+    raw = ctypes.CDLL(_lib.LIB_PATH)
+    missing = [n for n in names if not hasattr(raw, n)]
+    assert not missing, missing
+    assert set(names) >= set(_lib.SIGNATURES)
+
+
+def test_defaults_are_the_pages_sizes(L):
+    p = api.default_params()
+    assert (p.heads, p.head_dim, p.index_heads, p.index_dim, p.window, p.block_size,
+            p.topk_blocks, p.topk_pos, p.compress_ratio) == (64, 512, 32, 128, 128, 8, 2048, 512, 2)
+    assert abs(p.softmax_scale - 512 ** -0.5) < 1e-8
+    assert (p.kv_format, p.win_format, p.q_format) == (api.NVFP4, api.E4M3, api.BF16)
+
+
+def test_workspace_size_covers_split_partials(L):
+    p = api.default_params()
+    assert api.sparse_attn_workspace_size(p, 0) == 0
+    assert api.sparse_attn_workspace_size(p, 32) >= 32 * 5 * 64 * 512 * 4
+
+
+def test_host_side_rejections_without_launching(L):
+    p = api.default_params()
+    pp = ctypes.byref(p)
+    assert L.csa2_compress_append(pp, -1, 1, *([None] * 11)) == 1
+    assert L.csa2_compress_append(None, 1, 1, *([None] * 11)) == 1
+    assert "params" in L.csa2_last_error().decode()
+    assert L.csa2_index_scores(pp, 1, 10, *([None] * 10)) == 1  # NULL buffers
+    bad = api.default_params(index_heads=16)
+    assert L.csa2_index_scores(ctypes.byref(bad), 1, 10, *([None] * 10)) == 4
+    bad = api.default_params(topk_pos=256)
+    assert L.csa2_select_topk(ctypes.byref(bad), 1, 10, *([None] * 7)) == 4
+    assert L.csa2_sparse_attn(pp, 1, *([None] * 8), None, 0, None, None) == 1
+    assert L.csa2_nvfp4_quantize(None, 4, 24, None, None, None) == 2  # row_len % 16
+    # nothing to do is not an error
+    assert L.csa2_compress_append(pp, 0, 1, *([None] * 11)) == 0

@@ -1,0 +1,316 @@
+"""GPU parity of each C ABI call against the CPU oracle, element by element, at
+sizes that span several tiles and ragged tails, plus edge cases.
+
+Bars: NVFP4 bytes, FP8 window bytes, index scores, block maxima and selected
+indices bit-exact; bf16 attention within max|d| <= 1.5e-2 and relative
+Frobenius error <= 4e-3 of the fp64 oracle; the fp32 (unquantised) attention
+within 1e-4 / 1e-5 (fp32 rounding of 512-term dot products)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from csa2_compressed_sparse_02_gb300 import api, synth
+from oracle import oracle as orc
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def t(x, dtype=None):
+    return torch.from_numpy(np.ascontiguousarray(x)).to(DEV) if dtype is None else \
+        torch.from_numpy(np.ascontiguousarray(x)).to(DEV, dtype)
+
+
+def close_bf16(o, e):
+    err = np.abs(o - e).max()
+    rel = np.linalg.norm(o - e) / max(np.linalg.norm(e), 1e-30)
+    return err <= 1.5e-2 and rel <= 4e-3, (err, rel)
+
+
+# --------------------------------------------------------------------------- quantiser
+def test_nvfp4_quantize_bit_exact_on_identical_fp32():
+    rng = np.random.default_rng(0)
+    x = rng.standard_normal((700, 512)) * rng.choice([1e-4, 1e-2, 1, 100, 3e4], (700, 1))
+    grid = np.array([0, .25, .5, .75, 1, 1.25, 1.5, 1.75, 2, 2.5, 3, 3.5, 4, 5, 6, 7])
+    mid = np.tile(np.concatenate([grid, -grid]), 16)[:512] * 0.375  # ties after scaling
+    special = np.stack([np.zeros(512), mid, mid * 3, np.full(512, 1e30), np.full(512, 1e-30),
+                        -np.zeros(512), np.nextafter(mid, 10), np.nextafter(mid, -10)])
+    x = np.concatenate([x, special]).astype(np.float32)
+    vals = torch.empty(x.shape[0], 256, dtype=torch.uint8, device=DEV)
+    scales = torch.empty(x.shape[0], 32, dtype=torch.uint8, device=DEV)
+    api.nvfp4_quantize(t(x), vals, scales)
+    torch.cuda.synchronize()
+    rv, rs = orc.nvfp4_quantize(x)
+    assert np.array_equal(scales.cpu().numpy(), rs)
+    gv = vals.cpu().numpy()
+    bad = np.argwhere(gv != rv)
+    assert bad.size == 0, (bad[:4], gv[tuple(bad[0])] if bad.size else None)
+
+
+# --------------------------------------------------------------------------- compressor
+def _oracle_states(kv_chunks, g_chunks, B, caps, f32):
+    st = [orc.SeqState(cap_comp=caps[b], D=512, W=128, comp_f32=f32, win_f32=f32) for b in range(B)]
+    for kv, g in zip(kv_chunks, g_chunks):
+        for b in range(B):
+            st[b].append(kv[b], g[b])
+    return st
+
+
+def _near_boundary_flip_ok(c_ref_group, gpu_vals8, gpu_scale):
+    """The GPU's bytes equal the oracle's after nudging one element by <= 4 ulp."""
+    for i in range(16):
+        for k in (1, 2, 3, 4):
+            for sgn in (1, -1):
+                y = c_ref_group.copy()
+                for _ in range(k):
+                    y[i] = np.nextafter(y[i], np.float32(sgn * np.inf))
+                v, s = orc.nvfp4_quantize(y)
+                if s[0] == gpu_scale and np.array_equal(v, gpu_vals8):
+                    return True
+    return False
+
+
+@pytest.mark.parametrize("f32", [False, True])
+def test_compress_append_matches_oracle(f32):
+    rng = np.random.default_rng(1 if f32 else 2)
+    B = 3
+    n_news = [1, 1, 2, 7, 300, 1, 129, 33]
+    total = sum(n_news)
+    caps = [total // 2 + 1] * B
+    p = api.default_params() if not f32 else api.default_params(
+        kv_format=api.F32, win_format=api.F32, q_format=api.F32)
+    cache = api.LayerCache(B, caps, p)
+    kvs, gs = [], []
+    for n in n_news:
+        kv = (rng.standard_normal((B, n, 512)) * 2).astype(np.float32)
+        g = (rng.standard_normal((B, n, 512)) * 3).astype(np.float32)
+        kvs.append(kv)
+        gs.append(g)
+        cache.append(t(kv), t(g), dev_status=None)
+    torch.cuda.synchronize()
+    st = _oracle_states(kvs, gs, B, caps, f32)
+    assert cache.n_tokens.cpu().tolist() == [total] * B
+    n_c = total // 2
+    for b in range(B):
+        assert np.array_equal(cache.pend_kv[b].cpu().numpy(), st[b].pend_kv)
+        if f32:
+            got = cache.comp[b][:n_c].cpu().numpy()
+            ref = st[b].comp_f32[:n_c]
+            ulp = np.abs(got.view(np.int32).astype(np.int64) - ref.view(np.int32).astype(np.int64))
+            assert ulp.max() <= 4, ulp.max()
+            assert np.array_equal(cache.win[b].cpu().numpy(), st[b].win_f32)
+        else:
+            assert np.array_equal(cache.win[b].cpu().numpy(), st[b].win_u8)  # E4M3 of identical fp32
+            gv = cache.comp[b][:n_c].cpu().numpy()
+            gsc = cache.comp_scales[b][:n_c].cpu().numpy()
+            rv, rsc = st[b].comp_vals[:n_c], st[b].comp_scales[:n_c]
+            bad_groups = set(map(tuple, np.argwhere(gsc != rsc)))
+            bad_groups |= set((int(j), int(c) // 8) for j, c in np.argwhere(gv != rv))
+            assert len(bad_groups) <= max(2, n_c * 32 // 2000)
+            for j, gi in bad_groups:
+                # the oracle's pooled fp32 value of this group, for the nudge test
+                kv_all = np.concatenate([k[b] for k in kvs])
+                g_all = np.concatenate([g[b] for g in gs])
+                c = np.array([orc.pool(kv_all[2 * j, d], kv_all[2 * j + 1, d], g_all[2 * j, d],
+                                       g_all[2 * j + 1, d]) for d in range(16 * gi, 16 * gi + 16)],
+                             np.float32)
+                assert _near_boundary_flip_ok(c, gv[j, 8 * gi:8 * gi + 8], gsc[j, gi]), (j, gi)
+
+
+def test_compress_capacity_overflow_sets_status_and_writes_nothing_past_cap():
+    p = api.default_params()
+    cache = api.LayerCache(1, [2], p)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    kv = torch.randn(1, 8, 512, device=DEV)
+    cache.append(kv, kv, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() & 2
+    assert cache.n_tokens.item() == 8
+
+
+# --------------------------------------------------------------------------- indexer
+def _index_case(seed, n_cs, pow2=True):
+    rng = np.random.default_rng(seed)
+    B = len(n_cs)
+    key = synth.stream_key(seed, synth.IDX_K)
+    qv = synth.e2m1_bytes(key, np.arange(B * 32 * 64, dtype=np.uint64)).reshape(B, 32, 64)
+    qs = np.full((B, 32, 8), 0x38, np.uint8)
+    w = synth.w_pow2(key ^ 7, np.arange(B * 32, dtype=np.uint64)).reshape(B, 32)
+    kvs, kss = [], []
+    for b, n in enumerate(n_cs):
+        kv = synth.e2m1_bytes(key ^ (b + 11), np.arange(max(n, 1) * 64, dtype=np.uint64)).reshape(-1, 64)
+        ks = (synth.scale_pow2_bytes(key ^ (b + 99), np.arange(max(n, 1) * 8, dtype=np.uint64))
+              if pow2 else np.full(max(n, 1) * 8, 0x38, np.uint8)).reshape(-1, 8)
+        if n > 10:  # a planted key: q head copy with scale 4
+            kv[n // 3], ks[n // 3] = qv[b, int(np.argmax(w[b]))], 0x48
+        kvs.append(kv)
+        kss.append(ks)
+    return qv, qs, w, kvs, kss, rng
+
+
+def test_index_scores_bit_exact_ragged():
+    n_cs = [1, 7, 8, 9, 255, 256, 257, 1000, 5003, 0]
+    qv, qs, w, kvs, kss, _ = _index_case(3, n_cs)
+    B = len(n_cs)
+    max_nc = max(n_cs)
+    p = api.default_params()
+    kt = [t(k) for k in kvs]
+    st = [t(s) for s in kss]
+    n_tok = t(np.array([2 * n for n in n_cs], np.int32))
+    scores = torch.full((B, max_nc), -7.0, device=DEV)
+    bmax = torch.full((B, math.ceil(max_nc / 8)), -7.0, device=DEV)
+    api.index_scores(p, max_nc, t(qv), t(qs), t(w), api.ptr_array(kt), api.ptr_array(st), n_tok,
+                     scores, bmax)
+    torch.cuda.synchronize()
+    gs, gb = scores.cpu().numpy(), bmax.cpu().numpy()
+    for b, n in enumerate(n_cs):
+        ref, inexact = orc.index_scores(qv[b], qs[b], w[b], kvs[b][:n], kss[b][:n])
+        assert inexact == 0
+        assert np.array_equal(gs[b, :n], ref), b
+        assert np.all(gs[b, n:] == -7.0)  # untouched past n_c
+        nb = math.ceil(n / 8)
+        assert np.array_equal(gb[b, :nb], orc.block_max(ref, 8)), b
+
+
+def test_index_scores_clip_and_status_when_length_exceeds_max():
+    qv, qs, w, kvs, kss, _ = _index_case(4, [100])
+    p = api.default_params()
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    scores = torch.zeros(1, 50, device=DEV)
+    bmax = torch.zeros(1, 7, device=DEV)
+    api.index_scores(p, 50, t(qv), t(qs), t(w), api.ptr_array([t(kvs[0])]),
+                     api.ptr_array([t(kss[0])]), t(np.array([200], np.int32)), scores, bmax, st)
+    torch.cuda.synchronize()
+    assert st.item() & 2
+    ref, _ = orc.index_scores(qv[0], qs[0], w[0], kvs[0][:50], kss[0][:50])
+    assert np.array_equal(scores[0].cpu().numpy(), ref)
+
+
+# --------------------------------------------------------------------------- selection
+@pytest.mark.parametrize("levels", [3, 50, 0])
+def test_select_topk_exact_with_ties(levels):
+    rng = np.random.default_rng(levels + 5)
+    n_cs = [0, 1, 5, 511, 512, 513, 4095, 16384, 16385, 20000, 70001, 524288]
+    B, max_nc = len(n_cs), max(n_cs)
+    scores = np.zeros((B, max_nc), np.float32)
+    for b, n in enumerate(n_cs):
+        if levels:
+            scores[b, :n] = rng.integers(0, levels, n).astype(np.float32) * 0.25
+        else:
+            scores[b, :n] = rng.standard_normal(n).astype(np.float32)
+        if n > 100:
+            scores[b, rng.choice(n, 16, replace=False)] = 1e4
+    nb = math.ceil(max_nc / 8)
+    bm = np.full((B, nb), -np.inf, np.float32)
+    for b, n in enumerate(n_cs):
+        pad = np.full(math.ceil(n / 8) * 8, -np.inf, np.float32)
+        pad[:n] = scores[b, :n]
+        bm[b, :len(pad) // 8] = pad.reshape(-1, 8).max(1) if n else bm[b, :0]
+    p = api.default_params()
+    idx = torch.full((B, 512), 123, dtype=torch.int32, device=DEV)
+    n_sel = torch.zeros(B, dtype=torch.int32, device=DEV)
+    api.select_topk(p, max_nc, t(scores), t(bm), t(np.array([2 * n for n in n_cs], np.int32)),
+                    idx, n_sel)
+    torch.cuda.synchronize()
+    gi, gn = idx.cpu().numpy(), n_sel.cpu().numpy()
+    for b, n in enumerate(n_cs):
+        ref, m = orc.select(scores[b, :n], 8, 2048, 512)
+        assert gn[b] == m, (b, n)
+        assert np.array_equal(gi[b], ref), (b, n, np.nonzero(gi[b] != ref)[0][:5])
+
+
+# --------------------------------------------------------------------------- attention
+def _attn_case(rng, Ts, f32, n_idx_valid):
+    B = len(Ts)
+    p = api.default_params() if not f32 else api.default_params(
+        kv_format=api.F32, win_format=api.F32, q_format=api.F32)
+    caps = [max(1, T // 2) for T in Ts]
+    cache = api.LayerCache(B, caps, p)
+    st = []
+    for b, T in enumerate(Ts):
+        kv = rng.standard_normal((T, 512)).astype(np.float32)
+        g = rng.standard_normal((T, 512)).astype(np.float32)
+        s = orc.SeqState(cap_comp=caps[b], D=512, W=128, comp_f32=f32, win_f32=f32)
+        s.append(kv, g)
+        st.append(s)
+        # the device cache gets the oracle's bytes (this test isolates attention)
+        if f32:
+            cache.comp[b].copy_(t(s.comp_f32))
+            cache.win[b].copy_(t(s.win_f32))
+        else:
+            cache.comp[b].copy_(t(s.comp_vals))
+            cache.comp_scales[b].copy_(t(s.comp_scales))
+            cache.win[b].copy_(t(s.win_u8))
+    cache.n_tokens.copy_(t(np.array(Ts, np.int32)))
+    idx = np.full((B, 512), -1, np.int32)
+    for b, T in enumerate(Ts):
+        n_c = T // 2
+        k = min(n_idx_valid, n_c)
+        if k:
+            sel = np.sort(rng.choice(n_c, k, replace=False))
+            slots = rng.choice(512, k, replace=False)  # holes anywhere
+            idx[b, slots] = sel
+    q = rng.standard_normal((B, 64, 512)).astype(np.float32)
+    if not f32:
+        qb = synth.bf16_bits_rne(q)
+        q_dev = torch.from_numpy(qb.view(np.int16)).to(DEV).view(torch.bfloat16)
+        q64 = synth.bf16_to_f64(qb)
+    else:
+        q_dev, q64 = t(q), q.astype(np.float64)
+    sink = rng.standard_normal(64).astype(np.float32)
+    return p, cache, st, idx, q_dev, q64, sink
+
+
+@pytest.mark.parametrize("f32", [False, True])
+def test_sparse_attn_matches_oracle(f32):
+    rng = np.random.default_rng(7 if f32 else 8)
+    Ts = [1, 50, 127, 128, 129, 1000, 4096, 1025]
+    valid = [512, 512, 512, 100, 512, 512, 512, 0]
+    p, cache, st, idx, q_dev, q64, sink = _attn_case(rng, Ts, f32, 512)
+    for b, v in enumerate(valid):
+        if v < 512:
+            idx[b, rng.choice(512, 512 - v, replace=False)] = -1
+    B = len(Ts)
+    out = torch.empty(B, 64, 512, dtype=torch.float32 if f32 else torch.bfloat16, device=DEV)
+    ws = torch.empty(api.sparse_attn_workspace_size(p, B), dtype=torch.uint8, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    api.sparse_attn(p, q_dev, t(sink), cache.win_ptrs, cache.n_tokens, cache.comp_ptrs,
+                    cache.comp_scale_ptrs, t(idx), out, ws, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    got = out.float().cpu().numpy().astype(np.float64)
+    for b, T in enumerate(Ts):
+        s = st[b]
+        ref, n = orc.sparse_attn(q64[b], sink.astype(np.float64), 1 / math.sqrt(512), T, 128,
+                                 win_u8=s.win_u8, win_f32=s.win_f32, comp_vals=s.comp_vals,
+                                 comp_scales=s.comp_scales, comp_f32=s.comp_f32, idx=idx[b])
+        if f32:
+            err = np.abs(got[b] - ref).max()
+            rel = np.linalg.norm(got[b] - ref) / np.linalg.norm(ref)
+            assert err <= 1e-4 and rel <= 1e-5, (b, err, rel)
+        else:
+            ok, e = close_bf16(got[b], ref)
+            assert ok, (b, T, e)
+
+
+def test_sparse_attn_out_of_range_index_is_skipped_and_flagged():
+    rng = np.random.default_rng(9)
+    p, cache, st, idx, q_dev, q64, sink = _attn_case(rng, [600], False, 200)
+    idx[0, 5] = 10_000  # beyond n_c = 300
+    out = torch.empty(1, 64, 512, dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(api.sparse_attn_workspace_size(p, 1), dtype=torch.uint8, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    api.sparse_attn(p, q_dev, t(sink), cache.win_ptrs, cache.n_tokens, cache.comp_ptrs,
+                    cache.comp_scale_ptrs, t(idx), out, ws, status)
+    torch.cuda.synchronize()
+    assert status.item() & 1
+    keep = idx[0].copy()
+    keep[5] = -1
+    s = st[0]
+    ref, _ = orc.sparse_attn(q64[0], sink.astype(np.float64), 1 / math.sqrt(512), 600, 128,
+                             win_u8=s.win_u8, comp_vals=s.comp_vals, comp_scales=s.comp_scales,
+                             idx=keep)
+    ok, e = close_bf16(out[0].float().cpu().numpy().astype(np.float64), ref)
+    assert ok, e
