@@ -1,0 +1,357 @@
+"""CSA2 decode benchmark: query-tok/s at 1M context, batch 32 (4 KV-source groups
+x 10 layers per step), with the Indexer's and the attention's HBM bandwidth
+against the measured roofline.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 3]
+
+One step = one decode token for each of the B sequences through the whole
+path of every layer: per group a Compressor append on the KV-source layer, a
+window append on the 9 layers that share its compressed cache, one Indexer
+scan over all compressed positions, one two-level selection, and 10 sparse
+attention calls (one per layer, each with its own query and window).
+Inputs are resident in HBM before timing; the per-step caches (4.8 GB of
+index keys + 19 GB of compressed KV) are far larger than L2.
+
+Prints one JSON line (rank 0). --impl reference times the CPU oracle (fp64 C)
+on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "CSA2 decode query-tok/s at 1M ctx, batch 32; indexer+attn HBM GB/s vs roofline"
+UNIT = "query-tok/s"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+
+    Q = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid=None):
+        self.uuid = uuid
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def __enter__(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                                       "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except Exception:
+                self.p.kill()
+
+    def summary(self):
+        self.f.flush()
+        rows = []
+        with open(self.f.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 10:
+                    rows.append(parts)
+        os.unlink(self.f.name)
+        mine = [r for r in rows if self.uuid and self.uuid in r[1]]
+        rows = mine or rows
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i] == "Active"})
+        loaded = [x for x in sm if x > 0.5 * (max(mx) if mx else 1)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_units(cfg, units, threads):
+    """Run the oracle on `units` (group, seq) decode units of step 0 with `threads`
+    threads; returns (unit seconds list, cores used). Inputs are regenerated before
+    the timed oracle calls; each unit times only its own oracle arithmetic."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import numpy as np
+
+    from csa2_compressed_sparse_02_gb300 import inputs as I
+    from oracle import oracle as orc
+    from oracle import reference
+
+    def one(gs):
+        g, s = gs
+        T = cfg.first_lengths()[s]
+        n_c = T // 2
+        qv, qs, w = I.host_index_q(cfg, g, s, 0)
+        kv, ks = I.host_index_keys(cfg, g, s, n_c)
+        t0 = time.perf_counter()
+        scores, _ = orc.index_scores(qv, qs, w, kv, ks)
+        orc.block_max(scores, 8)
+        idx, n_sel = orc.select(scores, 8, 2048, 512)
+        sel = [int(j) for j in idx[:n_sel]]
+        comp = reference.compressed_rows(cfg, cfg.layer(g, 0), s, sel)
+        for r in range(cfg.readers):
+            reference.attention(cfg, g, r, s, 0, sel, comp)
+        return time.perf_counter() - t0
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        secs = list(ex.map(one, units))
+    return secs, threads
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(cfg, budget_units=None):
+    threads = max(1, min(cpu_threads(), 16))
+    n = budget_units or threads
+    units = [(i % cfg.groups, (7 * i) % cfg.B) for i in range(n)]
+    secs, cores = oracle_units(cfg, units, threads)
+    per_unit = statistics.mean(secs)
+    units_per_step = cfg.B * cfg.groups
+    # `cores` units run concurrently, one per core
+    value = cfg.B * cores / (per_unit * units_per_step)
+    return {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": "%d (group, sequence) units of step 0 (Indexer over all %d compressed "
+                      "positions, selection, compressed rows of the 512 selected, %d attention "
+                      "layers), %d in parallel; mean %.2f s per unit; scaled to %d units per step"
+                      % (n, cfg.first_lengths()[0] // 2, cfg.readers, cores, per_unit,
+                         units_per_step)}
+
+
+def run_reference(args, cfg, rank):
+    if rank != 0:
+        return
+    threads = max(1, min(cpu_threads(), 8))
+    per = []
+    for _ in range(args.warmup):
+        oracle_units(cfg, [(0, 0)], 1)
+    t_all = []
+    for k in range(args.steps):
+        units = [((k + i) % cfg.groups, (7 * (k + i)) % cfg.B) for i in range(threads)]
+        t0 = time.perf_counter()
+        secs, _ = oracle_units(cfg, units, threads)
+        t_all.append(time.perf_counter() - t0)
+        per += secs
+    per_unit = statistics.mean(per)
+    value = cfg.B * threads / (per_unit * cfg.B * cfg.groups)
+    ms_per_step = 1000.0 * per_unit * cfg.B * cfg.groups / threads
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": cfg.workload, "B": cfg.B,
+                                            "T": cfg.first_lengths()[0]},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": "per step %d (group, sequence) units in parallel; "
+                                       "scaled to %d units per step" % (threads, cfg.B * cfg.groups)},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- GPU
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--nvtx", action="store_true", help="mark the timed steps with an NVTX range")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    from csa2_compressed_sparse_02_gb300.inputs import CONFIGS
+    cfg = CONFIGS[args.config]
+    if args.impl == "reference":
+        run_reference(args, cfg, rank)
+        return
+
+    import torch
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    from csa2_compressed_sparse_02_gb300 import workloads
+
+    K, Wm = args.steps, args.warmup
+    e2e_steps = 0 if args.no_e2e else K
+    run = workloads.DecodeRun(cfg, n_steps=Wm + K + e2e_steps + Wm)
+    stream = torch.cuda.current_stream()
+
+    # ---------------- device-resident timing
+    for _ in range(Wm):
+        run.step()
+    torch.cuda.synchronize()
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    ev_idx = []
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    scan_bytes = []
+    with ClockSampler(uuid) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        if args.nvtx:
+            torch.cuda.nvtx.range_push("timed")
+        start.record(stream)
+        for _ in range(K):
+            scan_bytes.append(run.scan_bytes())
+            run.step(index_events=ev_idx)
+        end.record(stream)
+        if args.nvtx:
+            torch.cuda.nvtx.range_pop()
+        torch.cuda.synchronize()
+        barrier()
+    clocks = clk.summary()
+    elapsed = start.elapsed_time(end) / 1000.0
+    if dist is not None:
+        t = torch.tensor([elapsed], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    assert int(run.dev_status.item()) == 0, "device status %d" % int(run.dev_status.item())
+    step_s = elapsed / K
+    value = world * cfg.B * K / elapsed
+
+    scan_ms = [a.elapsed_time(b) for a, b in ev_idx]
+    scan_s = statistics.mean(scan_ms) / 1000.0
+    scan_b = statistics.mean(scan_bytes)
+    hbm_peak, peak_kind = peaks()
+    achieved = scan_b / scan_s / 1e9
+    attn_b = run.attn_bytes_per_call() * cfg.readers * cfg.groups
+    step_alg_bytes = scan_b * cfg.groups + attn_b
+
+    # ---------------- end to end through the public API with host buffers
+    e2e = None
+    if e2e_steps:
+        e2e = run_e2e(run, e2e_steps, stream, barrier)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": Wm, "ms_per_step": 1000.0 * step_s, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4/e4m3/bf16 in, fp32 accumulate",
+        "data": "synthetic (seeded counter-based generator; N(0,1)-shaped latents, "
+                "uniform E2M1 index codes, 16 planted keys/seq)",
+        "config": {"workload": cfg.workload, "B": cfg.B, "T": cfg.first_lengths()[0],
+                   "groups": cfg.groups, "layers_per_group": cfg.readers,
+                   "l2": "inputs larger than L2: %.2f GB of index keys streamed per step, "
+                         "%.1f GB compressed cache" % (scan_b / 76.5 * 72 * cfg.groups / 1e9,
+                                                       scan_b / 76.5 * 288 * cfg.groups / 1e9),
+                   "parallelism": "replicas x%d (sequences sharded, no collective)" % world},
+        "roofline": {"kernel": "index_scores (Indexer scan, fused block max)", "bound": "hbm",
+                     "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None,
+                     "peak_source": peak_kind, "launch_ms": 1000.0 * scan_s,
+                     "bytes_per_launch": scan_b},
+        "path_hbm": {"algorithmic_bytes_per_step": step_alg_bytes,
+                     "achieved_gbs": step_alg_bytes / step_s / 1e9,
+                     "frac": step_alg_bytes / step_s / 1e9 / hbm_peak},
+        "gpu_launches": run.launches_per_step() * K,
+        "clocks": clocks,
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(cfg)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def run_e2e(run, K, stream, barrier):
+    """Same steps through the public API with the step's inputs copied from pinned
+    host memory and the attention outputs copied back, inside the timed region."""
+    import torch
+    host_in, dev_in, host_out, dev_out = [], [], [], []
+    for grp in run.groups:
+        for name in ("kv", "gate", "kv_rd", "q", "iq", "iw"):
+            if name in grp:
+                t = grp[name]
+                h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                h.copy_(t)
+                host_in.append(h)
+                dev_in.append(t)
+        for o in grp["out"]:
+            host_out.append(torch.empty(o.shape, dtype=o.dtype, pin_memory=True))
+            dev_out.append(o)
+    torch.cuda.synchronize()
+    n_prep = run.n_prep
+    h2d = 0
+    d2h = sum(o.numel() * o.element_size() for o in dev_out)
+    for h in host_in:
+        h2d += h[0].numel() * h.element_size()  # one step's slice
+    for _ in range(3):
+        run.step()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    start.record(stream)
+    for _ in range(K):
+        k = run.step_done % n_prep
+        for h, d in zip(host_in, dev_in):
+            d[k].copy_(h[k], non_blocking=True)
+        run.step()
+        for h, d in zip(host_out, dev_out):
+            h.copy_(d, non_blocking=True)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    el = start.elapsed_time(end) / 1000.0
+    return {"value": run.cfg.B * K / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h}
+
+
+if __name__ == "__main__":
+    main()

@@ -69,6 +69,10 @@ CONFIGS = {
     3: DecodeConfig(3, "decode B=32 T=1048576 NVFP4, 4 KV-source groups x 10 layers", B=32,
                     groups=4, readers=10, steps=1, quant=True, plants=16, kscale_pow2=True,
                     T=1048576),
+    # a profiling size of the decode step: index keys (151 MB) still larger than L2
+    6: DecodeConfig(6, "decode B=32 T=131072 NVFP4, 1 group x 2 layers (profiling size)", B=32,
+                    groups=1, readers=2, steps=1, quant=True, plants=16, kscale_pow2=True,
+                    T=131072),
     5: DecodeConfig(5, "decode B=32 ragged T in [4096, 1048576], 1 index source + 5 readers, "
                        "16 steps", B=32, groups=1, readers=6, steps=16, quant=True, plants=16,
                     kscale_pow2=True),

@@ -15,10 +15,15 @@ from .inputs import CONFIGS, D, DI, H, HI, W, DecodeConfig, plants  # noqa: F401
 # =============================================================================== device side
 @dataclass
 class DecodeRun:
-    """Device state of one decode configuration, ready to run `n_steps` steps."""
+    """Device state of one decode configuration, ready to run `n_steps` steps.
+
+    Per-step inputs (new tokens, queries, index queries) are generated for
+    min(n_steps, max_prepared) steps and reused cyclically beyond that; the
+    caches always advance by one token per step."""
     cfg: DecodeConfig
     n_steps: int
     device: str = "cuda"
+    max_prepared: int = 64
     step_done: int = 0
     groups: list = field(default_factory=list)
 
@@ -30,6 +35,7 @@ class DecodeRun:
         cfg, dev = self.cfg, self.device
         self.T0 = cfg.first_lengths()
         self.B = cfg.B
+        self.n_prep = max(1, min(self.n_steps, self.max_prepared))
         if cfg.quant:
             self.params = api.default_params()
         else:
@@ -59,16 +65,16 @@ class DecodeRun:
             grp["out"] = [torch.empty(self.B, H, D, dtype=qdt, device=dev) for _ in range(cfg.readers)]
             grp["sink"] = [torch.empty(H, dtype=torch.float32, device=dev) for _ in range(cfg.readers)]
             # per-step inputs, resident before timing
-            grp["kv"] = torch.empty(self.n_steps, self.B, 1, D, dtype=torch.float32, device=dev)
-            grp["gate"] = torch.empty(self.n_steps, self.B, 1, D, dtype=torch.float32, device=dev)
+            grp["kv"] = torch.empty(self.n_prep, self.B, 1, D, dtype=torch.float32, device=dev)
+            grp["gate"] = torch.empty(self.n_prep, self.B, 1, D, dtype=torch.float32, device=dev)
             if cfg.readers > 1:
-                grp["kv_rd"] = torch.empty(self.n_steps, self.B * (cfg.readers - 1), 1, D,
+                grp["kv_rd"] = torch.empty(self.n_prep, self.B * (cfg.readers - 1), 1, D,
                                            dtype=torch.float32, device=dev)
-            grp["q"] = torch.empty(self.n_steps, cfg.readers, self.B, H, D, dtype=qdt, device=dev)
-            grp["iq"] = torch.empty(self.n_steps, self.B, HI, DI // 2, dtype=torch.uint8, device=dev)
-            grp["iqs"] = torch.full((self.n_steps, self.B, HI, DI // 16), synth.E4M3_ONE,
+            grp["q"] = torch.empty(self.n_prep, cfg.readers, self.B, H, D, dtype=qdt, device=dev)
+            grp["iq"] = torch.empty(self.n_prep, self.B, HI, DI // 2, dtype=torch.uint8, device=dev)
+            grp["iqs"] = torch.full((self.n_prep, self.B, HI, DI // 16), synth.E4M3_ONE,
                                     dtype=torch.uint8, device=dev)
-            grp["iw"] = torch.empty(self.n_steps, self.B, HI, dtype=torch.float32, device=dev)
+            grp["iw"] = torch.empty(self.n_prep, self.B, HI, dtype=torch.float32, device=dev)
             self.groups.append(grp)
         self._fill()
 
@@ -155,7 +161,7 @@ class DecodeRun:
                 synth.gpu_fill(synth.G_NORMAL_F32, [synth.stream_key(cfg.seed, synth.SINK, lay, 0)],
                                0, H, grp["sink"][r])
             qkind = synth.G_NORMAL_BF16 if cfg.quant else synth.G_NORMAL_F32
-            for k in range(self.n_steps):
+            for k in range(self.n_prep):
                 for seqs in self._seq_sets():
                     tok = self.T0[seqs[0]] - 1 + k  # raw position of this step's token
                     s0, nb = seqs[0], len(seqs)
@@ -183,19 +189,30 @@ class DecodeRun:
         torch.cuda.synchronize()
 
     # ------------------------------------------------------------------ one step
-    def step(self, stream=None):
-        """Enqueue one decode step (every group, every layer) on `stream`."""
-        api, cfg, k = self.api, self.cfg, self.step_done
-        assert k < self.n_steps, "more steps than prepared"
+    def step(self, stream=None, index_events=None):
+        """Enqueue one decode step (every group, every layer) on `stream`.
+        index_events: optional list receiving (start, end) CUDA events recorded
+        around each Indexer launch on the same stream."""
+        api, cfg = self.api, self.cfg
+        assert self.step_done < self.n_steps, "more steps than the caches were sized for"
+        k = self.step_done % self.n_prep
         p = self.params
+        torch = self.torch
+        st = torch.cuda.current_stream() if stream is None else stream
         for grp in self.groups:
             src = grp["src"]
             src.append(grp["kv"][k], grp["gate"][k], self.dev_status, stream)
             if cfg.readers > 1:
                 grp["rd"].append(grp["kv_rd"][k], None, self.dev_status, stream)
+            if index_events is not None:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
             api.index_scores(p, self.max_ncomp, grp["iq"][k], grp["iqs"][k], grp["iw"][k],
                              grp["keys"].val_ptrs, grp["keys"].scale_ptrs, src.n_tokens,
                              grp["scores"], grp["bmax"], self.dev_status, stream)
+            if index_events is not None:
+                e1.record(st)
+                index_events.append((e0, e1))
             api.select_topk(p, self.max_ncomp, grp["scores"], grp["bmax"], src.n_tokens,
                             grp["idx"], grp["n_sel"], self.dev_status, stream)
             for r in range(cfg.readers):
@@ -211,6 +228,29 @@ class DecodeRun:
 
     def tokens_after(self, s: int) -> int:
         return self.T0[s] - 1 + self.step_done
+
+    def launches_per_step(self) -> int:
+        """Kernels of this library one step launches (see step())."""
+        n = 0
+        for _ in self.groups:
+            n += 1 + (1 if self.cfg.readers > 1 else 0)   # compress / window appends
+            n += 1 + 1                                    # Indexer, selection
+            n += 2 * self.cfg.readers                      # attention split pass + merge
+        return n
+
+    def scan_bytes(self) -> float:
+        """Algorithmic bytes of one Indexer launch at the current step: 72 B of
+        key read + 4 B score + 0.5 B block max written per position."""
+        return sum((T - 1 + self.step_done) // 2 for T in self.T0) * 76.5
+
+    def attn_bytes_per_call(self) -> float:
+        """Algorithmic bytes of one sparse-attention call: per sequence the
+        window (128 x 512 B), the selected rows (512 x 288 B), q and out
+        (64 x 512 x 2 B each) and idx (512 x 4 B)."""
+        per = 128 * 512 + 512 * 288 + 2 * 64 * 512 * 2 + 512 * 4
+        if not self.cfg.quant:
+            per = 128 * 2048 + 512 * 2048 + 2 * 64 * 512 * 4 + 512 * 4
+        return per * self.B
 
 
 class _CacheView:
