@@ -102,6 +102,19 @@ def sparse_attn(params, q, sink, win_ptrs, n_tokens, comp_ptrs, comp_scale_ptrs,
         "sparse_attn")
 
 
+def sparse_attn_noalloc(params, q, sink, win_ptrs, n_tokens, comp_ptrs, comp_scale_ptrs, idx, out,
+                        dev_status=None, stream=None):
+    """csa2_sparse_attn without a workspace: for callers that cannot allocate device
+    memory (their HBM already belongs to an engine's pool, or an allocation would
+    synchronise a latency-critical path). At most 32 sequences per call; calls that
+    overlap on the GPU share the library's one scratch array and must be ordered."""
+    B = n_tokens.numel()
+    check(lib().csa2_sparse_attn_noalloc(
+        ctypes.byref(params), B, _ptr(q), _ptr(sink), _ptr(win_ptrs), _ptr(n_tokens),
+        _ptr(comp_ptrs), _ptr(comp_scale_ptrs), _ptr(idx), _ptr(out), _ptr(dev_status),
+        _stream(stream)), "sparse_attn_noalloc")
+
+
 # --------------------------------------------------------------------------- buffers
 @dataclass
 class LayerCache:

@@ -493,3 +493,56 @@ extern "C" int csa2_sparse_attn(const csa2_params* p, int B, const void* q, cons
     }
     return check_launch("sparse_attn");
 }
+
+// ---------------------------------------------------------------------------
+// No-allocation variant. Its split-KV scratch lives in this file-scope device
+// array, so the caller passes no workspace. Some callers cannot allocate device
+// memory at all: a serving engine that has already handed the free HBM to its
+// own pool (the KV cache is sized to fill it), or a latency-critical path where
+// a cudaMalloc/cudaFree would synchronise the device. The array holds the
+// partial outputs of at most kNoAllocMaxBatch sequences (the pages' serving
+// batch, max-num-seqs 32): 32 x 657,920 B = 21,053,440 B, held by every GPU that
+// loads the library until the process exits.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace {
+constexpr int kNoAllocMaxBatch = 32;
+constexpr size_t kNoAllocScratchBytes =
+    (size_t)kNoAllocMaxBatch * csa2::kSplits * csa2::kH * (csa2::kD * sizeof(float) + sizeof(float2));
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+}  // namespace
+
+static __device__ __align__(256) unsigned char g_sparse_attn_scratch[kNoAllocScratchBytes];
+
+extern "C" int csa2_sparse_attn_noalloc(const csa2_params* p, int B, const void* q,
+                                        const float* sink, const void* const* win,
+                                        const int32_t* n_tokens, const void* const* comp,
+                                        const uint8_t* const* comp_scales, const int32_t* idx,
+                                        void* out, int32_t* dev_status, void* stream) {
+    if (B > kNoAllocMaxBatch)
+        return fail(CSA2_ERR_UNSUPPORTED,
+                    "sparse_attn_noalloc: at most 32 sequences per call (the built-in scratch "
+                    "holds 32); split the batch or use csa2_sparse_attn with a workspace");
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return check_launch("sparse_attn_noalloc: current device");
+    void* scratch = nullptr;
+    {
+        // once per device, with that device current: the device address of the array
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        if (!g_noalloc_ptr[dev]) {
+            void* ptr = nullptr;
+            const cudaError_t e = cudaGetSymbolAddress(&ptr, g_sparse_attn_scratch);
+            if (e != cudaSuccess || !ptr)
+                return fail(CSA2_ERR_CUDA, std::string("sparse_attn_noalloc: scratch address: ") +
+                                               cudaGetErrorString(e));
+            g_noalloc_ptr[dev] = ptr;
+        }
+        scratch = g_noalloc_ptr[dev];
+    }
+    return csa2_sparse_attn(p, B, q, sink, win, n_tokens, comp, comp_scales, idx, out, scratch,
+                            kNoAllocScratchBytes, dev_status, stream);
+}

@@ -203,6 +203,33 @@ int csa2_sparse_attn(const csa2_params* p, int B,
                      void* workspace, size_t ws_bytes,
                      int32_t* dev_status, void* stream);
 
+/*
+ * csa2_sparse_attn_noalloc — csa2_sparse_attn without a caller workspace.
+ * (No counterpart in the pages: an addition for callers that cannot allocate.)
+ *
+ * Some callers cannot allocate device memory: a serving engine that has already
+ * given the free HBM to its own pool (the KV cache is sized to fill it), or a
+ * latency-critical path where cudaMalloc/cudaFree would synchronise the device.
+ * This entry point allocates nothing: its scratch is a fixed array inside the
+ * library (21,053,440 bytes, enough for 32 sequences), held on every GPU that
+ * loads the library until the process exits. Arguments and results are those
+ * of csa2_sparse_attn, minus workspace/ws_bytes.
+ *   - B > 32 returns CSA2_ERR_UNSUPPORTED (nothing enqueued): split the batch.
+ *   - The first call on a device looks up the array's device address (with that
+ *     device current) and caches it; make that first call before any stream
+ *     capture.
+ *   - Every call on a device shares the one array, which keeps the last call's
+ *     contents (nothing in it needs clearing between calls). Calls whose kernels
+ *     overlap on the GPU (different streams, no ordering between them) race on
+ *     it: order them on one stream or with events.
+ */
+int csa2_sparse_attn_noalloc(const csa2_params* p, int B,
+                             const void* q, const float* sink,
+                             const void* const* win, const int32_t* n_tokens,
+                             const void* const* comp, const uint8_t* const* comp_scales,
+                             const int32_t* idx, void* out,
+                             int32_t* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
