@@ -21,6 +21,7 @@ from ._lib import Csa2Error, Params, check, lib  # noqa: F401
 
 F32, NVFP4, E4M3, BF16 = 0, 1, 2, 3
 D, H, HI, DI, W, BLK, KB, KP = 512, 64, 32, 128, 128, 8, 2048, 512
+KEY_TILE, KEY_TILE_BYTES = 128, 9216
 
 
 def default_params(**over) -> Params:
@@ -71,13 +72,21 @@ def nvfp4_quantize(x, vals, scales, stream=None):
                                     _ptr(scales), _stream(stream)), "nvfp4_quantize")
 
 
-def index_scores(params, max_ncomp, q_vals, q_scales, w, key_val_ptrs, key_scale_ptrs, n_tokens,
-                 scores, block_max, dev_status=None, stream=None):
+def index_keys_write(params, vals, scales, pos0, dst_ptrs, cap, dev_status=None, stream=None):
+    """Plain NVFP4 index keys vals [B, n, 64] / scales [B, n, 8] -> tiled caches."""
+    B, n = vals.shape[0], vals.shape[1]
+    check(lib().csa2_index_keys_write(
+        ctypes.byref(params), B, n, _ptr(vals), _ptr(scales), _ptr(pos0), _ptr(dst_ptrs),
+        _ptr(cap), _ptr(dev_status), _stream(stream)), "index_keys_write")
+
+
+def index_scores(params, max_ncomp, q_vals, q_scales, w, key_cache_ptrs, n_tokens, scores,
+                 block_max, dev_status=None, stream=None, cuda_cores=False):
     B = n_tokens.numel()
-    check(lib().csa2_index_scores(
-        ctypes.byref(params), B, max_ncomp, _ptr(q_vals), _ptr(q_scales), _ptr(w),
-        _ptr(key_val_ptrs), _ptr(key_scale_ptrs), _ptr(n_tokens), _ptr(scores), _ptr(block_max),
-        _ptr(dev_status), _stream(stream)), "index_scores")
+    f = lib().csa2_index_scores_cuda_cores if cuda_cores else lib().csa2_index_scores
+    check(f(ctypes.byref(params), B, max_ncomp, _ptr(q_vals), _ptr(q_scales), _ptr(w),
+            _ptr(key_cache_ptrs), _ptr(n_tokens), _ptr(scores), _ptr(block_max), _ptr(dev_status),
+            _stream(stream)), "index_scores")
 
 
 def select_topk(params, max_ncomp, scores, block_max, n_tokens, idx, n_sel=None, dev_status=None,
@@ -164,17 +173,28 @@ class LayerCache:
 
 @dataclass
 class IndexKeyCache:
-    """Per-sequence FP4 index keys: values [cap, 64] and E4M3 scales [cap, 8]."""
+    """Per-sequence tiled FP4 index-key caches (include/csa2.h layout): ceil(cap/128)
+    tiles of 9216 bytes each."""
     caps: list
     device: str = "cuda"
 
     def __post_init__(self):
-        self.vals = [torch.zeros(max(1, int(c)), DI // 2, dtype=torch.uint8, device=self.device)
-                     for c in self.caps]
-        self.scales = [torch.zeros(max(1, int(c)), DI // 16, dtype=torch.uint8, device=self.device)
-                       for c in self.caps]
-        self.val_ptrs = ptr_array(self.vals)
-        self.scale_ptrs = ptr_array(self.scales)
+        self.tiles = [max(1, -(-int(c) // KEY_TILE)) for c in self.caps]
+        self.buf = [torch.zeros(t * KEY_TILE_BYTES, dtype=torch.uint8, device=self.device)
+                    for t in self.tiles]
+        self.ptrs = ptr_array(self.buf)
+        self.cap = torch.tensor([t * KEY_TILE for t in self.tiles], dtype=torch.int64,
+                                device=self.device)
+
+    def write(self, params, vals, scales, pos0, dev_status=None, stream=None):
+        """Write plain rows vals [B, n, 64], scales [B, n, 8] at positions pos0[b]..."""
+        index_keys_write(params, vals, scales, pos0, self.ptrs, self.cap, dev_status, stream)
+
+    def write_seq(self, params, b, vals, scales, pos0=0, dev_status=None, stream=None):
+        """Write plain rows [n, 64] / [n, 8] of one sequence starting at pos0."""
+        p0 = torch.tensor([pos0], dtype=torch.int64, device=self.device)
+        index_keys_write(params, vals[None], scales[None], p0, self.ptrs[b:b + 1],
+                         self.cap[b:b + 1], dev_status, stream)
 
 
 def n_blocks(n: int) -> int:

@@ -1,34 +1,89 @@
-// Decode Indexer with fused block maximum.
+// Decode Indexer with fused block maximum, and the writer of its key cache.
 // "DeepSeek-V4.1-Flash-NVFP4" §3.3: 32 FP4 index query heads score the shared
 // FP4 index key; ReLU, per-head weights, sum; blocks of 8 positions are scored
 // by their best position.
 //
-// CUDA-core build: one thread per key, 32 fp32 accumulators (one per head),
-// the query decoded once per CTA into shared memory as [dim][head] so that a
-// warp reads it by broadcast. Exact for the inputs the header describes
-// (every partial sum representable), so the fp32 result does not depend on
-// the order of the adds.
+// Key cache: tiles of 128 positions, each the 9216-byte shared-memory image the
+// tensor cores read (8 KB of E2M1 codes, K-major with the 64-byte swizzle, then
+// 1 KB of E4M3 group scales in the scale-factor order of block-scaled MMA; the
+// exact formulas are in include/csa2.h). One bulk copy moves one tile.
+//
+// Tensor-core build (k_index_scores_tc): per 128-position tile, D[128 x 32] =
+// K[128 x 128] . Q[32 x 128]^T as two tcgen05 block-scaled FP4 MMAs (K = 64 each,
+// UE4M3 scale per 16 elements) into TMEM; the epilogue warps read one position
+// per lane (32 heads), apply ReLU and the head weights, and reduce the block
+// maximum over 8 adjacent lanes. One persistent CTA per SM; warps 0-3 epilogue,
+// warp 4 loads (bulk copies into a 12-stage ring), warp 5 issues the MMAs;
+// accumulators double-buffered in TMEM so the epilogue of tile i overlaps the
+// MMAs of tile i+1.
+//
+// CUDA-core build (k_index_scores_cc): one thread per position, 32 fp32
+// accumulators, the query decoded once per CTA into shared memory.
 #include "common.cuh"
+#include "sm100.cuh"
+
+#include <algorithm>
 
 namespace csa2 {
 namespace {
 
+constexpr int kKeyTile = CSA2_KEY_TILE;            // 128 positions
+constexpr int kKeyTileBytes = CSA2_KEY_TILE_BYTES;  // 9216
+constexpr int kKeyValBytes = kKeyTile * (kDi / 2);  // 8192
+
+// byte offset, inside a tile, of 16-byte chunk c (dims 32c..32c+31) of position m
+__device__ __forceinline__ int key_val_off(int m, int c) { return m * 64 + ((c ^ ((m >> 1) & 3)) << 4); }
+// byte offset, inside a tile, of the 4 scales of groups 4h..4h+3 of position m
+__device__ __forceinline__ int key_scale_off(int m, int h) {
+    return kKeyValBytes + h * 512 + (m & 31) * 16 + (m >> 5) * 4;
+}
+
+__device__ __forceinline__ int64_t seq_ncomp(const int32_t* n_tokens, int b, int ratio,
+                                            int64_t max_ncomp, int32_t* dev_status, bool report) {
+    int64_t n_c = n_tokens[b] / ratio;
+    if (n_c > max_ncomp || n_c < 0) {
+        if (report) raise_status(dev_status, CSA2_DEV_BAD_LENGTH);
+        n_c = n_c < 0 ? 0 : max_ncomp;
+    }
+    return n_c;
+}
+
+// ------------------------------------------------------------------ key writer
+__global__ void __launch_bounds__(256)
+k_index_keys_write(int B, int64_t n, const uint8_t* __restrict__ vals,
+                   const uint8_t* __restrict__ scales, const int64_t* __restrict__ pos0,
+                   uint8_t* const* dst, const int64_t* __restrict__ cap, int32_t* dev_status) {
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= (int64_t)B * n) return;
+    const int b = (int)(e / n);
+    const int64_t t = pos0[b] + (e - (int64_t)b * n);
+    if (t < 0 || t >= cap[b]) {
+        raise_status(dev_status, CSA2_DEV_BAD_LENGTH);
+        return;
+    }
+    const uint4* src = reinterpret_cast<const uint4*>(vals + e * (kDi / 2));
+    uint8_t* tile = dst[b] + (t / kKeyTile) * kKeyTileBytes;
+    const int m = (int)(t % kKeyTile);
+#pragma unroll
+    for (int c = 0; c < 4; ++c) *reinterpret_cast<uint4*>(tile + key_val_off(m, c)) = src[c];
+    const uint2 sc = *reinterpret_cast<const uint2*>(scales + e * (kDi / kGroup));
+    *reinterpret_cast<uint32_t*>(tile + key_scale_off(m, 0)) = sc.x;
+    *reinterpret_cast<uint32_t*>(tile + key_scale_off(m, 1)) = sc.y;
+}
+
+// ------------------------------------------------------------------ CUDA-core build
 constexpr int kKeysPerCta = 256;
 
 __global__ void __launch_bounds__(kKeysPerCta)
 k_index_scores_cc(int64_t max_ncomp, int ratio, const uint8_t* __restrict__ q_vals,
                   const uint8_t* __restrict__ q_scales, const float* __restrict__ w,
-                  const uint8_t* const* key_vals, const uint8_t* const* key_scales,
-                  const int32_t* __restrict__ n_tokens, float* scores, float* block_max,
-                  int32_t* dev_status) {
+                  const uint8_t* const* key_cache, const int32_t* __restrict__ n_tokens,
+                  float* scores, float* block_max, int32_t* dev_status) {
     __shared__ float4 sq[kDi][kHi / 4];  // sq[d][h/4] = q[h..h+3][d]
     __shared__ float sw[kHi];
     const int b = blockIdx.y, tid = threadIdx.x;
-    int64_t n_c = n_tokens[b] / ratio;
-    if (n_c > max_ncomp || n_c < 0) {
-        if (tid == 0 && blockIdx.x == 0) raise_status(dev_status, CSA2_DEV_BAD_LENGTH);
-        n_c = n_c < 0 ? 0 : max_ncomp;
-    }
+    const int64_t n_c = seq_ncomp(n_tokens, b, ratio, max_ncomp, dev_status,
+                                  tid == 0 && blockIdx.x == 0);
     const int64_t t0 = (int64_t)blockIdx.x * kKeysPerCta;
     if (t0 >= n_c) return;
 
@@ -51,12 +106,13 @@ k_index_scores_cc(int64_t max_ncomp, int ratio, const uint8_t* __restrict__ q_va
 #pragma unroll
     for (int h = 0; h < kHi; ++h) acc[h] = 0.0f;
     if (valid) {
-        const uint4* kp = reinterpret_cast<const uint4*>(key_vals[b] + t * (kDi / 2));
-        const uint2 ks = *reinterpret_cast<const uint2*>(key_scales[b] + t * (kDi / kGroup));
-        const uint32_t sc[2] = {ks.x, ks.y};
+        const uint8_t* tile = key_cache[b] + (t / kKeyTile) * kKeyTileBytes;
+        const int m = (int)(t % kKeyTile);
+        const uint32_t sc[2] = {*reinterpret_cast<const uint32_t*>(tile + key_scale_off(m, 0)),
+                                *reinterpret_cast<const uint32_t*>(tile + key_scale_off(m, 1))};
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {  // 16 bytes = 32 dims = 2 groups
-            const uint4 kb = kp[q4];
+            const uint4 kb = *reinterpret_cast<const uint4*>(tile + key_val_off(m, q4));
             const uint32_t words[4] = {kb.x, kb.y, kb.z, kb.w};
 #pragma unroll
             for (int wi = 0; wi < 4; ++wi) {
@@ -92,12 +148,272 @@ k_index_scores_cc(int64_t max_ncomp, int ratio, const uint8_t* __restrict__ q_va
 #pragma unroll
     for (int h = 0; h < kHi; ++h) s = __fmaf_rn(sw[h], acc[h] > 0.0f ? acc[h] : 0.0f, s);
     if (valid) scores[(int64_t)b * max_ncomp + t] = s;
-    float m = valid ? s : -INFINITY;
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 4));
+    float mx = valid ? s : -INFINITY;
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
     if (valid && (tid & (kBlk - 1)) == 0)
-        block_max[(int64_t)b * ((max_ncomp + kBlk - 1) / kBlk) + t / kBlk] = m;
+        block_max[(int64_t)b * ((max_ncomp + kBlk - 1) / kBlk) + t / kBlk] = mx;
+}
+
+// ------------------------------------------------------------------ tensor-core build
+constexpr int kStages = 12;
+constexpr int kTcThreads = 192;  // warps 0-3 epilogue, 4 loader, 5 MMA
+constexpr int kMaxSeq = 1024;
+constexpr uint32_t kTmemCols = 128;
+constexpr uint32_t kColD = 0, kColSFA = 64, kColSFB = 80;  // D[2] x 32, SFA[2] x 8, SFB[2] x 8
+// Instruction descriptor: kind::mxf4nvf4, A and B E2M1 (1), K-major, dense,
+// N = 32 (N>>3 in bits 17..22), UE4M3 scales (bit 23 = 0), M = 128 (M>>4 in bits 24..28).
+constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((32u >> 3) << 17) | ((128u >> 4) << 24);
+
+struct TcShared {
+    uint8_t stage[kStages][kKeyTileBytes];  // 9216 = 9 x 1024: every stage 1024-aligned
+    uint8_t q[2][kHi * (kDi / 2)];          // B operand (32 heads x 64 B, 64-byte swizzle), 2 slots
+    uint8_t sfb[2][1024];                   // B scale factors, two 512-byte atoms per slot
+    uint64_t full[kStages], empty[kStages];
+    uint64_t qfull[2], qempty[2], accf[2], acce[2], done;
+    uint32_t tmem_base;
+    int abort;
+    int32_t prefix[kMaxSeq + 1];  // tiles of sequences < b
+    int32_t ncomp[kMaxSeq];
+};
+
+// position of flat tile f: advance b while f is past sequence b's tiles
+__device__ __forceinline__ int advance_seq(const TcShared& sh, int b, int64_t f) {
+    while (f >= sh.prefix[b + 1]) ++b;
+    return b;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict__ q_vals,
+                  const uint8_t* __restrict__ q_scales, const float* __restrict__ w,
+                  const uint8_t* const* key_cache, const int32_t* __restrict__ n_tokens,
+                  float* scores, float* block_max, int32_t* dev_status) {
+    using namespace sm100;
+    extern __shared__ uint8_t smem_raw[];
+    TcShared& sh = *reinterpret_cast<TcShared*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    volatile int* abort = &sh.abort;
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sh.full[s], 1);
+            mbar_init(&sh.empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sh.qfull[i], 1);
+            mbar_init(&sh.qempty[i], 1);
+            mbar_init(&sh.accf[i], 1);
+            mbar_init(&sh.acce[i], 4);
+        }
+        mbar_init(&sh.done, 1);
+        sh.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {  // per-sequence compressed lengths and tile prefix
+        int32_t run = 0;
+        const int per = (B + 31) / 32;
+        const int b0 = min(B, lane * per), b1 = min(B, b0 + per);
+        int32_t local = 0;
+        for (int b = b0; b < b1; ++b) {
+            const int64_t n_c = seq_ncomp(n_tokens, b, ratio, max_ncomp, dev_status,
+                                          blockIdx.x == 0);
+            sh.ncomp[b] = (int32_t)n_c;
+            local += (int32_t)((n_c + kKeyTile - 1) / kKeyTile);
+        }
+        int32_t incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t u = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        run = incl - local;
+        for (int b = b0; b < b1; ++b) {
+            sh.prefix[b] = run;
+            run += (sh.ncomp[b] + kKeyTile - 1) / kKeyTile;
+        }
+        if (lane == 31) sh.prefix[B] = incl;
+    }
+    if (warp == 5) {
+        tmem_alloc(&sh.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+    const int64_t total = sh.prefix[B];
+    const int64_t f0 = total * blockIdx.x / gridDim.x;
+    const int64_t f1 = total * (blockIdx.x + 1) / gridDim.x;
+
+    if (warp == 4) {
+        // ---------------- loader: query slots per sequence, key tiles per stage
+        int seg = -1, b = 0, prev_b = -1;
+        int64_t issued = 0;
+        for (int64_t f = f0; f < f1; ++f) {
+            b = advance_seq(sh, b, f);
+            const int64_t tile = f - sh.prefix[b];
+            if (b != prev_b) {
+                ++seg;
+                const int qs = seg & 1;
+                if (!mbar_wait(&sh.qempty[qs], ((seg >> 1) & 1) ^ 1, abort)) break;
+                // lane h writes head h: 64 B of codes in the swizzled K-major image,
+                // its 8 scales into the two scale-factor atoms (row h, bytes 0..3)
+                const uint4* src = reinterpret_cast<const uint4*>(
+                    q_vals + ((int64_t)b * kHi + lane) * (kDi / 2));
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<uint4*>(&sh.q[qs][lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)]) = src[c];
+                const uint2 sc = *reinterpret_cast<const uint2*>(
+                    q_scales + ((int64_t)b * kHi + lane) * (kDi / kGroup));
+                *reinterpret_cast<uint4*>(&sh.sfb[qs][lane * 16]) = make_uint4(sc.x, 0u, 0u, 0u);
+                *reinterpret_cast<uint4*>(&sh.sfb[qs][512 + lane * 16]) = make_uint4(sc.y, 0u, 0u, 0u);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.qfull[qs]);
+                prev_b = b;
+            }
+            const int64_t i = f - f0;
+            const int s = (int)(i % kStages);
+            if (!mbar_wait(&sh.empty[s], (uint32_t)((i / kStages) & 1) ^ 1, abort)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&sh.full[s], kKeyTileBytes);
+                bulk_g2s(sh.stage[s], key_cache[b] + tile * kKeyTileBytes, kKeyTileBytes, &sh.full[s]);
+            }
+            __syncwarp();
+            issued = i + 1;
+        }
+        // copies still in flight land before the CTA can exit
+        for (int64_t j = issued > kStages ? issued - kStages : 0; j < issued; ++j) {
+            for (uint32_t k = 0; k < kSpinLimit; ++k)
+                if (mbar_try_wait(&sh.full[j % kStages], (uint32_t)((j / kStages) & 1))) break;
+        }
+    } else if (warp == 5) {
+        // ---------------- MMA issuer (one thread)
+        if (lane == 0) {
+            int seg = -1, b = 0, prev_b = -1;
+            for (int64_t f = f0; f < f1; ++f) {
+                b = advance_seq(sh, b, f);
+                const int64_t i = f - f0;
+                const int s = (int)(i % kStages), a = (int)(i & 1);
+                if (!mbar_wait(&sh.full[s], (uint32_t)((i / kStages) & 1), abort)) break;
+                if (!mbar_wait(&sh.acce[a], (uint32_t)((i >> 1) & 1) ^ 1, abort)) break;
+                tc_fence_after();
+                if (b != prev_b) {
+                    if (seg >= 0) tc_commit(&sh.qempty[seg & 1]);
+                    ++seg;
+                    const int qs = seg & 1;
+                    if (!mbar_wait(&sh.qfull[qs], (uint32_t)((seg >> 1) & 1), abort)) break;
+                    tc_fence_after();
+                    const uint32_t sfb = smem_u32(sh.sfb[qs]);
+                    tmem_cp_32x128b_x4(tmem + kColSFB + 8 * qs, smem_desc(sfb, 128, 128, kLayoutNone));
+                    tmem_cp_32x128b_x4(tmem + kColSFB + 8 * qs + 4,
+                                       smem_desc(sfb + 512, 128, 128, kLayoutNone));
+                    prev_b = b;
+                }
+                const int qs = seg & 1;
+                const uint32_t st = smem_u32(sh.stage[s]);
+                const uint32_t qa = smem_u32(sh.q[qs]);
+                tmem_cp_32x128b_x4(tmem + kColSFA + 8 * a,
+                                   smem_desc(st + kKeyValBytes, 128, 128, kLayoutNone));
+                tmem_cp_32x128b_x4(tmem + kColSFA + 8 * a + 4,
+                                   smem_desc(st + kKeyValBytes + 512, 128, 128, kLayoutNone));
+                const uint32_t d = tmem + kColD + 32 * a;
+                mma_mxf4nvf4(d, smem_desc(st, 16, 512, kLayoutSw64), smem_desc(qa, 16, 512, kLayoutSw64),
+                             kIdesc, tmem + kColSFA + 8 * a, tmem + kColSFB + 8 * qs, 0);
+                mma_mxf4nvf4(d, smem_desc(st + 32, 16, 512, kLayoutSw64),
+                             smem_desc(qa + 32, 16, 512, kLayoutSw64), kIdesc,
+                             tmem + kColSFA + 8 * a + 4, tmem + kColSFB + 8 * qs + 4, 1);
+                tc_commit(&sh.empty[s]);
+                tc_commit(&sh.accf[a]);
+            }
+            // every MMA and copy issued above has completed before TMEM is freed
+            tc_commit(&sh.done);
+            for (uint32_t k = 0; k < kSpinLimit; ++k)
+                if (mbar_try_wait(&sh.done, 0)) break;
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue: warp q owns TMEM lanes 32q..32q+31 = positions of the tile
+        const int64_t ld_bm = (max_ncomp + kBlk - 1) / kBlk;
+        int b = 0, prev_b = -1;
+        float wv[kHi];
+        for (int64_t f = f0; f < f1; ++f) {
+            b = advance_seq(sh, b, f);
+            const int64_t i = f - f0;
+            const int a = (int)(i & 1);
+            if (b != prev_b) {
+                const float4* w4 = reinterpret_cast<const float4*>(w + (int64_t)b * kHi);
+#pragma unroll
+                for (int h4 = 0; h4 < kHi / 4; ++h4) {
+                    const float4 v = w4[h4];
+                    wv[4 * h4] = v.x;
+                    wv[4 * h4 + 1] = v.y;
+                    wv[4 * h4 + 2] = v.z;
+                    wv[4 * h4 + 3] = v.w;
+                }
+                prev_b = b;
+            }
+            if (!mbar_wait(&sh.accf[a], (uint32_t)((i >> 1) & 1), abort)) break;
+            tc_fence_after();
+            uint32_t r[kHi];
+            tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * warp) << 16) + kColD + 32 * a, r);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.acce[a]);
+            float s = 0.0f;
+#pragma unroll
+            for (int h = 0; h < kHi; ++h) {
+                const float dh = __uint_as_float(r[h]);
+                s = __fmaf_rn(wv[h], dh > 0.0f ? dh : 0.0f, s);
+            }
+            const int64_t t = (f - sh.prefix[b]) * kKeyTile + 32 * warp + lane;
+            const bool valid = t < sh.ncomp[b];
+            if (valid) scores[(int64_t)b * max_ncomp + t] = s;
+            float mx = valid ? s : -INFINITY;
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            if (valid && (lane & (kBlk - 1)) == 0) block_max[(int64_t)b * ld_bm + t / kBlk] = mx;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && sh.abort) raise_status(dev_status, CSA2_DEV_TIMEOUT);
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+constexpr int kTcSmem = (int)sizeof(TcShared) + 1024;
+
+int num_sms() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n <= 0) n = 1;
+    }
+    return n;
+}
+
+int check_index_args(const csa2_params* p, int B, int64_t max_ncomp, const void* q_vals,
+                     const void* q_scales, const void* w, const void* key_cache,
+                     const void* n_tokens, const void* scores, const void* block_max) {
+    if (!p) return fail(CSA2_ERR_INVALID_ARG, "index_scores: params is NULL");
+    if (B < 0 || max_ncomp < 0) return fail(CSA2_ERR_INVALID_ARG, "index_scores: negative size");
+    if (p->index_heads != kHi || p->index_dim != kDi || p->block_size != kBlk ||
+        p->compress_ratio < 1)
+        return fail(CSA2_ERR_UNSUPPORTED, "index_scores: built for 32 heads x 128, blocks of 8");
+    if (B == 0 || max_ncomp == 0) return -1;  // nothing to do
+    if (!q_vals || !q_scales || !w || !key_cache || !n_tokens || !scores || !block_max)
+        return fail(CSA2_ERR_INVALID_ARG, "index_scores: NULL buffer");
+    if (!aligned16(q_vals) || !aligned16(w) || (reinterpret_cast<uintptr_t>(q_scales) & 7))
+        return fail(CSA2_ERR_ALIGN, "index_scores: q_vals, w 16-byte, q_scales 8-byte aligned");
+    return CSA2_OK;
 }
 
 }  // namespace
@@ -105,24 +421,60 @@ k_index_scores_cc(int64_t max_ncomp, int ratio, const uint8_t* __restrict__ q_va
 
 using namespace csa2;
 
-extern "C" int csa2_index_scores(const csa2_params* p, int B, int64_t max_ncomp,
-                                 const uint8_t* q_vals, const uint8_t* q_scales, const float* w,
-                                 const uint8_t* const* key_vals, const uint8_t* const* key_scales,
-                                 const int32_t* n_tokens, float* scores, float* block_max,
-                                 int32_t* dev_status, void* stream) {
+extern "C" int csa2_index_keys_write(const csa2_params* p, int B, int64_t n, const uint8_t* vals,
+                                     const uint8_t* scales, const int64_t* pos0,
+                                     uint8_t* const* dst, const int64_t* cap, int32_t* dev_status,
+                                     void* stream) {
     CSA2_CHECK_PARAMS(p);
-    if (B < 0 || max_ncomp < 0) return fail(CSA2_ERR_INVALID_ARG, "index_scores: negative size");
-    if (B == 0 || max_ncomp == 0) return CSA2_OK;
-    if (p->index_heads != kHi || p->index_dim != kDi || p->block_size != kBlk ||
-        p->compress_ratio < 1)
-        return fail(CSA2_ERR_UNSUPPORTED, "index_scores: built for 32 heads x 128, blocks of 8");
-    if (!q_vals || !q_scales || !w || !key_vals || !key_scales || !n_tokens || !scores ||
-        !block_max)
-        return fail(CSA2_ERR_INVALID_ARG, "index_scores: NULL buffer");
+    if (B < 0 || n < 0) return fail(CSA2_ERR_INVALID_ARG, "index_keys_write: negative size");
+    if (p->index_dim != kDi) return fail(CSA2_ERR_UNSUPPORTED, "index_keys_write: built for Di=128");
+    if (B == 0 || n == 0) return CSA2_OK;
+    if (!vals || !scales || !pos0 || !dst || !cap)
+        return fail(CSA2_ERR_INVALID_ARG, "index_keys_write: NULL buffer");
+    if (!aligned16(vals) || (reinterpret_cast<uintptr_t>(scales) & 7))
+        return fail(CSA2_ERR_ALIGN, "index_keys_write: vals 16-byte, scales 8-byte aligned");
+    const int64_t total = (int64_t)B * n;
+    k_index_keys_write<<<(unsigned)((total + 255) / 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        B, n, vals, scales, pos0, dst, cap, dev_status);
+    return check_launch("index_keys_write");
+}
+
+extern "C" int csa2_index_scores_cuda_cores(const csa2_params* p, int B, int64_t max_ncomp,
+                                            const uint8_t* q_vals, const uint8_t* q_scales,
+                                            const float* w, const uint8_t* const* key_cache,
+                                            const int32_t* n_tokens, float* scores,
+                                            float* block_max, int32_t* dev_status, void* stream) {
+    const int rc = check_index_args(p, B, max_ncomp, q_vals, q_scales, w, key_cache, n_tokens,
+                                    scores, block_max);
+    if (rc != CSA2_OK) return rc < 0 ? CSA2_OK : rc;
     const int64_t gx = (max_ncomp + kKeysPerCta - 1) / kKeysPerCta;
     if (gx > 0x7fffffff) return fail(CSA2_ERR_UNSUPPORTED, "index_scores: too many positions");
     k_index_scores_cc<<<dim3((unsigned)gx, B), kKeysPerCta, 0, static_cast<cudaStream_t>(stream)>>>(
-        max_ncomp, p->compress_ratio, q_vals, q_scales, w, key_vals, key_scales, n_tokens, scores,
+        max_ncomp, p->compress_ratio, q_vals, q_scales, w, key_cache, n_tokens, scores, block_max,
+        dev_status);
+    return check_launch("index_scores_cuda_cores");
+}
+
+extern "C" int csa2_index_scores(const csa2_params* p, int B, int64_t max_ncomp,
+                                 const uint8_t* q_vals, const uint8_t* q_scales, const float* w,
+                                 const uint8_t* const* key_cache, const int32_t* n_tokens,
+                                 float* scores, float* block_max, int32_t* dev_status,
+                                 void* stream) {
+    const int rc = check_index_args(p, B, max_ncomp, q_vals, q_scales, w, key_cache, n_tokens,
+                                    scores, block_max);
+    if (rc != CSA2_OK) return rc < 0 ? CSA2_OK : rc;
+    if (B > kMaxSeq) return fail(CSA2_ERR_UNSUPPORTED, "index_scores: at most 1024 sequences per call");
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(k_index_scores_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kTcSmem) != cudaSuccess)
+            return check_launch("index_scores: smem attribute");
+        attr = true;
+    }
+    const int64_t tiles_max = (int64_t)B * ((max_ncomp + kKeyTile - 1) / kKeyTile);
+    const int grid = (int)std::min<int64_t>(tiles_max, num_sms());
+    k_index_scores_tc<<<grid, kTcThreads, kTcSmem, static_cast<cudaStream_t>(stream)>>>(
+        B, max_ncomp, p->compress_ratio, q_vals, q_scales, w, key_cache, n_tokens, scores,
         block_max, dev_status);
     return check_launch("index_scores");
 }

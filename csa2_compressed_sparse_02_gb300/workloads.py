@@ -24,6 +24,7 @@ class DecodeRun:
     n_steps: int
     device: str = "cuda"
     max_prepared: int = 64
+    cuda_core_indexer: bool = False
     step_done: int = 0
     groups: list = field(default_factory=list)
 
@@ -142,20 +143,23 @@ class DecodeRun:
             keys = grp["keys"]
             for s in range(self.B):
                 n = self.key_rows[s]
+                kv = torch.empty(n, DI // 2, dtype=torch.uint8, device=self.device)
+                ks = torch.empty(n, DI // 16, dtype=torch.uint8, device=self.device)
                 synth.gpu_fill(synth.G_E2M1_BYTES, [synth.stream_key(cfg.seed, synth.IDX_K, g, s)],
-                               0, n * DI // 2, keys.vals[s])
+                               0, n * DI // 2, kv)
                 if cfg.kscale_pow2:
                     synth.gpu_fill(synth.G_SCALE_POW2_BYTES,
                                    [synth.stream_key(cfg.seed, synth.IDX_K_SCALE, g, s)], 0,
-                                   n * DI // 16, keys.scales[s])
+                                   n * DI // 16, ks)
                 else:
-                    keys.scales[s].fill_(synth.E4M3_ONE)
+                    ks.fill_(synth.E4M3_ONE)
                 pos, rv, rs = plants(cfg, g, s)
                 pos = pos[pos < n]
                 if pos.size:
                     pi = torch.from_numpy(pos).to(self.device)
-                    keys.vals[s][pi] = torch.from_numpy(np.tile(rv, (pos.size, 1))).to(self.device)
-                    keys.scales[s][pi] = torch.from_numpy(np.tile(rs, (pos.size, 1))).to(self.device)
+                    kv[pi] = torch.from_numpy(np.tile(rv, (pos.size, 1))).to(self.device)
+                    ks[pi] = torch.from_numpy(np.tile(rs, (pos.size, 1))).to(self.device)
+                keys.write_seq(self.params, s, kv, ks, 0, self.dev_status)
             for r in range(cfg.readers):
                 lay = cfg.layer(g, r)
                 synth.gpu_fill(synth.G_NORMAL_F32, [synth.stream_key(cfg.seed, synth.SINK, lay, 0)],
@@ -208,8 +212,8 @@ class DecodeRun:
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(st)
             api.index_scores(p, self.max_ncomp, grp["iq"][k], grp["iqs"][k], grp["iw"][k],
-                             grp["keys"].val_ptrs, grp["keys"].scale_ptrs, src.n_tokens,
-                             grp["scores"], grp["bmax"], self.dev_status, stream)
+                             grp["keys"].ptrs, src.n_tokens, grp["scores"], grp["bmax"],
+                             self.dev_status, stream, cuda_cores=self.cuda_core_indexer)
             if index_events is not None:
                 e1.record(st)
                 index_events.append((e0, e1))

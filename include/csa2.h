@@ -55,6 +55,7 @@ extern "C" {
 /* ---- device status bits (OR-ed into *dev_status) ---- */
 #define CSA2_DEV_BAD_INDEX 1   /* a selected index >= the sequence's compressed length */
 #define CSA2_DEV_BAD_LENGTH 2  /* a sequence length beyond the stated capacity, or < 0 */
+#define CSA2_DEV_TIMEOUT 4     /* a pipeline wait gave up (the kernel returned early) */
 
 /* ---- formats ---- */
 #define CSA2_F32 0   /* fp32 */
@@ -138,29 +139,77 @@ int csa2_nvfp4_quantize(const float* x, int64_t n_rows, int row_len,
                         uint8_t* vals, uint8_t* scales, void* stream);
 
 /*
+ * Index-key cache layout (one per sequence). Positions are grouped in tiles of
+ * 128; tile j (positions 128j..128j+127) is CSA2_KEY_TILE_BYTES = 9216
+ * contiguous bytes, the exact shared-memory image the tensor-core Indexer
+ * consumes, so one bulk copy moves a tile:
+ *   bytes [0, 8192): E2M1 codes, 64 bytes per position m = t mod 128 (dim 2k in
+ *     the low nibble of byte k), K-major with the 64-byte swizzle: byte b of
+ *     16-byte chunk c of position m sits at  m*64 + ((c ^ ((m >> 1) & 3)) << 4) + b;
+ *   bytes [8192, 9216): E4M3 group scales, group g (dims 16g..16g+15) of
+ *     position m at  8192 + (g >> 2)*512 + (m & 31)*16 + (m >> 5)*4 + (g & 3).
+ * A sequence holding n positions needs ceil(n/128) tiles. Rows past n in the
+ * last tile are ignored. csa2_index_keys_write fills it from plain rows.
+ */
+#define CSA2_KEY_TILE 128
+#define CSA2_KEY_TILE_BYTES 9216
+
+/*
+ * csa2_index_keys_write — write n plain NVFP4 index keys per sequence into the
+ * tiled index-key caches (layout above), at positions pos0[b] .. pos0[b]+n-1.
+ * ("DeepSeek-V4.1-Flash-NVFP4" §3.3: the shared FP4 index key the index heads
+ * score; the keys come from a projection outside this path.)
+ *   vals   [B, n, Di/2] bytes, scales [B, n, Di/16] bytes (plain NVFP4 rows, as
+ *          csa2_nvfp4_quantize produces them), device;
+ *   pos0   [B] int64, device;  dst: device array [B] of tiled cache bases;
+ *   cap    [B] int64, device: positions each cache holds (tiles*128); a
+ *          position >= cap[b] is skipped and sets CSA2_DEV_BAD_LENGTH.
+ * Constraints: Di == 128.
+ */
+int csa2_index_keys_write(const csa2_params* p, int B, int64_t n,
+                          const uint8_t* vals, const uint8_t* scales, const int64_t* pos0,
+                          uint8_t* const* dst, const int64_t* cap,
+                          int32_t* dev_status, void* stream);
+
+/*
  * csa2_index_scores — decode Indexer over every compressed position of B
  * sequences ("DeepSeek-V4.1-Flash-NVFP4" §3.3):
  *   s_t = sum_{h<Hi} w[h] * ReLU( sum_{d<Di} q[h,d] * k[t,d] ),  t < n_c,
  * with q and k the NVFP4-decoded values (E2M1 code x E4M3 group scale), fp32
  * accumulation, and the block maximum m_b = max_{t in [8b, 8b+8), t < n_c} s_t.
- * n_c = n_tokens[b] / compress_ratio.
+ * n_c = n_tokens[b] / compress_ratio, clipped to max_ncomp.
+ * Runs on the 5th-generation tensor cores (block-scaled FP4 MMA, 128 positions
+ * x 32 heads per instruction pair), one CTA per SM streaming tiles.
  *
  *   q_vals   [B, Hi, Di/2] bytes   q_scales [B, Hi, Di/16] bytes   w [B, Hi] fp32
- *   key_vals, key_scales: device arrays [B] of per-sequence bases of the index
- *            key cache, [cap, Di/2] and [cap, Di/16] bytes (row t = position t).
+ *   key_cache device array [B] of tiled index-key caches (layout above); the
+ *            cache of sequence b must hold ceil(n_c/128) tiles.
  *   scores   [B, max_ncomp] fp32 out (entries >= n_c untouched)
  *   block_max [B, ceil(max_ncomp/8)] fp32 out (entries >= ceil(n_c/8) untouched)
  *   max_ncomp >= every n_c (else CSA2_DEV_BAD_LENGTH, and the sequence is clipped).
- * Constraints: Hi == 32, Di == 128, block_size == 8.
+ *   A pipeline wait that does not complete within about a second sets
+ *   CSA2_DEV_TIMEOUT and the kernel returns.
+ * Constraints: Hi == 32, Di == 128, block_size == 8, B <= 1024.
  * The fp32 result is exact (independent of summation order) when every
  * partial sum is a multiple of a common power of two below 2^24 of it — true
  * for E2M1 codes with power-of-two scales and weights.
  */
 int csa2_index_scores(const csa2_params* p, int B, int64_t max_ncomp,
                       const uint8_t* q_vals, const uint8_t* q_scales, const float* w,
-                      const uint8_t* const* key_vals, const uint8_t* const* key_scales,
+                      const uint8_t* const* key_cache,
                       const int32_t* n_tokens, float* scores, float* block_max,
                       int32_t* dev_status, void* stream);
+
+/*
+ * csa2_index_scores_cuda_cores — the same Indexer on CUDA cores (fp32 FMA, one
+ * thread per position). Same arguments and results; kept to validate the
+ * tensor-core build and as its ablation.
+ */
+int csa2_index_scores_cuda_cores(const csa2_params* p, int B, int64_t max_ncomp,
+                                 const uint8_t* q_vals, const uint8_t* q_scales, const float* w,
+                                 const uint8_t* const* key_cache,
+                                 const int32_t* n_tokens, float* scores, float* block_max,
+                                 int32_t* dev_status, void* stream);
 
 /*
  * csa2_select_topk — two-level selection ("DeepSeek-V4.1-Flash-NVFP4" §3.3).

@@ -51,9 +51,13 @@ def test_host_side_rejections_without_launching(L):
     assert L.csa2_compress_append(pp, -1, 1, *([None] * 11)) == 1
     assert L.csa2_compress_append(None, 1, 1, *([None] * 11)) == 1
     assert "params" in L.csa2_last_error().decode()
-    assert L.csa2_index_scores(pp, 1, 10, *([None] * 10)) == 1  # NULL buffers
+    assert L.csa2_index_scores(pp, 1, 10, *([None] * 9)) == 1  # NULL buffers
+    assert L.csa2_index_scores_cuda_cores(pp, 1, 10, *([None] * 9)) == 1
     bad = api.default_params(index_heads=16)
-    assert L.csa2_index_scores(ctypes.byref(bad), 1, 10, *([None] * 10)) == 4
+    assert L.csa2_index_scores(ctypes.byref(bad), 1, 10, *([None] * 9)) == 4
+    bad_dim = api.default_params(index_dim=64)
+    assert L.csa2_index_keys_write(ctypes.byref(bad_dim), 1, 4, *([None] * 7)) == 4
+    assert L.csa2_index_keys_write(pp, 1, 4, *([None] * 7)) == 1
     bad = api.default_params(topk_pos=256)
     assert L.csa2_select_topk(ctypes.byref(bad), 1, 10, *([None] * 7)) == 4
     assert L.csa2_sparse_attn(pp, 1, *([None] * 8), None, 0, None, None) == 1

@@ -161,43 +161,102 @@ def _index_case(seed, n_cs, pow2=True):
     return qv, qs, w, kvs, kss, rng
 
 
-def test_index_scores_bit_exact_ragged():
-    n_cs = [1, 7, 8, 9, 255, 256, 257, 1000, 5003, 0]
+def _tiled_caches(p, kvs, kss):
+    """Index-key caches written through csa2_index_keys_write from plain rows."""
+    cache = api.IndexKeyCache([max(len(k), 1) for k in kvs])
+    for b, (kv, ks) in enumerate(zip(kvs, kss)):
+        cache.write_seq(p, b, t(kv), t(ks))
+    return cache
+
+
+def test_index_keys_write_produces_the_documented_tile_image():
+    rng = np.random.default_rng(12)
+    n = 300  # 3 tiles, the last partial
+    kv = rng.integers(0, 256, (n, 64), dtype=np.uint8)
+    ks = rng.integers(0, 256, (n, 8), dtype=np.uint8)
+    p = api.default_params()
+    cache = _tiled_caches(p, [kv], [ks])
+    torch.cuda.synchronize()
+    img = cache.buf[0].cpu().numpy()
+    assert img.size == 3 * 9216
+    for t_ in range(n):  # formulas of include/csa2.h, written out independently here
+        tile, m = divmod(t_, 128)
+        base = tile * 9216
+        for c in range(4):
+            off = base + m * 64 + ((c ^ ((m >> 1) & 3)) << 4)
+            assert np.array_equal(img[off:off + 16], kv[t_, 16 * c:16 * c + 16])
+        for g in range(8):
+            off = base + 8192 + (g >> 2) * 512 + (m & 31) * 16 + (m >> 5) * 4 + (g & 3)
+            assert img[off] == ks[t_, g]
+
+
+@pytest.mark.parametrize("cuda_cores", [False, True])
+def test_index_scores_bit_exact_ragged(cuda_cores):
+    n_cs = [1, 7, 8, 9, 127, 128, 129, 255, 256, 257, 1000, 5003, 0, 70000]
     qv, qs, w, kvs, kss, _ = _index_case(3, n_cs)
     B = len(n_cs)
     max_nc = max(n_cs)
     p = api.default_params()
-    kt = [t(k) for k in kvs]
-    st = [t(s) for s in kss]
+    cache = _tiled_caches(p, kvs, kss)
     n_tok = t(np.array([2 * n for n in n_cs], np.int32))
     scores = torch.full((B, max_nc), -7.0, device=DEV)
     bmax = torch.full((B, math.ceil(max_nc / 8)), -7.0, device=DEV)
-    api.index_scores(p, max_nc, t(qv), t(qs), t(w), api.ptr_array(kt), api.ptr_array(st), n_tok,
-                     scores, bmax)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    api.index_scores(p, max_nc, t(qv), t(qs), t(w), cache.ptrs, n_tok, scores, bmax, st,
+                     cuda_cores=cuda_cores)
     torch.cuda.synchronize()
+    assert st.item() == 0
     gs, gb = scores.cpu().numpy(), bmax.cpu().numpy()
     for b, n in enumerate(n_cs):
         ref, inexact = orc.index_scores(qv[b], qs[b], w[b], kvs[b][:n], kss[b][:n])
         assert inexact == 0
-        assert np.array_equal(gs[b, :n], ref), b
+        bad = np.nonzero(gs[b, :n] != ref)[0]
+        assert bad.size == 0, (b, n, bad[:5], gs[b, bad[:5]], ref[bad[:5]])
         assert np.all(gs[b, n:] == -7.0)  # untouched past n_c
         nb = math.ceil(n / 8)
         assert np.array_equal(gb[b, :nb], orc.block_max(ref, 8)), b
 
 
+def test_index_scores_general_e4m3_scales_match_cuda_cores():
+    """Non-power-of-two E4M3 scales (mantissa bits): the tensor-core and CUDA-core
+    builds must agree with the oracle to fp32 rounding."""
+    rng = np.random.default_rng(21)
+    n_cs = [4000, 333]
+    qv, qs, w, kvs, kss, _ = _index_case(5, n_cs)
+    qs = rng.integers(0x28, 0x40, qs.shape, dtype=np.uint8)        # 0.125 .. 1.875
+    kss = [rng.integers(0x28, 0x48, k.shape, dtype=np.uint8) for k in kss]
+    p = api.default_params()
+    cache = _tiled_caches(p, kvs, kss)
+    n_tok = t(np.array([2 * n for n in n_cs], np.int32))
+    outs = []
+    for cc in (False, True):
+        scores = torch.zeros(2, max(n_cs), device=DEV)
+        bmax = torch.zeros(2, math.ceil(max(n_cs) / 8), device=DEV)
+        api.index_scores(p, max(n_cs), t(qv), t(qs), t(w), cache.ptrs, n_tok, scores, bmax,
+                         cuda_cores=cc)
+        torch.cuda.synchronize()
+        outs.append(scores.cpu().numpy())
+    for b, n in enumerate(n_cs):
+        ref, _ = orc.index_scores(qv[b], qs[b], w[b], kvs[b][:n], kss[b][:n])
+        for o in outs:
+            err = np.abs(o[b, :n].astype(np.float64) - ref) / np.maximum(np.abs(ref), 1.0)
+            assert err.max() < 1e-5, err.max()
+
+
 def test_index_scores_clip_and_status_when_length_exceeds_max():
     qv, qs, w, kvs, kss, _ = _index_case(4, [100])
     p = api.default_params()
-    st = torch.zeros(1, dtype=torch.int32, device=DEV)
-    scores = torch.zeros(1, 50, device=DEV)
-    bmax = torch.zeros(1, 7, device=DEV)
-    keys, kscales = t(kvs[0]), t(kss[0])  # must outlive the kernel: only their addresses are passed
-    api.index_scores(p, 50, t(qv), t(qs), t(w), api.ptr_array([keys]), api.ptr_array([kscales]),
-                     t(np.array([200], np.int32)), scores, bmax, st)
-    torch.cuda.synchronize()
-    assert st.item() & 2
-    ref, _ = orc.index_scores(qv[0], qs[0], w[0], kvs[0][:50], kss[0][:50])
-    assert np.array_equal(scores[0].cpu().numpy(), ref)
+    cache = _tiled_caches(p, kvs, kss)
+    for cc in (False, True):
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        scores = torch.zeros(1, 50, device=DEV)
+        bmax = torch.zeros(1, 7, device=DEV)
+        api.index_scores(p, 50, t(qv), t(qs), t(w), cache.ptrs, t(np.array([200], np.int32)),
+                         scores, bmax, st, cuda_cores=cc)
+        torch.cuda.synchronize()
+        assert st.item() & 2
+        ref, _ = orc.index_scores(qv[0], qs[0], w[0], kvs[0][:50], kss[0][:50])
+        assert np.array_equal(scores[0].cpu().numpy(), ref)
 
 
 # --------------------------------------------------------------------------- selection
