@@ -195,6 +195,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--nvtx", action="store_true", help="mark the timed steps with an NVTX range")
+    ap.add_argument("--eager", action="store_true", help="launch kernels one by one (no CUDA graph)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -225,21 +226,28 @@ def main():
 
     K, Wm = args.steps, args.warmup
     e2e_steps = 0 if args.no_e2e else K
-    run = workloads.DecodeRun(cfg, n_steps=Wm + K + e2e_steps + Wm)
+    run = workloads.DecodeRun(cfg, n_steps=Wm + 2 + K + e2e_steps + 5)
     stream = torch.cuda.current_stream()
 
-    # ---------------- device-resident timing
+    # ---------------- warm-up, then one CUDA graph per prepared step
     for _ in range(Wm):
         run.step()
     torch.cuda.synchronize()
+    mode = "eager"
+    if not args.eager:
+        if run.capture(with_timers=True):
+            mode = "cuda-graph"
+            for _ in range(2):
+                run.step_graph()
+            torch.cuda.synchronize()
+    advance = run.step_graph if mode == "cuda-graph" else None
     uuid = None
     try:
         uuid = str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
         pass
-    ev_idx = []
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    scan_bytes = []
+    scan_bytes, eager_timers, slots = [], {}, []
     with ClockSampler(uuid) as clk:
         barrier()
         torch.cuda.synchronize()
@@ -248,7 +256,11 @@ def main():
         start.record(stream)
         for _ in range(K):
             scan_bytes.append(run.scan_bytes())
-            run.step(index_events=ev_idx)
+            slots.append(run.step_done % run.n_prep)
+            if advance:
+                advance()
+            else:
+                run.step(timers=eager_timers)
         end.record(stream)
         if args.nvtx:
             torch.cuda.nvtx.range_pop()
@@ -264,8 +276,18 @@ def main():
     step_s = elapsed / K
     value = world * cfg.B * K / elapsed
 
-    scan_ms = [a.elapsed_time(b) for a, b in ev_idx]
-    scan_s = statistics.mean(scan_ms) / 1000.0
+    # kernel durations from the events recorded around each call in the timed steps
+    if mode == "cuda-graph":
+        timers = {}
+        for k in dict.fromkeys(slots):  # last replay of every slot used
+            for cat, evs in run.graph_timers[k].items():
+                timers.setdefault(cat, []).extend(evs)
+    else:
+        timers = eager_timers
+    steps_covered = len(set(slots)) if mode == "cuda-graph" else K
+    breakdown = {cat: sum(a.elapsed_time(b) for a, b in evs) / steps_covered
+                 for cat, evs in timers.items()}  # ms per step spent in each call category
+    scan_s = statistics.mean(a.elapsed_time(b) for a, b in timers["index"]) / 1000.0
     scan_b = statistics.mean(scan_bytes)
     hbm_peak, peak_kind = peaks()
     achieved = scan_b / scan_s / 1e9
@@ -298,6 +320,8 @@ def main():
                      "achieved_gbs": step_alg_bytes / step_s / 1e9,
                      "frac": step_alg_bytes / step_s / 1e9 / hbm_peak},
         "gpu_launches": run.launches_per_step() * K,
+        "launch_mode": mode,
+        "ms_per_step_by_call": breakdown,
         "clocks": clocks,
     }
     if e2e:
@@ -332,8 +356,9 @@ def run_e2e(run, K, stream, barrier):
     d2h = sum(o.numel() * o.element_size() for o in dev_out)
     for h in host_in:
         h2d += h[0].numel() * h.element_size()  # one step's slice
+    advance = run.step_graph if getattr(run, "graphs", None) else run.step
     for _ in range(3):
-        run.step()
+        advance()
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
@@ -342,7 +367,7 @@ def run_e2e(run, K, stream, barrier):
         k = run.step_done % n_prep
         for h, d in zip(host_in, dev_in):
             d[k].copy_(h[k], non_blocking=True)
-        run.step()
+        advance()
         for h, d in zip(host_out, dev_out):
             h.copy_(d, non_blocking=True)
     end.record(stream)

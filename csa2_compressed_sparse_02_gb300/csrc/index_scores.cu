@@ -12,10 +12,10 @@
 // K[128 x 128] . Q[32 x 128]^T as two tcgen05 block-scaled FP4 MMAs (K = 64 each,
 // UE4M3 scale per 16 elements) into TMEM; the epilogue warps read one position
 // per lane (32 heads), apply ReLU and the head weights, and reduce the block
-// maximum over 8 adjacent lanes. One persistent CTA per SM; warps 0-3 epilogue,
-// warp 4 loads (bulk copies into a 12-stage ring), warp 5 issues the MMAs;
-// accumulators double-buffered in TMEM so the epilogue of tile i overlaps the
-// MMAs of tile i+1.
+// maximum over 8 adjacent lanes. One persistent CTA per SM; warps 0-7 epilogue
+// (two warpgroups taking alternate super-tiles), warp 8 loads (one bulk copy
+// per super-tile of 4 tiles into a 5-stage ring), warp 9 issues the MMAs;
+// three super-tile accumulator sets in TMEM so epilogues overlap the MMAs.
 //
 // CUDA-core build (k_index_scores_cc): one thread per position, 32 fp32
 // accumulators, the query decoded once per CTA into shared memory.
@@ -157,31 +157,50 @@ k_index_scores_cc(int64_t max_ncomp, int ratio, const uint8_t* __restrict__ q_va
 }
 
 // ------------------------------------------------------------------ tensor-core build
-constexpr int kStages = 12;
-constexpr int kTcThreads = 192;  // warps 0-3 epilogue, 4 loader, 5 MMA
+// Unit of work: a super-tile of up to kTilesPerStage consecutive tiles of one sequence
+// (contiguous in the cache, so one bulk copy of up to 36 KB). Per super-tile the
+// MMA thread issues 2 scale copies + 2 MMAs per tile into the tile's own TMEM
+// accumulator, then one commit for the stage and one for the epilogue: the
+// fixed per-commit and per-copy costs are paid once per 36 KB, not per 9 KB.
+constexpr int kTilesPerStage = 4;
+constexpr int kStageBytes = kTilesPerStage * kKeyTileBytes;  // 36,864 = 36 x 1024
+constexpr int kStages = 5;
+constexpr int kAcc = 3;          // super-tile accumulators in flight between MMA and epilogue
+constexpr int kEpiGroups = 2;    // epilogue warpgroups, alternating super-tiles
+constexpr int kLoadWarp = 4 * kEpiGroups, kMmaWarp = kLoadWarp + 1;
+constexpr int kTcThreads = 32 * (kMmaWarp + 1);  // warps 0-7 epilogue, 8 loader, 9 MMA
 constexpr int kMaxSeq = 1024;
-constexpr uint32_t kTmemCols = 128;
-constexpr uint32_t kColD = 0, kColSFA = 64, kColSFB = 80;  // D[2] x 32, SFA[2] x 8, SFB[2] x 8
+constexpr uint32_t kTmemCols = 512;
+// TMEM columns: D[kAcc][kTilesPerStage] x 32, then SFA[kAcc][kTilesPerStage] x 8, then SFB[2] x 8
+constexpr uint32_t kColD = 0, kColSFA = 32 * kAcc * kTilesPerStage, kColSFB = kColSFA + 8 * kAcc * kTilesPerStage;
+static_assert(kColSFB + 16 <= kTmemCols, "TMEM columns");
 // Instruction descriptor: kind::mxf4nvf4, A and B E2M1 (1), K-major, dense,
 // N = 32 (N>>3 in bits 17..22), UE4M3 scales (bit 23 = 0), M = 128 (M>>4 in bits 24..28).
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((32u >> 3) << 17) | ((128u >> 4) << 24);
 
 struct TcShared {
-    uint8_t stage[kStages][kKeyTileBytes];  // 9216 = 9 x 1024: every stage 1024-aligned
-    uint8_t q[2][kHi * (kDi / 2)];          // B operand (32 heads x 64 B, 64-byte swizzle), 2 slots
-    uint8_t sfb[2][1024];                   // B scale factors, two 512-byte atoms per slot
+    uint8_t stage[kStages][kStageBytes];  // every stage 1024-aligned
+    uint8_t q[2][kHi * (kDi / 2)];         // B operand (32 heads x 64 B, 64-byte swizzle), 2 slots
+    uint8_t sfb[2][1024];                  // B scale factors, two 512-byte atoms per slot
     uint64_t full[kStages], empty[kStages];
-    uint64_t qfull[2], qempty[2], accf[2], acce[2], done;
+    uint64_t qfull[2], qempty[2], accf[kAcc], acce[kAcc], done;
     uint32_t tmem_base;
     int abort;
-    int32_t prefix[kMaxSeq + 1];  // tiles of sequences < b
+    int32_t prefix[kMaxSeq + 1];  // super-tiles of sequences < b
     int32_t ncomp[kMaxSeq];
 };
 
-// position of flat tile f: advance b while f is past sequence b's tiles
+// sequence of flat super-tile f: advance b while f is past sequence b's super-tiles
 __device__ __forceinline__ int advance_seq(const TcShared& sh, int b, int64_t f) {
     while (f >= sh.prefix[b + 1]) ++b;
     return b;
+}
+
+// tiles in super-tile g of a sequence with n_c positions
+__device__ __forceinline__ int tiles_in(int64_t g, int32_t n_c) {
+    const int64_t nt = (n_c + kKeyTile - 1) / kKeyTile;
+    const int64_t left = nt - g * kTilesPerStage;
+    return left < kTilesPerStage ? (int)left : kTilesPerStage;
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -204,6 +223,8 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.qfull[i], 1);
             mbar_init(&sh.qempty[i], 1);
+        }
+        for (int i = 0; i < kAcc; ++i) {
             mbar_init(&sh.accf[i], 1);
             mbar_init(&sh.acce[i], 4);
         }
@@ -211,8 +232,7 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
         sh.abort = 0;
         fence_mbar_init();
     }
-    if (warp == 0) {  // per-sequence compressed lengths and tile prefix
-        int32_t run = 0;
+    if (warp == 0) {  // per-sequence compressed lengths and super-tile prefix
         const int per = (B + 31) / 32;
         const int b0 = min(B, lane * per), b1 = min(B, b0 + per);
         int32_t local = 0;
@@ -220,7 +240,7 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
             const int64_t n_c = seq_ncomp(n_tokens, b, ratio, max_ncomp, dev_status,
                                           blockIdx.x == 0);
             sh.ncomp[b] = (int32_t)n_c;
-            local += (int32_t)((n_c + kKeyTile - 1) / kKeyTile);
+            local += (int32_t)((n_c + kTilesPerStage * kKeyTile - 1) / (kTilesPerStage * kKeyTile));
         }
         int32_t incl = local;
 #pragma unroll
@@ -228,14 +248,14 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
             const int32_t u = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += u;
         }
-        run = incl - local;
+        int32_t run = incl - local;
         for (int b = b0; b < b1; ++b) {
             sh.prefix[b] = run;
-            run += (sh.ncomp[b] + kKeyTile - 1) / kKeyTile;
+            run += (sh.ncomp[b] + kTilesPerStage * kKeyTile - 1) / (kTilesPerStage * kKeyTile);
         }
         if (lane == 31) sh.prefix[B] = incl;
     }
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tmem_alloc(&sh.tmem_base, kTmemCols);
         tmem_relinquish();
     }
@@ -247,13 +267,13 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
     const int64_t f0 = total * blockIdx.x / gridDim.x;
     const int64_t f1 = total * (blockIdx.x + 1) / gridDim.x;
 
-    if (warp == 4) {
-        // ---------------- loader: query slots per sequence, key tiles per stage
+    if (warp == kLoadWarp) {
+        // ---------------- loader: query slots per sequence, super-tiles per stage
         int seg = -1, b = 0, prev_b = -1;
         int64_t issued = 0;
         for (int64_t f = f0; f < f1; ++f) {
             b = advance_seq(sh, b, f);
-            const int64_t tile = f - sh.prefix[b];
+            const int64_t g = f - sh.prefix[b];
             if (b != prev_b) {
                 ++seg;
                 const int qs = seg & 1;
@@ -266,7 +286,7 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
                 for (int c = 0; c < 4; ++c)
                     *reinterpret_cast<uint4*>(&sh.q[qs][lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)]) = src[c];
                 const uint2 sc = *reinterpret_cast<const uint2*>(
-                    q_scales + ((int64_t)b * kHi + lane) * (kDi / kGroup));
+                    q_scales + ((int64_t)b * kHi + lane) * (kDi / 16));
                 *reinterpret_cast<uint4*>(&sh.sfb[qs][lane * 16]) = make_uint4(sc.x, 0u, 0u, 0u);
                 *reinterpret_cast<uint4*>(&sh.sfb[qs][512 + lane * 16]) = make_uint4(sc.y, 0u, 0u, 0u);
                 fence_proxy_async_smem();
@@ -278,8 +298,9 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
             const int s = (int)(i % kStages);
             if (!mbar_wait(&sh.empty[s], (uint32_t)((i / kStages) & 1) ^ 1, abort)) break;
             if (lane == 0) {
-                mbar_arrive_expect_tx(&sh.full[s], kKeyTileBytes);
-                bulk_g2s(sh.stage[s], key_cache[b] + tile * kKeyTileBytes, kKeyTileBytes, &sh.full[s]);
+                const uint32_t bytes = (uint32_t)tiles_in(g, sh.ncomp[b]) * kKeyTileBytes;
+                mbar_arrive_expect_tx(&sh.full[s], bytes);
+                bulk_g2s(sh.stage[s], key_cache[b] + g * kStageBytes, bytes, &sh.full[s]);
             }
             __syncwarp();
             issued = i + 1;
@@ -289,16 +310,16 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
             for (uint32_t k = 0; k < kSpinLimit; ++k)
                 if (mbar_try_wait(&sh.full[j % kStages], (uint32_t)((j / kStages) & 1))) break;
         }
-    } else if (warp == 5) {
+    } else if (warp == kMmaWarp) {
         // ---------------- MMA issuer (one thread)
         if (lane == 0) {
             int seg = -1, b = 0, prev_b = -1;
             for (int64_t f = f0; f < f1; ++f) {
                 b = advance_seq(sh, b, f);
                 const int64_t i = f - f0;
-                const int s = (int)(i % kStages), a = (int)(i & 1);
+                const int s = (int)(i % kStages), a = (int)(i % kAcc);
                 if (!mbar_wait(&sh.full[s], (uint32_t)((i / kStages) & 1), abort)) break;
-                if (!mbar_wait(&sh.acce[a], (uint32_t)((i >> 1) & 1) ^ 1, abort)) break;
+                if (!mbar_wait(&sh.acce[a], (uint32_t)((i / kAcc) & 1) ^ 1, abort)) break;
                 tc_fence_after();
                 if (b != prev_b) {
                     if (seg >= 0) tc_commit(&sh.qempty[seg & 1]);
@@ -313,18 +334,20 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
                     prev_b = b;
                 }
                 const int qs = seg & 1;
-                const uint32_t st = smem_u32(sh.stage[s]);
                 const uint32_t qa = smem_u32(sh.q[qs]);
-                tmem_cp_32x128b_x4(tmem + kColSFA + 8 * a,
-                                   smem_desc(st + kKeyValBytes, 128, 128, kLayoutNone));
-                tmem_cp_32x128b_x4(tmem + kColSFA + 8 * a + 4,
-                                   smem_desc(st + kKeyValBytes + 512, 128, 128, kLayoutNone));
-                const uint32_t d = tmem + kColD + 32 * a;
-                mma_mxf4nvf4(d, smem_desc(st, 16, 512, kLayoutSw64), smem_desc(qa, 16, 512, kLayoutSw64),
-                             kIdesc, tmem + kColSFA + 8 * a, tmem + kColSFB + 8 * qs, 0);
-                mma_mxf4nvf4(d, smem_desc(st + 32, 16, 512, kLayoutSw64),
-                             smem_desc(qa + 32, 16, 512, kLayoutSw64), kIdesc,
-                             tmem + kColSFA + 8 * a + 4, tmem + kColSFB + 8 * qs + 4, 1);
+                const uint32_t sfb = tmem + kColSFB + 8 * qs;
+                const int nt = tiles_in(f - sh.prefix[b], sh.ncomp[b]);
+                for (int j = 0; j < nt; ++j) {
+                    const uint32_t st = smem_u32(sh.stage[s]) + j * kKeyTileBytes;
+                    const uint32_t sfa = tmem + kColSFA + 8 * (a * kTilesPerStage + j);
+                    const uint32_t d = tmem + kColD + 32 * (a * kTilesPerStage + j);
+                    tmem_cp_32x128b_x4(sfa, smem_desc(st + kKeyValBytes, 128, 128, kLayoutNone));
+                    tmem_cp_32x128b_x4(sfa + 4, smem_desc(st + kKeyValBytes + 512, 128, 128, kLayoutNone));
+                    mma_mxf4nvf4(d, smem_desc(st, 16, 512, kLayoutSw64),
+                                 smem_desc(qa, 16, 512, kLayoutSw64), kIdesc, sfa, sfb, 0);
+                    mma_mxf4nvf4(d, smem_desc(st + 32, 16, 512, kLayoutSw64),
+                                 smem_desc(qa + 32, 16, 512, kLayoutSw64), kIdesc, sfa + 4, sfb + 4, 1);
+                }
                 tc_commit(&sh.empty[s]);
                 tc_commit(&sh.accf[a]);
             }
@@ -335,14 +358,16 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
         }
         __syncwarp();
     } else {
-        // ---------------- epilogue: warp q owns TMEM lanes 32q..32q+31 = positions of the tile
+        // ---------------- epilogue: warpgroup e handles super-tiles i with i % kEpiGroups == e;
+        // warp q of it owns TMEM lanes 32q..32q+31 = positions 32q.. of each tile
+        const int eg = warp >> 2, wq = warp & 3;
         const int64_t ld_bm = (max_ncomp + kBlk - 1) / kBlk;
         int b = 0, prev_b = -1;
         float wv[kHi];
         for (int64_t f = f0; f < f1; ++f) {
             b = advance_seq(sh, b, f);
             const int64_t i = f - f0;
-            const int a = (int)(i & 1);
+            const int a = (int)(i % kAcc);
             if (b != prev_b) {
                 const float4* w4 = reinterpret_cast<const float4*>(w + (int64_t)b * kHi);
 #pragma unroll
@@ -355,33 +380,40 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
                 }
                 prev_b = b;
             }
-            if (!mbar_wait(&sh.accf[a], (uint32_t)((i >> 1) & 1), abort)) break;
+            if ((int)(i % kEpiGroups) != eg) continue;
+            if (!mbar_wait(&sh.accf[a], (uint32_t)((i / kAcc) & 1), abort)) break;
             tc_fence_after();
-            uint32_t r[kHi];
-            tmem_ld_32x32b_x32(tmem + ((uint32_t)(32 * warp) << 16) + kColD + 32 * a, r);
+            const int64_t g = f - sh.prefix[b];
+            const int nt = tiles_in(g, sh.ncomp[b]);
+            const int32_t n_c = sh.ncomp[b];
+            for (int j = 0; j < nt; ++j) {
+                uint32_t r[kHi];
+                tmem_ld_32x32b_x32(
+                    tmem + ((uint32_t)(32 * wq) << 16) + kColD + 32 * (a * kTilesPerStage + j), r);
+                float s = 0.0f;
+#pragma unroll
+                for (int h = 0; h < kHi; ++h) {
+                    const float dh = __uint_as_float(r[h]);
+                    s = __fmaf_rn(wv[h], dh > 0.0f ? dh : 0.0f, s);
+                }
+                const int64_t t = (g * kTilesPerStage + j) * kKeyTile + 32 * wq + lane;
+                const bool valid = t < n_c;
+                if (valid) scores[(int64_t)b * max_ncomp + t] = s;
+                float mx = valid ? s : -INFINITY;
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                if (valid && (lane & (kBlk - 1)) == 0) block_max[(int64_t)b * ld_bm + t / kBlk] = mx;
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.acce[a]);
-            float s = 0.0f;
-#pragma unroll
-            for (int h = 0; h < kHi; ++h) {
-                const float dh = __uint_as_float(r[h]);
-                s = __fmaf_rn(wv[h], dh > 0.0f ? dh : 0.0f, s);
-            }
-            const int64_t t = (f - sh.prefix[b]) * kKeyTile + 32 * warp + lane;
-            const bool valid = t < sh.ncomp[b];
-            if (valid) scores[(int64_t)b * max_ncomp + t] = s;
-            float mx = valid ? s : -INFINITY;
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-            if (valid && (lane & (kBlk - 1)) == 0) block_max[(int64_t)b * ld_bm + t / kBlk] = mx;
         }
     }
     tc_fence_before();
     __syncthreads();
     if (tid == 0 && sh.abort) raise_status(dev_status, CSA2_DEV_TIMEOUT);
-    if (warp == 5) {
+    if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
@@ -471,7 +503,7 @@ extern "C" int csa2_index_scores(const csa2_params* p, int B, int64_t max_ncomp,
             return check_launch("index_scores: smem attribute");
         attr = true;
     }
-    const int64_t tiles_max = (int64_t)B * ((max_ncomp + kKeyTile - 1) / kKeyTile);
+    const int64_t tiles_max = (int64_t)B * ((max_ncomp + kTilesPerStage * kKeyTile - 1) / (kTilesPerStage * kKeyTile));
     const int grid = (int)std::min<int64_t>(tiles_max, num_sms());
     k_index_scores_tc<<<grid, kTcThreads, kTcSmem, static_cast<cudaStream_t>(stream)>>>(
         B, max_ncomp, p->compress_ratio, q_vals, q_scales, w, key_cache, n_tokens, scores,

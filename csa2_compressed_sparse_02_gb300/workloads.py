@@ -193,41 +193,95 @@ class DecodeRun:
         torch.cuda.synchronize()
 
     # ------------------------------------------------------------------ one step
-    def step(self, stream=None, index_events=None):
-        """Enqueue one decode step (every group, every layer) on `stream`.
-        index_events: optional list receiving (start, end) CUDA events recorded
-        around each Indexer launch on the same stream."""
-        api, cfg = self.api, self.cfg
-        assert self.step_done < self.n_steps, "more steps than the caches were sized for"
-        k = self.step_done % self.n_prep
-        p = self.params
+    def _timed(self, timers, cat, st, fn):
+        if timers is None:
+            fn()
+            return
         torch = self.torch
+        kw = {"enable_timing": True}
+        if getattr(self, "_external_events", False):
+            kw["external"] = True
+        e0, e1 = torch.cuda.Event(**kw), torch.cuda.Event(**kw)
+        e0.record(st)
+        fn()
+        e1.record(st)
+        timers.setdefault(cat, []).append((e0, e1))
+
+    def _enqueue(self, k, stream=None, timers=None):
+        """Enqueue one decode step (every group, every layer) using input slot k.
+        timers: optional dict receiving (start, end) CUDA events per call category
+        ("compress", "index", "select", "attn"), recorded on the launching stream."""
+        api, cfg, p, torch = self.api, self.cfg, self.params, self.torch
         st = torch.cuda.current_stream() if stream is None else stream
+        ds = self.dev_status
         for grp in self.groups:
             src = grp["src"]
-            src.append(grp["kv"][k], grp["gate"][k], self.dev_status, stream)
-            if cfg.readers > 1:
-                grp["rd"].append(grp["kv_rd"][k], None, self.dev_status, stream)
-            if index_events is not None:
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(st)
-            api.index_scores(p, self.max_ncomp, grp["iq"][k], grp["iqs"][k], grp["iw"][k],
-                             grp["keys"].ptrs, src.n_tokens, grp["scores"], grp["bmax"],
-                             self.dev_status, stream, cuda_cores=self.cuda_core_indexer)
-            if index_events is not None:
-                e1.record(st)
-                index_events.append((e0, e1))
-            api.select_topk(p, self.max_ncomp, grp["scores"], grp["bmax"], src.n_tokens,
-                            grp["idx"], grp["n_sel"], self.dev_status, stream)
-            for r in range(cfg.readers):
-                if r == 0:
-                    win_ptrs, n_tok = src.win_ptrs, src.n_tokens
-                else:
-                    sl = slice((r - 1) * self.B, r * self.B)
-                    win_ptrs, n_tok = grp["rd"].win_ptrs[sl], grp["rd"].n_tokens[sl]
-                api.sparse_attn(p, grp["q"][k, r], grp["sink"][r], win_ptrs, n_tok, src.comp_ptrs,
-                                src.comp_scale_ptrs, grp["idx"], grp["out"][r], self.workspace,
-                                self.dev_status, stream)
+
+            def compress():
+                src.append(grp["kv"][k], grp["gate"][k], ds, stream)
+                if cfg.readers > 1:
+                    grp["rd"].append(grp["kv_rd"][k], None, ds, stream)
+
+            def index():
+                api.index_scores(p, self.max_ncomp, grp["iq"][k], grp["iqs"][k], grp["iw"][k],
+                                 grp["keys"].ptrs, src.n_tokens, grp["scores"], grp["bmax"], ds,
+                                 stream, cuda_cores=self.cuda_core_indexer)
+
+            def select():
+                api.select_topk(p, self.max_ncomp, grp["scores"], grp["bmax"], src.n_tokens,
+                                grp["idx"], grp["n_sel"], ds, stream)
+
+            def attn():
+                for r in range(cfg.readers):
+                    if r == 0:
+                        win_ptrs, n_tok = src.win_ptrs, src.n_tokens
+                    else:
+                        sl = slice((r - 1) * self.B, r * self.B)
+                        win_ptrs, n_tok = grp["rd"].win_ptrs[sl], grp["rd"].n_tokens[sl]
+                    api.sparse_attn(p, grp["q"][k, r], grp["sink"][r], win_ptrs, n_tok,
+                                    src.comp_ptrs, src.comp_scale_ptrs, grp["idx"], grp["out"][r],
+                                    self.workspace, ds, stream)
+
+            self._timed(timers, "compress", st, compress)
+            self._timed(timers, "index", st, index)
+            self._timed(timers, "select", st, select)
+            self._timed(timers, "attn", st, attn)
+
+    def step(self, stream=None, timers=None):
+        """Enqueue the next decode step eagerly (one launch per kernel)."""
+        assert self.step_done < self.n_steps, "more steps than the caches were sized for"
+        self._enqueue(self.step_done % self.n_prep, stream, timers)
+        self.step_done += 1
+
+    def capture(self, with_timers=False):
+        """Capture one CUDA graph per prepared input slot (a whole step each).
+        Returns False if the timers were requested but this torch cannot record
+        events inside a graph."""
+        torch = self.torch
+        self._external_events = False
+        if with_timers:
+            try:
+                torch.cuda.Event(enable_timing=True, external=True)
+                self._external_events = True
+            except TypeError:
+                return False
+        self.graphs, self.graph_timers = [], []
+        cs = torch.cuda.Stream()
+        cs.wait_stream(torch.cuda.current_stream())
+        for k in range(self.n_prep):
+            g = torch.cuda.CUDAGraph()
+            tm = {} if with_timers else None
+            with torch.cuda.graph(g, stream=cs):
+                self._enqueue(k, None, tm)
+            self.graphs.append(g)
+            self.graph_timers.append(tm)
+        torch.cuda.current_stream().wait_stream(cs)
+        return True
+
+    def step_graph(self):
+        """Replay the captured step of the next input slot on the current stream."""
+        assert self.step_done < self.n_steps, "more steps than the caches were sized for"
+        self.graphs[self.step_done % self.n_prep].replay()
         self.step_done += 1
 
     def tokens_after(self, s: int) -> int:
