@@ -10,6 +10,14 @@
 // takes the tied elements with the lowest indices. Level 2 works on a copy of
 // the candidate keys in shared memory; its candidate list is ascending by
 // position, so the output comes out ascending by construction.
+//
+// Level 1 keeps 2,047 of up to 65,535 blocks, so it first narrows the field:
+// a threshold estimated from a strided sample of 2,048 block maxima, one pass
+// that keeps the blocks at or above it (in index order, in shared memory), and
+// the exact select among those. The answer is unchanged because the top 2,047
+// all lie at or above any threshold that at least 2,047 blocks reach; when the
+// count falls outside [2,047, kMaxFiltered] the threshold moves, and after a
+// few tries the exact select runs over all blocks in global memory.
 #include "common.cuh"
 
 namespace csa2 {
@@ -19,12 +27,19 @@ constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCand = kKb * kBlk;  // 16384
 
+constexpr int kSample = 2048;
+constexpr int kMaxFiltered = 8192;
+constexpr int kSample2 = 1024;       // level 2 sample (stored at the end of cand_idx)
+constexpr int kMaxFiltered2 = 4096;
+
 struct SelShared {
     uint32_t hist[256];
     uint32_t warp_sum[kWarps];
     int32_t bcast[4];
     int32_t kept[kKb];
-    uint32_t cand[kMaxCand];
+    uint32_t cand[kMaxCand];        // level 2 keys; level 1: filtered keys, sample at the end
+    int32_t cand_idx[kMaxFiltered];  // index of each filtered key; level 2 sample at the end
+    uint32_t cand2[kMaxFiltered2];   // level 2 filtered keys
 };
 
 __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
@@ -37,36 +52,32 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
     return v;
 }
 
-// Exclusive prefix sum of one value per thread over the CTA (in thread order).
-__device__ uint32_t block_excl_scan(uint32_t v, SelShared& sh) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint32_t incl = warp_incl_scan(v);
-    if (lane == 31) sh.warp_sum[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        const uint32_t x = sh.warp_sum[lane];
-        const uint32_t xi = warp_incl_scan(x);
-        sh.warp_sum[lane] = xi - x;
-    }
-    __syncthreads();
-    const uint32_t r = sh.warp_sum[warp] + incl - v;
-    __syncthreads();
-    return r;
-}
-
 // K-th largest key among n keys (1 <= K <= n). On return *need_eq is how many
 // elements equal to the K-th key belong to the top K.
+// With digits < 4 only the top 8*digits bits are resolved: the result is the
+// K-th largest key with its low bits cleared, a lower bound that at least K keys
+// reach (used as a filter threshold).
 template <class KeyAt>
-__device__ uint32_t radix_kth(int n, int K, KeyAt key_at, SelShared& sh, int* need_eq) {
+__device__ uint32_t radix_kth(int n, int K, KeyAt key_at, SelShared& sh, int* need_eq,
+                              int digits = 4) {
     const int tid = threadIdx.x, lane = tid & 31;
     uint32_t prefix = 0, mask = 0;
     int remaining = K;
-    for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int shift = 24; shift >= 32 - 8 * digits; shift -= 8) {
         if (tid < 256) sh.hist[tid] = 0;
         __syncthreads();
-        for (int i = tid; i < n; i += kThreads) {
-            const uint32_t k = key_at(i);
-            if ((k & mask) == prefix) atomicAdd(&sh.hist[(k >> shift) & 255u], 1u);
+        // warp-aggregated: one shared atomic per distinct digit per warp (scores share
+        // sign and exponent, so most keys of a pass land in very few bins)
+        for (int base = 0; base < n; base += kThreads) {
+            const int i = base + tid;
+            const uint32_t k = i < n ? key_at(i) : 0u;
+            const bool active = i < n && (k & mask) == prefix;
+            const uint32_t am = __ballot_sync(0xffffffffu, active);
+            if (active) {
+                const uint32_t d = (k >> shift) & 255u;
+                const uint32_t peers = __match_any_sync(am, d);
+                if (lane == __ffs(peers) - 1) atomicAdd(&sh.hist[d], (uint32_t)__popc(peers));
+            }
         }
         __syncthreads();
         if (tid < 32) {
@@ -101,35 +112,123 @@ __device__ uint32_t radix_kth(int n, int K, KeyAt key_at, SelShared& sh, int* ne
     return prefix;
 }
 
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Exclusive scan of one value per warp (lane 0 holds it) over the CTA's warps;
+// every lane of warp w receives the sum over warps < w. *total gets the sum.
+__device__ uint32_t warp_excl_scan(uint32_t v, SelShared& sh, uint32_t* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) sh.warp_sum[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t x = sh.warp_sum[lane];
+        const uint32_t xi = warp_incl_scan(x);
+        sh.warp_sum[lane] = xi - x;
+        if (lane == 31) sh.bcast[3] = (int)xi;
+    }
+    __syncthreads();
+    const uint32_t r = sh.warp_sum[warp];
+    *total = (uint32_t)sh.bcast[3];
+    __syncthreads();
+    return r;
+}
+
 // Marks the top K of n keys (ties -> lower index) and writes the marked
-// indices, in ascending order, through emit(rank, i). Each thread owns a
-// contiguous chunk of indices so that tie ranks follow index order.
+// indices, in ascending order, through emit(rank, i). Each warp owns a
+// contiguous range of indices and walks it 32 at a time (coalesced), so tie
+// ranks and output ranks follow index order via ballots.
 template <class KeyAt, class Emit>
 __device__ void select_top(int n, int K, KeyAt key_at, Emit emit, SelShared& sh) {
     int need_eq;
     const uint32_t kth = radix_kth(n, K, key_at, sh, &need_eq);
-    const int chunk = (n + kThreads - 1) / kThreads;
-    const int i0 = min(n, (int)threadIdx.x * chunk), i1 = min(n, i0 + chunk);
-    uint32_t n_eq = 0;
-    for (int i = i0; i < i1; ++i) n_eq += key_at(i) == kth;
-    uint32_t eq_rank = block_excl_scan(n_eq, sh);
-    uint32_t n_sel = 0;
-    {
-        uint32_t r = eq_rank;
-        for (int i = i0; i < i1; ++i) {
-            const uint32_t k = key_at(i);
-            n_sel += (k > kth) || (k == kth && r++ < (uint32_t)need_eq);
-        }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t lt = lanemask_lt();
+    const int R = (n + kWarps - 1) / kWarps;
+    const int w0 = min(n, warp * R), w1 = min(n, w0 + R);
+    uint32_t n_gt = 0, n_eq = 0;
+    for (int base = w0; base < w1; base += 32) {
+        const int i = base + lane;
+        const uint32_t k = i < w1 ? key_at(i) : 0u;
+        n_gt += __popc(__ballot_sync(0xffffffffu, i < w1 && k > kth));
+        n_eq += __popc(__ballot_sync(0xffffffffu, i < w1 && k == kth));
     }
-    uint32_t out = block_excl_scan(n_sel, sh);
-    for (int i = i0; i < i1; ++i) {
-        const uint32_t k = key_at(i);
-        if ((k > kth) || (k == kth && eq_rank++ < (uint32_t)need_eq)) emit(out++, i);
+    uint32_t tot;
+    const uint32_t eq_off = warp_excl_scan(n_eq, sh, &tot);
+    const int take_eq = max(0, min((int)n_eq, need_eq - (int)eq_off));
+    uint32_t out = warp_excl_scan(n_gt + (uint32_t)take_eq, sh, &tot);
+    uint32_t r_eq = eq_off;
+    for (int base = w0; base < w1; base += 32) {
+        const int i = base + lane;
+        const uint32_t k = i < w1 ? key_at(i) : 0u;
+        const bool gt = i < w1 && k > kth, eq = i < w1 && k == kth;
+        const uint32_t eqm = __ballot_sync(0xffffffffu, eq);
+        const bool take = gt || (eq && r_eq + __popc(eqm & lt) < (uint32_t)need_eq);
+        const uint32_t tm = __ballot_sync(0xffffffffu, take);
+        if (take) emit(out + __popc(tm & lt), i);
+        out += __popc(tm);
+        r_eq += __popc(eqm);
     }
     __syncthreads();
 }
 
-__global__ void __launch_bounds__(kThreads)
+
+// Keys at or above thr among key_at(0..n), kept in index order: (key, index)
+// pairs written to keys_out/idx_out (capacity cap). Each warp walks its own
+// contiguous range, 8 x 32 elements per round with the loads issued first.
+// Returns the count (which may exceed cap: then nothing was written).
+template <class KeyAt>
+__device__ int filter_ge(int n, uint32_t thr, KeyAt key_at, uint32_t* keys_out, int32_t* idx_out,
+                         int cap, SelShared& sh) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t lt = lanemask_lt();
+    const int R = (n + kWarps - 1) / kWarps;
+    const int w0 = min(n, warp * R), w1 = min(n, w0 + R);
+    constexpr int U = 8;
+    uint32_t c = 0;
+    for (int base = w0; base < w1; base += 32 * U) {
+        uint32_t k[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + 32 * u + lane;
+            k[u] = i < w1 ? key_at(i) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + 32 * u + lane;
+            c += __popc(__ballot_sync(0xffffffffu, i < w1 && k[u] >= thr));
+        }
+    }
+    uint32_t total;
+    uint32_t o = warp_excl_scan(c, sh, &total);
+    if ((int)total > cap) return (int)total;
+    for (int base = w0; base < w1; base += 32 * U) {
+        uint32_t k[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + 32 * u + lane;
+            k[u] = i < w1 ? key_at(i) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + 32 * u + lane;
+            const bool keep = i < w1 && k[u] >= thr;
+            const uint32_t m = __ballot_sync(0xffffffffu, keep);
+            if (keep) {
+                keys_out[o + __popc(m & lt)] = k[u];
+                idx_out[o + __popc(m & lt)] = i;
+            }
+            o += __popc(m);
+        }
+    }
+    __syncthreads();
+    return (int)total;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
 k_select_topk(int64_t max_ncomp, int ratio, const float* __restrict__ scores,
               const float* __restrict__ block_max, const int32_t* __restrict__ n_tokens,
               int32_t* idx, int32_t* n_sel_out, int32_t* dev_status) {
@@ -155,9 +254,43 @@ k_select_topk(int64_t max_ncomp, int ratio, const float* __restrict__ scores,
         n_kept = n_b;
     } else {
         // best K_b - 1 among blocks [0, n_b - 1), then the newest block n_b - 1
-        select_top(
-            n_b - 1, kKb - 1, [&](int i) { return score_key(bm[i]); },
-            [&](uint32_t r, int i) { sh.kept[r] = i; }, sh);
+        const int n1 = n_b - 1, K1 = kKb - 1;
+        // (a) threshold from a strided sample: the r-th largest sample key, r chosen so
+        //     that about 1.5 K1 blocks of all n1 reach it
+        for (int i = tid; i < kSample; i += kThreads)
+            sh.cand[kMaxCand - kSample + i] = score_key(bm[(int64_t)i * n1 / kSample]);
+        __syncthreads();
+        int r = (int)(1.5f * K1 * kSample / n1) + 1;
+        bool done = false;
+        for (int attempt = 0; attempt < 4 && !done; ++attempt) {
+            r = max(1, min(kSample, r));
+            int unused;
+            // the top 16 bits of the r-th largest sample key: a slightly lower threshold
+            const uint32_t thr = radix_kth(kSample, r, [&](int i) { return sh.cand[kMaxCand - kSample + i]; },
+                                           sh, &unused, 2);
+            const int total = filter_ge(
+                n1, thr, [&](int i) { return score_key(bm[i]); }, sh.cand, sh.cand_idx,
+                kMaxFiltered, sh);
+            if (total < K1) {          // threshold too high: take a lower sample rank
+                r = r * 2 + 8;
+                continue;
+            }
+            if (total > kMaxFiltered) {  // too many candidates: take a higher sample rank
+                if (r <= 1) break;
+                r = r / 2;
+                continue;
+            }
+            select_top(
+                total, K1, [&](int i) { return sh.cand[i]; },
+                [&](uint32_t rank, int i) { sh.kept[rank] = sh.cand_idx[i]; }, sh);
+            done = true;
+        }
+        if (!done) {  // exact select over every block, read from global memory
+            __syncthreads();
+            select_top(
+                n1, K1, [&](int i) { return score_key(bm[i]); },
+                [&](uint32_t rank, int i) { sh.kept[rank] = i; }, sh);
+        }
         if (tid == 0) sh.kept[kKb - 1] = n_b - 1;
         n_kept = kKb;
     }
@@ -170,12 +303,47 @@ k_select_topk(int64_t max_ncomp, int ratio, const float* __restrict__ scores,
         sh.cand[i] = score_key(sc[sh.kept[i / kBlk] * kBlk + (i % kBlk)]);
     for (int i = tid; i < kKp; i += kThreads) out[i] = -1;
     __syncthreads();
+    auto pos_of = [&](int i) { return sh.kept[i / kBlk] * kBlk + i % kBlk; };
     if (n_cand <= kKp) {
-        for (int i = tid; i < n_cand; i += kThreads) out[i] = sh.kept[i / kBlk] * kBlk + i % kBlk;
+        for (int i = tid; i < n_cand; i += kThreads) out[i] = pos_of(i);
     } else {
-        select_top(
-            n_cand, kKp, [&](int i) { return sh.cand[i]; },
-            [&](uint32_t r, int i) { out[r] = sh.kept[i / kBlk] * kBlk + i % kBlk; }, sh);
+        // sample -> threshold -> filter -> exact select, as at level 1
+        bool done = false;
+        if (n_cand > 2 * kSample2) {
+            uint32_t* sample = reinterpret_cast<uint32_t*>(sh.cand_idx) + kMaxFiltered - kSample2;
+            for (int i = tid; i < kSample2; i += kThreads)
+                sample[i] = sh.cand[(int64_t)i * n_cand / kSample2];
+            __syncthreads();
+            int r = (int)(1.5f * kKp * kSample2 / n_cand) + 1;
+            for (int attempt = 0; attempt < 4 && !done; ++attempt) {
+                r = max(1, min(kSample2, r));
+                int unused;
+                const uint32_t thr = radix_kth(kSample2, r, [&](int i) { return sample[i]; }, sh,
+                                               &unused, 2);
+                const int total = filter_ge(
+                    n_cand, thr, [&](int i) { return sh.cand[i]; }, sh.cand2, sh.cand_idx,
+                    kMaxFiltered2, sh);
+                if (total < kKp) {
+                    r = r * 2 + 8;
+                    continue;
+                }
+                if (total > kMaxFiltered2) {
+                    if (r <= 1) break;
+                    r = r / 2;
+                    continue;
+                }
+                select_top(
+                    total, kKp, [&](int i) { return sh.cand2[i]; },
+                    [&](uint32_t rank, int i) { out[rank] = pos_of(sh.cand_idx[i]); }, sh);
+                done = true;
+            }
+        }
+        if (!done) {
+            __syncthreads();
+            select_top(
+                n_cand, kKp, [&](int i) { return sh.cand[i]; },
+                [&](uint32_t rank, int i) { out[rank] = pos_of(i); }, sh);
+        }
     }
     if (tid == 0 && n_sel_out) n_sel_out[b] = min(n_cand, kKp);
 }
