@@ -111,6 +111,17 @@ def sparse_attn(params, q, sink, win_ptrs, n_tokens, comp_ptrs, comp_scale_ptrs,
         "sparse_attn")
 
 
+def sparse_attn_layers(params, q, sink, win_ptrs, n_tokens, comp_ptrs, comp_scale_ptrs, idx, out,
+                       dev_status=None, stream=None):
+    """L layers sharing one compressed cache and selection: q/out [L, B, H, D] bf16,
+    sink [L, H], win_ptrs [L*B] (layer-major), n_tokens [B]."""
+    L, B = q.shape[0], q.shape[1]
+    check(lib().csa2_sparse_attn_layers(
+        ctypes.byref(params), L, B, _ptr(q), _ptr(sink), _ptr(win_ptrs), _ptr(n_tokens),
+        _ptr(comp_ptrs), _ptr(comp_scale_ptrs), _ptr(idx), _ptr(out), _ptr(dev_status),
+        _stream(stream)), "sparse_attn_layers")
+
+
 def sparse_attn_noalloc(params, q, sink, win_ptrs, n_tokens, comp_ptrs, comp_scale_ptrs, idx, out,
                         dev_status=None, stream=None):
     """csa2_sparse_attn without a workspace: for callers that cannot allocate device

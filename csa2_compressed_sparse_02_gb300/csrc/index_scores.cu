@@ -14,8 +14,9 @@
 // per lane (32 heads), apply ReLU and the head weights, and reduce the block
 // maximum over 8 adjacent lanes. One persistent CTA per SM; warps 0-7 epilogue
 // (two warpgroups taking alternate super-tiles), warp 8 loads (one bulk copy
-// per super-tile of 4 tiles into a 5-stage ring), warp 9 issues the MMAs;
-// three super-tile accumulator sets in TMEM so epilogues overlap the MMAs.
+// per super-tile of 4 tiles into a 5-stage ring), warps 9 and 10 issue the
+// MMAs of alternate super-tiles (a single issuing thread serialises each scale
+// copy with its MMA; two overlap them), each into its own TMEM accumulators.
 //
 // CUDA-core build (k_index_scores_cc): one thread per position, 32 fp32
 // accumulators, the query decoded once per CTA into shared memory.
@@ -165,15 +166,16 @@ k_index_scores_cc(int64_t max_ncomp, int ratio, const uint8_t* __restrict__ q_va
 constexpr int kTilesPerStage = 4;
 constexpr int kStageBytes = kTilesPerStage * kKeyTileBytes;  // 36,864 = 36 x 1024
 constexpr int kStages = 5;
-constexpr int kAcc = 3;          // super-tile accumulators in flight between MMA and epilogue
+constexpr int kIssuers = 2;      // MMA-issuing warps, alternating super-tiles
+constexpr int kAcc = kIssuers;   // one super-tile accumulator set per issuer
 constexpr int kEpiGroups = 2;    // epilogue warpgroups, alternating super-tiles
 constexpr int kLoadWarp = 4 * kEpiGroups, kMmaWarp = kLoadWarp + 1;
-constexpr int kTcThreads = 32 * (kMmaWarp + 1);  // warps 0-7 epilogue, 8 loader, 9 MMA
+constexpr int kTcThreads = 32 * (kMmaWarp + kIssuers);  // 0-7 epilogue, 8 loader, 9-10 MMA
 constexpr int kMaxSeq = 1024;
 constexpr uint32_t kTmemCols = 512;
-// TMEM columns: D[kAcc][kTilesPerStage] x 32, then SFA[kAcc][kTilesPerStage] x 8, then SFB[2] x 8
+// TMEM columns: D[kAcc][kTilesPerStage] x 32, SFA[kAcc][kTilesPerStage] x 8, SFB[kIssuers][2] x 8
 constexpr uint32_t kColD = 0, kColSFA = 32 * kAcc * kTilesPerStage, kColSFB = kColSFA + 8 * kAcc * kTilesPerStage;
-static_assert(kColSFB + 16 <= kTmemCols, "TMEM columns");
+static_assert(kColSFB + 16 * kIssuers <= kTmemCols, "TMEM columns");
 // Instruction descriptor: kind::mxf4nvf4, A and B E2M1 (1), K-major, dense,
 // N = 32 (N>>3 in bits 17..22), UE4M3 scales (bit 23 = 0), M = 128 (M>>4 in bits 24..28).
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((32u >> 3) << 17) | ((128u >> 4) << 24);
@@ -222,13 +224,13 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.qfull[i], 1);
-            mbar_init(&sh.qempty[i], 1);
+            mbar_init(&sh.qempty[i], kIssuers);
         }
         for (int i = 0; i < kAcc; ++i) {
             mbar_init(&sh.accf[i], 1);
             mbar_init(&sh.acce[i], 4);
         }
-        mbar_init(&sh.done, 1);
+        mbar_init(&sh.done, kIssuers);
         sh.abort = 0;
         fence_mbar_init();
     }
@@ -255,7 +257,7 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
         }
         if (lane == 31) sh.prefix[B] = incl;
     }
-    if (warp == kMmaWarp) {
+    if (warp == kMmaWarp) {  // the first MMA warp owns the TMEM allocation
         tmem_alloc(&sh.tmem_base, kTmemCols);
         tmem_relinquish();
     }
@@ -310,17 +312,16 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
             for (uint32_t k = 0; k < kSpinLimit; ++k)
                 if (mbar_try_wait(&sh.full[j % kStages], (uint32_t)((j / kStages) & 1))) break;
         }
-    } else if (warp == kMmaWarp) {
-        // ---------------- MMA issuer (one thread)
+    } else if (warp >= kMmaWarp) {
+        // ---------------- MMA issuers: warp kMmaWarp + e issues super-tiles i with
+        // i % kIssuers == e (a single thread each); every issuer copies the query
+        // scale factors of every sequence segment into its own TMEM slots.
+        const int e = warp - kMmaWarp;
         if (lane == 0) {
             int seg = -1, b = 0, prev_b = -1;
             for (int64_t f = f0; f < f1; ++f) {
                 b = advance_seq(sh, b, f);
                 const int64_t i = f - f0;
-                const int s = (int)(i % kStages), a = (int)(i % kAcc);
-                if (!mbar_wait(&sh.full[s], (uint32_t)((i / kStages) & 1), abort)) break;
-                if (!mbar_wait(&sh.acce[a], (uint32_t)((i / kAcc) & 1) ^ 1, abort)) break;
-                tc_fence_after();
                 if (b != prev_b) {
                     if (seg >= 0) tc_commit(&sh.qempty[seg & 1]);
                     ++seg;
@@ -328,14 +329,19 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
                     if (!mbar_wait(&sh.qfull[qs], (uint32_t)((seg >> 1) & 1), abort)) break;
                     tc_fence_after();
                     const uint32_t sfb = smem_u32(sh.sfb[qs]);
-                    tmem_cp_32x128b_x4(tmem + kColSFB + 8 * qs, smem_desc(sfb, 128, 128, kLayoutNone));
-                    tmem_cp_32x128b_x4(tmem + kColSFB + 8 * qs + 4,
-                                       smem_desc(sfb + 512, 128, 128, kLayoutNone));
+                    const uint32_t col = tmem + kColSFB + 16 * e + 8 * qs;
+                    tmem_cp_32x128b_x4(col, smem_desc(sfb, 128, 128, kLayoutNone));
+                    tmem_cp_32x128b_x4(col + 4, smem_desc(sfb + 512, 128, 128, kLayoutNone));
                     prev_b = b;
                 }
+                if ((int)(i % kIssuers) != e) continue;
+                const int s = (int)(i % kStages), a = (int)(i % kAcc);
+                if (!mbar_wait(&sh.full[s], (uint32_t)((i / kStages) & 1), abort)) break;
+                if (!mbar_wait(&sh.acce[a], (uint32_t)((i / kAcc) & 1) ^ 1, abort)) break;
+                tc_fence_after();
                 const int qs = seg & 1;
                 const uint32_t qa = smem_u32(sh.q[qs]);
-                const uint32_t sfb = tmem + kColSFB + 8 * qs;
+                const uint32_t sfb = tmem + kColSFB + 16 * e + 8 * qs;
                 const int nt = tiles_in(f - sh.prefix[b], sh.ncomp[b]);
                 for (int j = 0; j < nt; ++j) {
                     const uint32_t st = smem_u32(sh.stage[s]) + j * kKeyTileBytes;

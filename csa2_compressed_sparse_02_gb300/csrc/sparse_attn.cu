@@ -423,6 +423,263 @@ k_sparse_attn_merge(const float* __restrict__ sink, const float* __restrict__ ws
     }
 }
 
+// ---- fused multi-layer flash-decode (bf16 tensor cores, output in registers) ----
+// One CTA per (layer, sequence): 64 query heads x all 640 positions, streamed
+// as 10 chunks of 64 positions (2 window chunks, 8 compressed chunks) with an
+// online softmax. The output O[64 x 512] lives in registers: warp w owns rows
+// 16*(w%4).. and dims 128*(w/4).. (16 mma n-tiles, 64 fp32 per thread). The
+// next chunk's raw bytes are loaded into registers while the current chunk is
+// multiplied, then decoded exactly into bf16 shared memory. The sink joins the
+// denominator once at the end; no workspace, no merge pass. All L layers of a
+// launch share the compressed cache and the selected indices.
+constexpr int kFdWarps = 16;
+constexpr int kFdThreads = 32 * kFdWarps;
+constexpr int kFdChunk = 64;
+constexpr int kFdChunks = (kW + kKp) / kFdChunk;  // 10
+constexpr int kFdOffQ = 0;                                  // 64 x 1024 B
+constexpr int kFdOffKV = kFdOffQ + kH * kD * 2;             // 2 x 64 x 1024 B
+constexpr int kFdOffP = kFdOffKV + 2 * kFdChunk * kD * 2;    // 64 x 128 B
+constexpr int kFdOffMax = kFdOffP + kH * kFdChunk * 2;       // float [4][64]
+constexpr int kFdOffSum = kFdOffMax + 4 * kH * 4;            // float [4][64]
+constexpr int kFdOffValid = kFdOffSum + 4 * kH * 4;          // int [2][64]
+constexpr int kSmemFd = kFdOffValid + 2 * kFdChunk * 4;
+
+// Raw bytes of 4 rows of a chunk, per lane (the warp covers one row per step).
+struct FdRaw {
+    uint4 v[4];       // window: 16 E4M3 bytes; compressed: .x/.y = 8 E2M1 bytes
+    uint32_t sc;      // compressed: the lane's group-scale byte, 4 rows packed
+    uint32_t valid;   // bit r: row r of the 4 is valid
+};
+
+__device__ __forceinline__ void fd_load(FdRaw& raw, int c, int warp, int lane, int64_t T,
+                                        int64_t n_c, const uint8_t* win, const uint8_t* comp,
+                                        const uint8_t* comp_sc, const int32_t* idx,
+                                        int32_t* dev_status) {
+    raw.valid = 0;
+    raw.sc = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int r = warp * 4 + k;  // row within the chunk
+        raw.v[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (c < kW / kFdChunk) {  // window chunk: ring slot c*64 + r
+            const int slot = c * kFdChunk + r;
+            if (T > 0 && window_slot_valid(slot, T)) {
+                raw.v[k] = *reinterpret_cast<const uint4*>(win + (int64_t)slot * kD + 16 * lane);
+                raw.valid |= 1u << k;
+            }
+        } else {
+            const int64_t j = idx[(c - kW / kFdChunk) * kFdChunk + r];
+            if (j >= n_c && lane == 0) raise_status(dev_status, CSA2_DEV_BAD_INDEX);
+            if (j >= 0 && j < n_c) {
+                const uint2 v = *reinterpret_cast<const uint2*>(comp + j * (kD / 2) + 8 * lane);
+                raw.v[k] = make_uint4(v.x, v.y, 0u, 0u);
+                raw.sc |= (uint32_t)comp_sc[j * (kD / kGroup) + lane] << (8 * k);
+                raw.valid |= 1u << k;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void fd_store(const FdRaw& raw, int c, int warp, int lane,
+                                         unsigned char* sKV, int* sValid) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int r = warp * 4 + k;
+        uint32_t o[8];
+        const bool valid = (raw.valid >> k) & 1u;
+        if (valid && c < kW / kFdChunk) {
+            e4m3x16_to_bf16(raw.v[k], o);
+        } else if (valid) {
+            nvfp4x16_to_bf16(make_uint2(raw.v[k].x, raw.v[k].y),
+                             e4m3_value((uint8_t)(raw.sc >> (8 * k))), o);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[i] = 0u;
+        }
+        if (c < kW / kFdChunk) {  // window row: lane covers dims 16*lane..+15 = chunks 2l, 2l+1
+            *reinterpret_cast<uint4*>(sKV + swz(r, 2 * lane, 64)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(sKV + swz(r, 2 * lane + 1, 64)) = make_uint4(o[4], o[5], o[6], o[7]);
+        } else {  // compressed row: lane covers its 16-element group = dims 16*lane..+15
+            *reinterpret_cast<uint4*>(sKV + swz(r, 2 * lane, 64)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(sKV + swz(r, 2 * lane + 1, 64)) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        if (lane == 0) sValid[r] = valid;
+    }
+}
+
+__global__ void __launch_bounds__(kFdThreads, 1)
+k_sparse_attn_fd(int B, const __nv_bfloat16* __restrict__ q, const float* __restrict__ sink,
+                 const void* const* win, const int32_t* __restrict__ n_tokens,
+                 const void* const* comp, const uint8_t* const* comp_scales,
+                 const int32_t* __restrict__ idx, int ratio, float scale_log2,
+                 __nv_bfloat16* out, int32_t* dev_status) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    const int layer = blockIdx.x, b = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int wm = warp & 3, wn = warp >> 2;  // row group (16 heads), column group
+    const int g = lane >> 2, t = lane & 3;
+    unsigned char* sQ = smem + kFdOffQ;
+    unsigned char* sP = smem + kFdOffP;
+    float* sMax = reinterpret_cast<float*>(smem + kFdOffMax);
+    float* sSum = reinterpret_cast<float*>(smem + kFdOffSum);
+    int* sValid = reinterpret_cast<int*>(smem + kFdOffValid);
+    const int64_t T = n_tokens[b];
+    const int64_t n_c = T / ratio;
+    const int64_t lb = (int64_t)layer * B + b;
+    const uint8_t* winb = static_cast<const uint8_t*>(win[lb]);
+    const uint8_t* compb = static_cast<const uint8_t*>(comp[b]);
+    const uint8_t* compsb = comp_scales[b];
+    const int32_t* idxb = idx + (int64_t)b * kKp;
+
+    // ---- Q -> shared (async), chunk 0 -> shared ----
+    const unsigned char* qb = reinterpret_cast<const unsigned char*>(q + lb * kH * kD);
+    for (int e = tid; e < kH * (kD / 8); e += kFdThreads) {
+        const int r = e / (kD / 8), c = e % (kD / 8);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(sQ + swz(r, c, 64))),
+                     "l"(qb + (int64_t)e * 16));
+    }
+    asm volatile("cp.async.commit_group;\n");
+    FdRaw raw;
+    fd_load(raw, 0, warp, lane, T, n_c, winb, compb, compsb, idxb, dev_status);
+    fd_store(raw, 0, warp, lane, smem + kFdOffKV, sValid);
+    asm volatile("cp.async.wait_all;\n");
+
+    float o_acc[16][4];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) o_acc[j][0] = o_acc[j][1] = o_acc[j][2] = o_acc[j][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows 16wm+g, +8
+    const uint32_t sQ_u = smem_u32(sQ), sP_u = smem_u32(sP);
+
+    for (int c = 0; c < kFdChunks; ++c) {
+        __syncthreads();  // chunk c in sKV[c&1] and its sValid are complete
+        unsigned char* sKV = smem + kFdOffKV + (c & 1) * (kFdChunk * kD * 2);
+        const int* vld = sValid + (c & 1) * kFdChunk;
+        const uint32_t sKV_u = smem_u32(sKV);
+        if (c + 1 < kFdChunks)
+            fd_load(raw, c + 1, warp, lane, T, n_c, winb, compb, compsb, idxb, dev_status);
+
+        // ---- S = Q K^T for rows 16wm.., positions 16wn.. (2 n-tiles) ----
+        float s_acc[2][4];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) s_acc[j][0] = s_acc[j][1] = s_acc[j][2] = s_acc[j][3] = 0.f;
+#pragma unroll 4
+        for (int kk = 0; kk < kD / 16; ++kk) {
+            uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+            ldsm_x4(sQ_u + swz(16 * wm + (lane & 15), 2 * kk + (lane >> 4), 64), a0, a1, a2, a3);
+            ldsm_x4(sKV_u + swz(16 * wn + (lane & 7) + ((lane >> 4) << 3), 2 * kk + ((lane >> 3) & 1), 64),
+                    b0, b1, b2, b3);
+            mma_bf16(s_acc[0], a0, a1, a2, a3, b0, b1);
+            mma_bf16(s_acc[1], a0, a1, a2, a3, b2, b3);
+        }
+        // ---- online softmax (log2 domain) ----
+        float cm0 = -INFINITY, cm1 = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int col = 16 * wn + 8 * j + 2 * t;
+            const bool v0 = vld[col], v1 = vld[col + 1];
+            s_acc[j][0] = v0 ? s_acc[j][0] * scale_log2 : -INFINITY;
+            s_acc[j][1] = v1 ? s_acc[j][1] * scale_log2 : -INFINITY;
+            s_acc[j][2] = v0 ? s_acc[j][2] * scale_log2 : -INFINITY;
+            s_acc[j][3] = v1 ? s_acc[j][3] * scale_log2 : -INFINITY;
+            cm0 = fmaxf(cm0, fmaxf(s_acc[j][0], s_acc[j][1]));
+            cm1 = fmaxf(cm1, fmaxf(s_acc[j][2], s_acc[j][3]));
+        }
+        cm0 = fmaxf(cm0, __shfl_xor_sync(0xffffffffu, cm0, 1));
+        cm0 = fmaxf(cm0, __shfl_xor_sync(0xffffffffu, cm0, 2));
+        cm1 = fmaxf(cm1, __shfl_xor_sync(0xffffffffu, cm1, 1));
+        cm1 = fmaxf(cm1, __shfl_xor_sync(0xffffffffu, cm1, 2));
+        if (t == 0) {
+            sMax[wn * kH + 16 * wm + g] = cm0;
+            sMax[wn * kH + 16 * wm + g + 8] = cm1;
+        }
+        __syncthreads();
+        float n0 = m0, n1 = m1;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            n0 = fmaxf(n0, sMax[k * kH + 16 * wm + g]);
+            n1 = fmaxf(n1, sMax[k * kH + 16 * wm + g + 8]);
+        }
+        const float al0 = n0 == -INFINITY ? 1.f : exp2f(m0 - n0);
+        const float al1 = n1 == -INFINITY ? 1.f : exp2f(m1 - n1);
+        const float base0 = n0 == -INFINITY ? 0.f : n0, base1 = n1 == -INFINITY ? 0.f : n1;
+        float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const __nv_bfloat162 p01 = __floats2bfloat162_rn(exp2f(s_acc[j][0] - base0),
+                                                             exp2f(s_acc[j][1] - base0));
+            const __nv_bfloat162 p23 = __floats2bfloat162_rn(exp2f(s_acc[j][2] - base1),
+                                                             exp2f(s_acc[j][3] - base1));
+            const float2 f01 = __bfloat1622float2(p01), f23 = __bfloat1622float2(p23);
+            ps0 += f01.x + f01.y;
+            ps1 += f23.x + f23.y;
+            const int col = 16 * wn + 8 * j + 2 * t;
+            *reinterpret_cast<__nv_bfloat162*>(sP + swz(16 * wm + g, col >> 3, 8) + (col & 7) * 2) = p01;
+            *reinterpret_cast<__nv_bfloat162*>(sP + swz(16 * wm + g + 8, col >> 3, 8) + (col & 7) * 2) = p23;
+        }
+        ps0 += __shfl_xor_sync(0xffffffffu, ps0, 1);
+        ps0 += __shfl_xor_sync(0xffffffffu, ps0, 2);
+        ps1 += __shfl_xor_sync(0xffffffffu, ps1, 1);
+        ps1 += __shfl_xor_sync(0xffffffffu, ps1, 2);
+        if (t == 0) {
+            sSum[wn * kH + 16 * wm + g] = ps0;
+            sSum[wn * kH + 16 * wm + g + 8] = ps1;
+        }
+        __syncthreads();
+        float cs0 = 0.f, cs1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            cs0 += sSum[k * kH + 16 * wm + g];
+            cs1 += sSum[k * kH + 16 * wm + g + 8];
+        }
+        l0 = l0 * al0 + cs0;
+        l1 = l1 * al1 + cs1;
+        m0 = n0;
+        m1 = n1;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            o_acc[j][0] *= al0;
+            o_acc[j][1] *= al0;
+            o_acc[j][2] *= al1;
+            o_acc[j][3] *= al1;
+        }
+        // ---- O += P V for rows 16wm.., dims 128wn.. (16 n-tiles), 64 positions ----
+#pragma unroll
+        for (int kk = 0; kk < kFdChunk / 16; ++kk) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4(sP_u + swz(16 * wm + (lane & 15), 2 * kk + (lane >> 4), 8), a0, a1, a2, a3);
+#pragma unroll
+            for (int jp = 0; jp < 8; ++jp) {
+                uint32_t b0, b1, b2, b3;
+                const int prow = 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
+                ldsm_x4_t(sKV_u + swz(prow, 16 * wn + 2 * jp + (lane >> 4), 64), b0, b1, b2, b3);
+                mma_bf16(o_acc[2 * jp], a0, a1, a2, a3, b0, b1);
+                mma_bf16(o_acc[2 * jp + 1], a0, a1, a2, a3, b2, b3);
+            }
+        }
+        if (c + 1 < kFdChunks)
+            fd_store(raw, c + 1, warp, lane, smem + kFdOffKV + ((c + 1) & 1) * (kFdChunk * kD * 2),
+                     sValid + ((c + 1) & 1) * kFdChunk);
+    }
+
+    // ---- sink and normalisation, bf16 out ----
+    const float sink2 = sink[(int64_t)layer * kH + 16 * wm + g] * kLog2e;
+    const float sink2b = sink[(int64_t)layer * kH + 16 * wm + g + 8] * kLog2e;
+    const float M0 = fmaxf(m0, sink2), M1 = fmaxf(m1, sink2b);
+    const float sc0 = m0 == -INFINITY ? 0.f : exp2f(m0 - M0);
+    const float sc1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M1);
+    const float f0 = sc0 / (l0 * sc0 + exp2f(sink2 - M0));
+    const float f1 = sc1 / (l1 * sc1 + exp2f(sink2b - M1));
+    __nv_bfloat16* ob = out + lb * kH * kD;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const int col = 128 * wn + 8 * j + 2 * t;
+        *reinterpret_cast<uint32_t*>(ob + (int64_t)(16 * wm + g) * kD + col) =
+            pack_bf16(o_acc[j][0] * f0, o_acc[j][1] * f0);
+        *reinterpret_cast<uint32_t*>(ob + (int64_t)(16 * wm + g + 8) * kD + col) =
+            pack_bf16(o_acc[j][2] * f1, o_acc[j][3] * f1);
+    }
+}
+
 size_t ws_o_bytes(int B) { return (size_t)B * kSplits * kH * kD * sizeof(float); }
 size_t ws_ml_bytes(int B) { return (size_t)B * kSplits * kH * sizeof(float2); }
 
@@ -435,6 +692,37 @@ extern "C" size_t csa2_sparse_attn_workspace_size(const csa2_params* p, int B) {
     (void)p;
     if (B <= 0) return 0;
     return ws_o_bytes(B) + ws_ml_bytes(B);
+}
+
+extern "C" int csa2_sparse_attn_layers(const csa2_params* p, int L, int B, const void* q,
+                                       const float* sink, const void* const* win,
+                                       const int32_t* n_tokens, const void* const* comp,
+                                       const uint8_t* const* comp_scales, const int32_t* idx,
+                                       void* out, int32_t* dev_status, void* stream) {
+    CSA2_CHECK_PARAMS(p);
+    if (L < 0 || B < 0) return fail(CSA2_ERR_INVALID_ARG, "sparse_attn_layers: negative size");
+    if (L == 0 || B == 0) return CSA2_OK;
+    if (p->heads != kH || p->head_dim != kD || p->window != kW || p->topk_pos != kKp ||
+        p->compress_ratio < 1)
+        return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn_layers: built for 64 heads x 512, W=128, k=512");
+    if (p->kv_format != CSA2_NVFP4 || p->win_format != CSA2_E4M3 || p->q_format != CSA2_BF16)
+        return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn_layers: formats must be NVFP4, E4M3, BF16");
+    if (!q || !sink || !win || !n_tokens || !comp || !comp_scales || !idx || !out)
+        return fail(CSA2_ERR_INVALID_ARG, "sparse_attn_layers: NULL buffer");
+    if (!aligned16(q) || !aligned16(out))
+        return fail(CSA2_ERR_ALIGN, "sparse_attn_layers: q, out must be 16-byte aligned");
+    if (L > 65535 || B > 65535) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn_layers: grid too large");
+    static bool attr = false;
+    if (!attr) {
+        if (cudaFuncSetAttribute(k_sparse_attn_fd, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kSmemFd) != cudaSuccess)
+            return check_launch("sparse_attn_layers: smem attribute");
+        attr = true;
+    }
+    k_sparse_attn_fd<<<dim3(L, B), kFdThreads, kSmemFd, static_cast<cudaStream_t>(stream)>>>(
+        B, static_cast<const __nv_bfloat16*>(q), sink, win, n_tokens, comp, comp_scales, idx,
+        p->compress_ratio, p->softmax_scale * kLog2e, static_cast<__nv_bfloat16*>(out), dev_status);
+    return check_launch("sparse_attn_layers");
 }
 
 extern "C" int csa2_sparse_attn(const csa2_params* p, int B, const void* q, const float* sink,

@@ -25,6 +25,7 @@ class DecodeRun:
     device: str = "cuda"
     max_prepared: int = 64
     cuda_core_indexer: bool = False
+    fused_attention: bool = True
     step_done: int = 0
     groups: list = field(default_factory=list)
 
@@ -59,12 +60,18 @@ class DecodeRun:
                 grp["rd"] = api.LayerCache(self.B * (cfg.readers - 1), [1] * (self.B * (cfg.readers - 1)),
                                            self.params, has_comp=False, device=dev)
             grp["keys"] = api.IndexKeyCache(self.key_rows, device=dev)
+            if cfg.readers > 1:
+                grp["win_all"] = torch.cat([grp["src"].win_ptrs, grp["rd"].win_ptrs])
+            else:
+                grp["win_all"] = grp["src"].win_ptrs
             grp["scores"] = torch.empty(self.B, self.max_ncomp, dtype=torch.float32, device=dev)
             grp["bmax"] = torch.empty(self.B, self.n_b_max, dtype=torch.float32, device=dev)
             grp["idx"] = torch.empty(self.B, 512, dtype=torch.int32, device=dev)
             grp["n_sel"] = torch.empty(self.B, dtype=torch.int32, device=dev)
-            grp["out"] = [torch.empty(self.B, H, D, dtype=qdt, device=dev) for _ in range(cfg.readers)]
-            grp["sink"] = [torch.empty(H, dtype=torch.float32, device=dev) for _ in range(cfg.readers)]
+            grp["out_all"] = torch.empty(cfg.readers, self.B, H, D, dtype=qdt, device=dev)
+            grp["out"] = list(grp["out_all"].unbind(0))
+            grp["sink_all"] = torch.empty(cfg.readers, H, dtype=torch.float32, device=dev)
+            grp["sink"] = list(grp["sink_all"].unbind(0))
             # per-step inputs, resident before timing
             grp["kv"] = torch.empty(self.n_prep, self.B, 1, D, dtype=torch.float32, device=dev)
             grp["gate"] = torch.empty(self.n_prep, self.B, 1, D, dtype=torch.float32, device=dev)
@@ -232,6 +239,11 @@ class DecodeRun:
                                 grp["idx"], grp["n_sel"], ds, stream)
 
             def attn():
+                if cfg.quant and self.fused_attention:
+                    api.sparse_attn_layers(p, grp["q"][k], grp["sink_all"], grp["win_all"],
+                                           src.n_tokens, src.comp_ptrs, src.comp_scale_ptrs,
+                                           grp["idx"], grp["out_all"], ds, stream)
+                    return
                 for r in range(cfg.readers):
                     if r == 0:
                         win_ptrs, n_tok = src.win_ptrs, src.n_tokens
@@ -293,7 +305,10 @@ class DecodeRun:
         for _ in self.groups:
             n += 1 + (1 if self.cfg.readers > 1 else 0)   # compress / window appends
             n += 1 + 1                                    # Indexer, selection
-            n += 2 * self.cfg.readers                      # attention split pass + merge
+            if self.cfg.quant and self.fused_attention:
+                n += 1                                    # fused multi-layer attention
+            else:
+                n += 2 * self.cfg.readers                  # attention split pass + merge
         return n
 
     def scan_bytes(self) -> float:

@@ -253,6 +253,27 @@ int csa2_sparse_attn(const csa2_params* p, int B,
                      int32_t* dev_status, void* stream);
 
 /*
+ * csa2_sparse_attn_layers — csa2_sparse_attn for L layers that share one
+ * compressed cache and one selection ("DeepSeek-V4.1-Flash-NVFP4" §四: the
+ * KV-source layers' compressed cache is read by the layers in between; §3.3:
+ * a published top-k is reused), each with its own query, window and sink.
+ * Same arithmetic as csa2_sparse_attn; one CTA per (layer, sequence) streams
+ * all 640 positions with an online softmax, so it needs no workspace.
+ *   q    [L, B, H, D] bf16      sink [L, H] fp32      out [L, B, H, D] bf16
+ *   win  device array [L*B] of ring bases, layer-major (entry l*B + b)
+ *   n_tokens [B]: raw tokens of sequence b (the same in every layer: the layers
+ *        process one token stream); comp, comp_scales [B]; idx [B, topk_pos].
+ * Constraints: H == 64, D == 512, W == 128, topk_pos == 512, NVFP4 cache,
+ * E4M3 window, bf16 query/output.
+ */
+int csa2_sparse_attn_layers(const csa2_params* p, int L, int B,
+                            const void* q, const float* sink,
+                            const void* const* win, const int32_t* n_tokens,
+                            const void* const* comp, const uint8_t* const* comp_scales,
+                            const int32_t* idx, void* out,
+                            int32_t* dev_status, void* stream);
+
+/*
  * csa2_sparse_attn_noalloc — csa2_sparse_attn without a caller workspace.
  * (No counterpart in the pages: an addition for callers that cannot allocate.)
  *

@@ -385,3 +385,62 @@ def test_sparse_attn_out_of_range_index_is_skipped_and_flagged():
                              idx=keep)
     ok, e = close_bf16(out[0].float().cpu().numpy().astype(np.float64), ref)
     assert ok, e
+
+
+def test_sparse_attn_layers_matches_oracle_per_layer():
+    """L layers share one compressed cache and one selection; each has its own
+    window ring, query and sink (the KV-sharing readers of a source layer)."""
+    rng = np.random.default_rng(31)
+    L = 3
+    Ts = [1, 70, 128, 129, 900, 4096, 2001]
+    B = len(Ts)
+    p = api.default_params()
+    src = api.LayerCache(B, [max(1, T // 2) for T in Ts], p)
+    wins = [api.LayerCache(B, [1] * B, p, has_comp=False) for _ in range(L - 1)]
+    st_src, st_win = [], [[] for _ in range(L - 1)]
+    for b, T in enumerate(Ts):
+        kv = rng.standard_normal((T, 512)).astype(np.float32)
+        g = rng.standard_normal((T, 512)).astype(np.float32)
+        s = orc.SeqState(cap_comp=max(1, T // 2), D=512, W=128)
+        s.append(kv, g)
+        st_src.append(s)
+        src.comp[b].copy_(t(s.comp_vals))
+        src.comp_scales[b].copy_(t(s.comp_scales))
+        src.win[b].copy_(t(s.win_u8))
+        for l in range(L - 1):
+            w = orc.SeqState(cap_comp=1, D=512, W=128, has_comp=False)
+            w.append(rng.standard_normal((T, 512)).astype(np.float32), None)
+            st_win[l].append(w)
+            wins[l].win[b].copy_(t(w.win_u8))
+    src.n_tokens.copy_(t(np.array(Ts, np.int32)))
+    idx = np.full((B, 512), -1, np.int32)
+    for b, T in enumerate(Ts):
+        n_c = T // 2
+        k = min(int(rng.integers(0, 513)), n_c) if b % 2 else min(512, n_c)
+        if k:
+            idx[b, np.sort(rng.choice(512, k, replace=False))] = np.sort(rng.choice(n_c, k, replace=False))
+    idx[5, 7] = 10 ** 6  # out of range: skipped, flagged
+    q = rng.standard_normal((L, B, 64, 512)).astype(np.float32)
+    qb = synth.bf16_bits_rne(q)
+    q_dev = torch.from_numpy(qb.view(np.int16)).to(DEV).view(torch.bfloat16)
+    sink = rng.standard_normal((L, 64)).astype(np.float32)
+    win_all = torch.cat([src.win_ptrs] + [w.win_ptrs for w in wins])
+    out = torch.empty(L, B, 64, 512, dtype=torch.bfloat16, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    api.sparse_attn_layers(p, q_dev, t(sink), win_all, src.n_tokens, src.comp_ptrs,
+                           src.comp_scale_ptrs, t(idx), out, status)
+    torch.cuda.synchronize()
+    assert status.item() & 1
+    got = out.float().cpu().numpy().astype(np.float64)
+    q64 = synth.bf16_to_f64(qb)
+    for l in range(L):
+        for b, T in enumerate(Ts):
+            keep = idx[b].copy()
+            keep[keep >= T // 2] = -1
+            win = st_src[b].win_u8 if l == 0 else st_win[l - 1][b].win_u8
+            s = st_src[b]
+            ref, _ = orc.sparse_attn(q64[l, b], sink[l].astype(np.float64), 1 / math.sqrt(512), T,
+                                     128, win_u8=win, comp_vals=s.comp_vals,
+                                     comp_scales=s.comp_scales, idx=keep)
+            ok, e = close_bf16(got[l, b], ref)
+            assert ok, (l, b, T, e)
