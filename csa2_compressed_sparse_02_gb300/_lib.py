@@ -27,7 +27,7 @@ class Params(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "heads", "head_dim", "index_heads", "index_dim", "window", "block_size", "topk_blocks",
         "topk_pos", "compress_ratio", "kv_format", "win_format", "q_format")] + [
-        ("softmax_scale", ctypes.c_float)]
+        ("softmax_scale", ctypes.c_float), ("win_layout", ctypes.c_int)]
 
 
 PP = ctypes.POINTER(Params)
@@ -38,6 +38,7 @@ SIGNATURES = {
     "csa2_last_error": (ctypes.c_char_p, []),
     "csa2_compress_append": (I32, [PP, I32, I32, P, P, P, P, P, P, P, P, P, P, P]),
     "csa2_nvfp4_quantize": (I32, [P, I64, I32, P, P, P]),
+    "csa2_window_linear": (I32, [PP, I32, I32, P, P, P, P, P]),
     "csa2_index_keys_write": (I32, [PP, I32, I64, P, P, P, P, P, P, P]),
     "csa2_index_scores": (I32, [PP, I32, I64, P, P, P, P, P, P, P, P, P]),
     "csa2_index_scores_cuda_cores": (I32, [PP, I32, I64, P, P, P, P, P, P, P, P, P]),

@@ -20,6 +20,7 @@ import torch
 from ._lib import Csa2Error, Params, check, lib  # noqa: F401
 
 F32, NVFP4, E4M3, BF16 = 0, 1, 2, 3
+WIN_RING, WIN_LINEAR = 0, 1
 D, H, HI, DI, W, BLK, KB, KP = 512, 64, 32, 128, 128, 8, 2048, 512
 KEY_TILE, KEY_TILE_BYTES = 128, 9216
 
@@ -65,6 +66,13 @@ def compress_append(params, kv_new, gate_new, pend_kv, pend_gate, comp_ptrs, com
         ctypes.byref(params), B, n_new, _ptr(kv_new), _ptr(gate_new), _ptr(pend_kv),
         _ptr(pend_gate), _ptr(comp_ptrs), _ptr(comp_scale_ptrs), _ptr(comp_cap), _ptr(win_ptrs),
         _ptr(n_tokens), _ptr(dev_status), _stream(stream)), "compress_append")
+
+
+def window_linear(params, kv_new, win_ptrs, n_tokens, out, stream=None):
+    """Linear FP8 windows of a prefill chunk (before its append): out [B, W-1+n_new, D]."""
+    B, n_new = n_tokens.numel(), kv_new.shape[1]
+    check(lib().csa2_window_linear(ctypes.byref(params), B, n_new, _ptr(kv_new), _ptr(win_ptrs),
+                                   _ptr(n_tokens), _ptr(out), _stream(stream)), "window_linear")
 
 
 def nvfp4_quantize(x, vals, scales, stream=None):

@@ -38,8 +38,9 @@ extern "C" void csa2_default_params(csa2_params* p) {
     p->win_format = CSA2_E4M3;
     p->q_format = CSA2_BF16;
     p->softmax_scale = 1.0f / std::sqrt((float)csa2::kD);
+    p->win_layout = CSA2_WIN_RING;
 }
 
-extern "C" int csa2_version(void) { return 100; }
+extern "C" int csa2_version(void) { return 200; }
 
 extern "C" const char* csa2_last_error(void) { return csa2::g_last_error.c_str(); }

@@ -145,10 +145,51 @@ k_nvfp4_quantize(const float* __restrict__ x, int64_t n_elems, uint8_t* vals, ui
     if (((e >> 2) & 3) == 0) scales[e / kGroup] = sb;
 }
 
+// Linear prefill window: rows i < W-1 copy raw position T-(W-1)+i from the
+// ring (zero when negative), rows W-1+t cast chunk token t to E4M3.
+__global__ void __launch_bounds__(kThreads)
+k_window_linear(int n_new, const float* __restrict__ kv_new, const void* const* win,
+                const int32_t* __restrict__ n_tokens, uint8_t* out) {
+    const int b = blockIdx.y, tid = threadIdx.x, ch = 4 * tid;
+    const int rows = kW - 1 + n_new;
+    const int64_t T = n_tokens[b];
+    for (int i = blockIdx.x; i < rows; i += gridDim.x) {
+        uint32_t v;
+        if (i < kW - 1) {
+            const int64_t pos = T - (kW - 1) + i;
+            v = pos < 0 ? 0u
+                        : *reinterpret_cast<const uint32_t*>(static_cast<const uint8_t*>(win[b]) +
+                                                             (pos % kW) * kD + ch);
+        } else {
+            v = e4m3x4(ld4(kv_new + ((int64_t)b * n_new + (i - (kW - 1))) * kD + ch));
+        }
+        *reinterpret_cast<uint32_t*>(out + ((int64_t)b * rows + i) * kD + ch) = v;
+    }
+}
+
 }  // namespace
 }  // namespace csa2
 
 using namespace csa2;
+
+extern "C" int csa2_window_linear(const csa2_params* p, int B, int n_new, const float* kv_new,
+                                  const void* const* win, const int32_t* n_tokens, uint8_t* out,
+                                  void* stream) {
+    CSA2_CHECK_PARAMS(p);
+    if (B < 0 || n_new < 0) return fail(CSA2_ERR_INVALID_ARG, "window_linear: negative size");
+    if (B == 0) return CSA2_OK;
+    if (p->head_dim != kD || p->window != kW || p->win_format != CSA2_E4M3)
+        return fail(CSA2_ERR_UNSUPPORTED, "window_linear: built for D=512, W=128, E4M3 windows");
+    if ((n_new && !kv_new) || !win || !n_tokens || !out)
+        return fail(CSA2_ERR_INVALID_ARG, "window_linear: NULL buffer");
+    if ((kv_new && !aligned16(kv_new)) || !aligned16(out))
+        return fail(CSA2_ERR_ALIGN, "window_linear: kv_new and out must be 16-byte aligned");
+    const int rows = kW - 1 + n_new;
+    const int gx = rows < 1024 ? rows : 1024;
+    k_window_linear<<<dim3(gx, B), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        n_new, kv_new, win, n_tokens, out);
+    return check_launch("window_linear");
+}
 
 extern "C" int csa2_compress_append(const csa2_params* p, int B, int n_new,
                                     const float* kv_new, const float* gate_new,

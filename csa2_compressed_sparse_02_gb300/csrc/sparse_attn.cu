@@ -99,17 +99,19 @@ __device__ __forceinline__ void e4m3x16_to_bf16(uint4 v, uint32_t* o) {
     }
 }
 
-// Valid window slot r for a sequence of T raw tokens: the ring holds raw
-// positions max(0,T-W)..T-1, position p in slot p mod W.
-__device__ __forceinline__ bool window_slot_valid(int r, int64_t T) {
-    return T >= kW || (int64_t)r < T;
+// Valid window row r for a sequence of T raw tokens. Ring layout: the ring
+// holds raw positions max(0,T-W)..T-1, position p in slot p mod W. Linear
+// layout: row r holds raw position T-W+r.
+__device__ __forceinline__ bool window_slot_valid(int r, int64_t T, int linear) {
+    return linear ? T - kW + r >= 0 : (T >= kW || (int64_t)r < T);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
 k_sparse_attn_bf16(const __nv_bfloat16* __restrict__ q, const void* const* win,
                    const int32_t* __restrict__ n_tokens, const void* const* comp,
                    const uint8_t* const* comp_scales, const int32_t* __restrict__ idx, int ratio,
-                   float scale_log2, float* ws_o, float2* ws_ml, int32_t* dev_status) {
+                   float scale_log2, float* ws_o, float2* ws_ml, int32_t* dev_status,
+                   int win_linear) {
     extern __shared__ __align__(1024) unsigned char smem[];
     const int split = blockIdx.x, b = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -138,7 +140,7 @@ k_sparse_attn_bf16(const __nv_bfloat16* __restrict__ q, const void* const* win,
         uint32_t o[8];
         bool valid;
         if (split == 0) {
-            valid = T > 0 && window_slot_valid(r, T);
+            valid = T > 0 && window_slot_valid(r, T, win_linear);
             if (valid) {
                 const uint4 v = *reinterpret_cast<const uint4*>(
                     static_cast<const uint8_t*>(win[b]) + (int64_t)r * kD + 16 * lane);
@@ -287,7 +289,7 @@ __global__ void __launch_bounds__(kF32Threads)
 k_sparse_attn_f32(const float* __restrict__ q, const void* const* win,
                   const int32_t* __restrict__ n_tokens, const void* const* comp,
                   const int32_t* __restrict__ idx, int ratio, float scale_log2, float* ws_o,
-                  float2* ws_ml, int32_t* dev_status) {
+                  float2* ws_ml, int32_t* dev_status, int win_linear) {
     extern __shared__ __align__(1024) unsigned char smem[];
     float* sQt = reinterpret_cast<float*>(smem);  // [D][H]
     float* sS = sQt + kD * kH;                     // [H][rows]
@@ -302,7 +304,7 @@ k_sparse_attn_f32(const float* __restrict__ q, const void* const* win,
         const int r = tid;
         const float* row = nullptr;
         if (split == 0) {
-            if (T > 0 && window_slot_valid(r, T))
+            if (T > 0 && window_slot_valid(r, T, win_linear))
                 row = static_cast<const float*>(win[b]) + (int64_t)r * kD;
         } else {
             const int64_t j = idx[(int64_t)b * kKp + (split - 1) * kRows + r];
@@ -426,8 +428,9 @@ k_sparse_attn_merge(const float* __restrict__ sink, const float* __restrict__ ws
 // ---- fused multi-layer flash-decode (bf16 tensor cores, output in registers) ----
 // One CTA per (layer, sequence): 64 query heads x all 640 positions, streamed
 // as 10 chunks of 64 positions (2 window chunks, 8 compressed chunks) with an
-// online softmax. The output O[64 x 512] lives in registers: warp w owns rows
-// 16*(w%4).. and dims 128*(w/4).. (16 mma n-tiles, 64 fp32 per thread). The
+// online softmax. The output O[64 x 512] lives in registers: warp w owns all
+// 64 rows and dims 32w..32w+31 (4 x 4 mma tiles, 64 fp32 per thread), so each
+// V fragment is read from shared memory once per chunk. The
 // next chunk's raw bytes are loaded into registers while the current chunk is
 // multiplied, then decoded exactly into bf16 shared memory. The sink joins the
 // denominator once at the end; no workspace, no merge pass. All L layers of a
@@ -439,10 +442,11 @@ constexpr int kFdChunks = (kW + kKp) / kFdChunk;  // 10
 constexpr int kFdOffQ = 0;                                  // 64 x 1024 B
 constexpr int kFdOffKV = kFdOffQ + kH * kD * 2;             // 2 x 64 x 1024 B
 constexpr int kFdOffP = kFdOffKV + 2 * kFdChunk * kD * 2;    // 64 x 128 B
-constexpr int kFdOffMax = kFdOffP + kH * kFdChunk * 2;       // float [4][64]
-constexpr int kFdOffSum = kFdOffMax + 4 * kH * 4;            // float [4][64]
+constexpr int kFdOffMax = kFdOffP + kH * kFdChunk * 2;       // float [5][64]: maxima, alpha
+constexpr int kFdOffSum = kFdOffMax + 5 * kH * 4;            // float [4][64]
 constexpr int kFdOffValid = kFdOffSum + 4 * kH * 4;          // int [2][64]
-constexpr int kSmemFd = kFdOffValid + 2 * kFdChunk * 4;
+constexpr int kFdOffIdx = kFdOffValid + 2 * kFdChunk * 4;     // int [512] selected positions
+constexpr int kSmemFd = kFdOffIdx + kKp * 4;
 
 // Raw bytes of 4 rows of a chunk, per lane (the warp covers one row per step).
 struct FdRaw {
@@ -454,7 +458,7 @@ struct FdRaw {
 __device__ __forceinline__ void fd_load(FdRaw& raw, int c, int warp, int lane, int64_t T,
                                         int64_t n_c, const uint8_t* win, const uint8_t* comp,
                                         const uint8_t* comp_sc, const int32_t* idx,
-                                        int32_t* dev_status) {
+                                        int32_t* dev_status, int win_linear) {
     raw.valid = 0;
     raw.sc = 0;
 #pragma unroll
@@ -463,7 +467,7 @@ __device__ __forceinline__ void fd_load(FdRaw& raw, int c, int warp, int lane, i
         raw.v[k] = make_uint4(0u, 0u, 0u, 0u);
         if (c < kW / kFdChunk) {  // window chunk: ring slot c*64 + r
             const int slot = c * kFdChunk + r;
-            if (T > 0 && window_slot_valid(slot, T)) {
+            if (T > 0 && window_slot_valid(slot, T, win_linear)) {
                 raw.v[k] = *reinterpret_cast<const uint4*>(win + (int64_t)slot * kD + 16 * lane);
                 raw.valid |= 1u << k;
             }
@@ -512,7 +516,7 @@ k_sparse_attn_fd(int B, const __nv_bfloat16* __restrict__ q, const float* __rest
                  const void* const* win, const int32_t* __restrict__ n_tokens,
                  const void* const* comp, const uint8_t* const* comp_scales,
                  const int32_t* __restrict__ idx, int ratio, float scale_log2,
-                 __nv_bfloat16* out, int32_t* dev_status) {
+                 __nv_bfloat16* out, int32_t* dev_status, int win_linear) {
     extern __shared__ __align__(1024) unsigned char smem[];
     const int layer = blockIdx.x, b = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -529,7 +533,10 @@ k_sparse_attn_fd(int B, const __nv_bfloat16* __restrict__ q, const float* __rest
     const uint8_t* winb = static_cast<const uint8_t*>(win[lb]);
     const uint8_t* compb = static_cast<const uint8_t*>(comp[b]);
     const uint8_t* compsb = comp_scales[b];
-    const int32_t* idxb = idx + (int64_t)b * kKp;
+    int32_t* sIdx = reinterpret_cast<int32_t*>(smem + kFdOffIdx);
+    for (int i = tid; i < kKp; i += kFdThreads) sIdx[i] = idx[(int64_t)b * kKp + i];
+    __syncthreads();
+    const int32_t* idxb = sIdx;  // gathers read the indices from shared memory
 
     // ---- Q -> shared (async), chunk 0 -> shared ----
     const unsigned char* qb = reinterpret_cast<const unsigned char*>(q + lb * kH * kD);
@@ -540,14 +547,19 @@ k_sparse_attn_fd(int B, const __nv_bfloat16* __restrict__ q, const float* __rest
     }
     asm volatile("cp.async.commit_group;\n");
     FdRaw raw;
-    fd_load(raw, 0, warp, lane, T, n_c, winb, compb, compsb, idxb, dev_status);
+    fd_load(raw, 0, warp, lane, T, n_c, winb, compb, compsb, idxb, dev_status, win_linear);
     fd_store(raw, 0, warp, lane, smem + kFdOffKV, sValid);
     asm volatile("cp.async.wait_all;\n");
 
-    float o_acc[16][4];
+    // O accumulator: all 64 rows (4 m-tiles) x dims 32*warp .. +31 (4 n-tiles)
+    float o_acc[4][4][4];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) o_acc[j][0] = o_acc[j][1] = o_acc[j][2] = o_acc[j][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;  // rows 16wm+g, +8
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o_acc[mt][j][0] = o_acc[mt][j][1] = o_acc[mt][j][2] = o_acc[mt][j][3] = 0.f;
+    // running max / sum of rows 16wm+g, +8 (the S-phase rows of this thread)
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float* sAlpha = sMax;  // per-row rescale factor of the chunk, reuses the max buffer
     const uint32_t sQ_u = smem_u32(sQ), sP_u = smem_u32(sP);
 
     for (int c = 0; c < kFdChunks; ++c) {
@@ -556,7 +568,8 @@ k_sparse_attn_fd(int B, const __nv_bfloat16* __restrict__ q, const float* __rest
         const int* vld = sValid + (c & 1) * kFdChunk;
         const uint32_t sKV_u = smem_u32(sKV);
         if (c + 1 < kFdChunks)
-            fd_load(raw, c + 1, warp, lane, T, n_c, winb, compb, compsb, idxb, dev_status);
+            fd_load(raw, c + 1, warp, lane, T, n_c, winb, compb, compsb, idxb, dev_status,
+                    win_linear);
 
         // ---- S = Q K^T for rows 16wm.., positions 16wn.. (2 n-tiles) ----
         float s_acc[2][4];
@@ -635,25 +648,41 @@ k_sparse_attn_fd(int B, const __nv_bfloat16* __restrict__ q, const float* __rest
         l1 = l1 * al1 + cs1;
         m0 = n0;
         m1 = n1;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            o_acc[j][0] *= al0;
-            o_acc[j][1] *= al0;
-            o_acc[j][2] *= al1;
-            o_acc[j][3] *= al1;
+        if (wn == 0 && t == 0) {  // publish the rescale factors of all 64 rows (slot 0)
+            sAlpha[4 * kH + 16 * wm + g] = al0;
+            sAlpha[4 * kH + 16 * wm + g + 8] = al1;
         }
-        // ---- O += P V for rows 16wm.., dims 128wn.. (16 n-tiles), 64 positions ----
+        __syncthreads();
+#pragma unroll
+        for (int mt = 0; mt < 4; ++mt) {
+            const float a0 = sAlpha[4 * kH + 16 * mt + g], a1 = sAlpha[4 * kH + 16 * mt + g + 8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                o_acc[mt][j][0] *= a0;
+                o_acc[mt][j][1] *= a0;
+                o_acc[mt][j][2] *= a1;
+                o_acc[mt][j][3] *= a1;
+            }
+        }
+        // ---- O += P V: all 64 rows x dims 32*warp.. (4 n-tiles), 64 positions ----
 #pragma unroll
         for (int kk = 0; kk < kFdChunk / 16; ++kk) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(sP_u + swz(16 * wm + (lane & 15), 2 * kk + (lane >> 4), 8), a0, a1, a2, a3);
+            uint32_t bv[2][4];
 #pragma unroll
-            for (int jp = 0; jp < 8; ++jp) {
-                uint32_t b0, b1, b2, b3;
+            for (int jp = 0; jp < 2; ++jp) {
                 const int prow = 16 * kk + (lane & 7) + (((lane >> 3) & 1) << 3);
-                ldsm_x4_t(sKV_u + swz(prow, 16 * wn + 2 * jp + (lane >> 4), 64), b0, b1, b2, b3);
-                mma_bf16(o_acc[2 * jp], a0, a1, a2, a3, b0, b1);
-                mma_bf16(o_acc[2 * jp + 1], a0, a1, a2, a3, b2, b3);
+                ldsm_x4_t(sKV_u + swz(prow, 4 * warp + 2 * jp + (lane >> 4), 64), bv[jp][0], bv[jp][1],
+                          bv[jp][2], bv[jp][3]);
+            }
+#pragma unroll
+            for (int mt = 0; mt < 4; ++mt) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(sP_u + swz(16 * mt + (lane & 15), 2 * kk + (lane >> 4), 8), a0, a1, a2, a3);
+#pragma unroll
+                for (int jp = 0; jp < 2; ++jp) {
+                    mma_bf16(o_acc[mt][2 * jp], a0, a1, a2, a3, bv[jp][0], bv[jp][1]);
+                    mma_bf16(o_acc[mt][2 * jp + 1], a0, a1, a2, a3, bv[jp][2], bv[jp][3]);
+                }
             }
         }
         if (c + 1 < kFdChunks)
@@ -662,21 +691,29 @@ k_sparse_attn_fd(int B, const __nv_bfloat16* __restrict__ q, const float* __rest
     }
 
     // ---- sink and normalisation, bf16 out ----
-    const float sink2 = sink[(int64_t)layer * kH + 16 * wm + g] * kLog2e;
-    const float sink2b = sink[(int64_t)layer * kH + 16 * wm + g + 8] * kLog2e;
-    const float M0 = fmaxf(m0, sink2), M1 = fmaxf(m1, sink2b);
-    const float sc0 = m0 == -INFINITY ? 0.f : exp2f(m0 - M0);
-    const float sc1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M1);
-    const float f0 = sc0 / (l0 * sc0 + exp2f(sink2 - M0));
-    const float f1 = sc1 / (l1 * sc1 + exp2f(sink2b - M1));
+    __syncthreads();  // every warp is done reading the last chunk's rescale factors
+    if (wn == 0 && t == 0) {  // final factor of every row: e^{m}/(e^{sink} + sum) in log2 form
+        const float sink2 = sink[(int64_t)layer * kH + 16 * wm + g] * kLog2e;
+        const float sink2b = sink[(int64_t)layer * kH + 16 * wm + g + 8] * kLog2e;
+        const float M0 = fmaxf(m0, sink2), M1 = fmaxf(m1, sink2b);
+        const float sc0 = m0 == -INFINITY ? 0.f : exp2f(m0 - M0);
+        const float sc1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M1);
+        sAlpha[4 * kH + 16 * wm + g] = sc0 / (l0 * sc0 + exp2f(sink2 - M0));
+        sAlpha[4 * kH + 16 * wm + g + 8] = sc1 / (l1 * sc1 + exp2f(sink2b - M1));
+    }
+    __syncthreads();
     __nv_bfloat16* ob = out + lb * kH * kD;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        const int col = 128 * wn + 8 * j + 2 * t;
-        *reinterpret_cast<uint32_t*>(ob + (int64_t)(16 * wm + g) * kD + col) =
-            pack_bf16(o_acc[j][0] * f0, o_acc[j][1] * f0);
-        *reinterpret_cast<uint32_t*>(ob + (int64_t)(16 * wm + g + 8) * kD + col) =
-            pack_bf16(o_acc[j][2] * f1, o_acc[j][3] * f1);
+    for (int mt = 0; mt < 4; ++mt) {
+        const float f0 = sAlpha[4 * kH + 16 * mt + g], f1 = sAlpha[4 * kH + 16 * mt + g + 8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int col = 32 * warp + 8 * j + 2 * t;
+            *reinterpret_cast<uint32_t*>(ob + (int64_t)(16 * mt + g) * kD + col) =
+                pack_bf16(o_acc[mt][j][0] * f0, o_acc[mt][j][1] * f0);
+            *reinterpret_cast<uint32_t*>(ob + (int64_t)(16 * mt + g + 8) * kD + col) =
+                pack_bf16(o_acc[mt][j][2] * f1, o_acc[mt][j][3] * f1);
+        }
     }
 }
 
@@ -721,7 +758,8 @@ extern "C" int csa2_sparse_attn_layers(const csa2_params* p, int L, int B, const
     }
     k_sparse_attn_fd<<<dim3(L, B), kFdThreads, kSmemFd, static_cast<cudaStream_t>(stream)>>>(
         B, static_cast<const __nv_bfloat16*>(q), sink, win, n_tokens, comp, comp_scales, idx,
-        p->compress_ratio, p->softmax_scale * kLog2e, static_cast<__nv_bfloat16*>(out), dev_status);
+        p->compress_ratio, p->softmax_scale * kLog2e, static_cast<__nv_bfloat16*>(out), dev_status,
+        p->win_layout == CSA2_WIN_LINEAR);
     return check_launch("sparse_attn_layers");
 }
 
@@ -765,7 +803,7 @@ extern "C" int csa2_sparse_attn(const csa2_params* p, int B, const void* q, cons
         }
         k_sparse_attn_bf16<<<grid, kThreads, kSmemBf16, s>>>(
             static_cast<const __nv_bfloat16*>(q), win, n_tokens, comp, comp_scales, idx,
-            p->compress_ratio, scale_log2, ws_o, ws_ml, dev_status);
+            p->compress_ratio, scale_log2, ws_o, ws_ml, dev_status, p->win_layout == CSA2_WIN_LINEAR);
         k_sparse_attn_merge<true><<<dim3(kH, B), 128, 0, s>>>(sink, ws_o, ws_ml, out);
     } else {
         if (!attr_f32) {
@@ -776,7 +814,7 @@ extern "C" int csa2_sparse_attn(const csa2_params* p, int B, const void* q, cons
         }
         k_sparse_attn_f32<<<grid, kF32Threads, kSmemF32, s>>>(
             static_cast<const float*>(q), win, n_tokens, comp, idx, p->compress_ratio, scale_log2,
-            ws_o, ws_ml, dev_status);
+            ws_o, ws_ml, dev_status, p->win_layout == CSA2_WIN_LINEAR);
         k_sparse_attn_merge<false><<<dim3(kH, B), 128, 0, s>>>(sink, ws_o, ws_ml, out);
     }
     return check_launch("sparse_attn");

@@ -78,6 +78,39 @@ CONFIGS = {
                     kscale_pow2=True),
 }
 
+
+
+@dataclass(frozen=True)
+class PrefillConfig:
+    """A prefill chunk appended to a prior context of one sequence: query i sits
+    at raw position T0 + i, so its context (itself included) is T0 + i + 1 tokens
+    and it sees compressed positions j with 2j + 1 <= T0 + i (n_c = (T0+i+1)//2).
+    Per-query inputs use the decode recipe with the query index as the step."""
+    number: int
+    workload: str
+    T0: int
+    chunk: int
+    quant: bool = True
+    plants: int = 16
+    kscale_pow2: bool = True
+    B: int = 1
+    groups: int = 1
+    readers: int = 1
+
+    @property
+    def seed(self) -> int:
+        return SEED_BASE + self.number
+
+    def first_lengths(self) -> list:
+        return [self.T0 + 1]
+
+    def layer(self, g: int, r: int) -> int:
+        return g * self.readers + r
+
+
+PREFILL = PrefillConfig(4, "prefill chunk of 8192 queries on a 262,144-token context, NVFP4",
+                        T0=262144, chunk=8192)
+
 D, H, HI, DI, W = 512, 64, 32, 128, 128
 
 

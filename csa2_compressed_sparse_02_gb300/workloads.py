@@ -337,3 +337,99 @@ class _CacheView:
         self.comp_scale_ptrs = cache.comp_scale_ptrs[sl] if cache.comp_scale_ptrs is not None else None
         self.comp_cap = cache.comp_cap[sl]
         self.win_ptrs = cache.win_ptrs[sl]
+
+
+class PrefillRun:
+    """Device state of a prefill chunk (inputs.PrefillConfig): the prior context is
+    compressed into the cache, then run() appends the chunk and computes, for
+    every query of the chunk, its Indexer scores over the compressed positions it
+    sees, its two-level selection and its sparse attention (window rows from a
+    linear buffer built before the append)."""
+
+    def __init__(self, cfg, device="cuda", index_batch=1024):
+        import torch
+
+        from . import api
+        self.torch, self.api, self.cfg, self.device = torch, api, cfg, device
+        self.index_batch = index_batch
+        T0, n = cfg.T0, cfg.chunk
+        self.n_c_final = (T0 + n) // 2
+        self.params = api.default_params()
+        self.params_lin = api.default_params(win_layout=api.WIN_LINEAR)
+        dev = device
+        self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.src = api.LayerCache(1, [self.n_c_final + 1], self.params, device=dev)
+        # prior context through the Compressor
+        kvk = [synth.stream_key(cfg.seed, synth.KV, 0, 0)]
+        gk = [synth.stream_key(cfg.seed, synth.GATE, 0, 0)]
+        ch = 65536
+        kv = torch.empty(1, ch, D, dtype=torch.float32, device=dev)
+        gt = torch.empty_like(kv)
+        for t0 in range(0, T0, ch):
+            m = min(ch, T0 - t0)
+            synth.gpu_fill(synth.G_NORMAL_F32, kvk, t0 * D, m * D, kv)
+            synth.gpu_fill(synth.G_NORMAL_F32, gk, t0 * D, m * D, gt)
+            self.src.append(kv[:, :m], gt[:, :m], self.dev_status)
+        # the chunk's raw tokens
+        self.kv = torch.empty(1, n, D, dtype=torch.float32, device=dev)
+        self.gate = torch.empty_like(self.kv)
+        synth.gpu_fill(synth.G_NORMAL_F32, kvk, T0 * D, n * D, self.kv)
+        synth.gpu_fill(synth.G_NORMAL_F32, gk, T0 * D, n * D, self.gate)
+        # index keys of every compressed position the chunk will expose
+        self.keys = api.IndexKeyCache([self.n_c_final], device=dev)
+        nk = self.n_c_final
+        kv8 = torch.empty(nk, DI // 2, dtype=torch.uint8, device=dev)
+        ks8 = torch.empty(nk, DI // 16, dtype=torch.uint8, device=dev)
+        synth.gpu_fill(synth.G_E2M1_BYTES, [synth.stream_key(cfg.seed, synth.IDX_K, 0, 0)], 0,
+                       nk * DI // 2, kv8)
+        synth.gpu_fill(synth.G_SCALE_POW2_BYTES, [synth.stream_key(cfg.seed, synth.IDX_K_SCALE, 0, 0)],
+                       0, nk * DI // 16, ks8)
+        pos, rv, rs = plants(cfg, 0, 0)
+        if pos.size:
+            pi = torch.from_numpy(pos).to(dev)
+            kv8[pi] = torch.from_numpy(np.tile(rv, (pos.size, 1))).to(dev)
+            ks8[pi] = torch.from_numpy(np.tile(rs, (pos.size, 1))).to(dev)
+        self.keys.write_seq(self.params, 0, kv8, ks8, 0, self.dev_status)
+        del kv8, ks8
+        # per-query inputs (query i = step i of the recipe)
+        self.iq = torch.empty(n, HI, DI // 2, dtype=torch.uint8, device=dev)
+        synth.gpu_fill(synth.G_E2M1_BYTES, [synth.stream_key(cfg.seed, synth.IDX_Q, 0, 0)], 0,
+                       n * HI * DI // 2, self.iq)
+        self.iqs = torch.full((n, HI, DI // 16), synth.E4M3_ONE, dtype=torch.uint8, device=dev)
+        self.iw = torch.empty(n, HI, dtype=torch.float32, device=dev)
+        synth.gpu_fill(synth.G_W_POW2_F32, [synth.stream_key(cfg.seed, synth.IDX_W, 0, 0)], 0,
+                       n * HI, self.iw)
+        self.q = torch.empty(1, n, H, D, dtype=torch.bfloat16, device=dev)
+        synth.gpu_fill(synth.G_NORMAL_BF16, [synth.stream_key(cfg.seed, synth.Q, 0, 0)], 0,
+                       n * H * D, self.q)
+        self.sink = torch.empty(1, H, dtype=torch.float32, device=dev)
+        synth.gpu_fill(synth.G_NORMAL_F32, [synth.stream_key(cfg.seed, synth.SINK, 0, 0)], 0, H,
+                       self.sink)
+        # per-query views of the one sequence
+        self.n_tok_q = torch.arange(T0 + 1, T0 + 1 + n, dtype=torch.int32, device=dev)
+        self.key_ptrs = self.keys.ptrs[:1].repeat(n)
+        self.comp_ptrs = self.src.comp_ptrs[:1].repeat(n)
+        self.comp_scale_ptrs = self.src.comp_scale_ptrs[:1].repeat(n)
+        self.winbuf = torch.empty(1, W - 1 + n, D, dtype=torch.uint8, device=dev)
+        self.win_q = (self.winbuf.data_ptr() +
+                      torch.arange(n, dtype=torch.int64, device=dev) * D)
+        self.scores = torch.empty(n, self.n_c_final, dtype=torch.float32, device=dev)
+        self.bmax = torch.empty(n, math.ceil(self.n_c_final / 8), dtype=torch.float32, device=dev)
+        self.idx = torch.empty(n, 512, dtype=torch.int32, device=dev)
+        self.n_sel = torch.empty(n, dtype=torch.int32, device=dev)
+        self.out = torch.empty(1, n, H, D, dtype=torch.bfloat16, device=dev)
+        torch.cuda.synchronize()
+
+    def run(self, timers=None):
+        api, n, ds = self.api, self.cfg.chunk, self.dev_status
+        api.window_linear(self.params, self.kv, self.src.win_ptrs, self.src.n_tokens, self.winbuf)
+        self.src.append(self.kv, self.gate, ds)
+        for s0 in range(0, n, self.index_batch):
+            s1 = min(n, s0 + self.index_batch)
+            api.index_scores(self.params, self.n_c_final, self.iq[s0:s1], self.iqs[s0:s1],
+                             self.iw[s0:s1], self.key_ptrs[s0:s1], self.n_tok_q[s0:s1],
+                             self.scores[s0:s1], self.bmax[s0:s1], ds)
+        api.select_topk(self.params, self.n_c_final, self.scores, self.bmax, self.n_tok_q, self.idx,
+                        self.n_sel, ds)
+        api.sparse_attn_layers(self.params_lin, self.q, self.sink, self.win_q, self.n_tok_q,
+                               self.comp_ptrs, self.comp_scale_ptrs, self.idx, self.out, ds)

@@ -77,10 +77,17 @@ typedef struct csa2_params {
     int win_format;       /* window ring: CSA2_E4M3 (or CSA2_F32) */
     int q_format;         /* query and output: CSA2_BF16 (or CSA2_F32) */
     float softmax_scale;  /* logit scale: 1/sqrt(head_dim) */
+    int win_layout;       /* window rows: CSA2_WIN_RING (row r = ring slot r, the
+                             newest raw position p < T with p mod W = r) or
+                             CSA2_WIN_LINEAR (row r = raw position T-W+r; used by
+                             prefill, where each query has its own window) */
 } csa2_params;
 
+#define CSA2_WIN_RING 0
+#define CSA2_WIN_LINEAR 1
+
 /* Fills *p with the pages' configuration (64/512/32/128/128/8/2048/512/2,
- * NVFP4 cache, E4M3 window, bf16 query, 1/sqrt(512)). */
+ * NVFP4 cache, E4M3 window, bf16 query, 1/sqrt(512), ring window). */
 void csa2_default_params(csa2_params* p);
 
 /* Library ABI version (major*10000 + minor*100 + patch). */
@@ -126,6 +133,23 @@ int csa2_compress_append(const csa2_params* p, int B, int n_new,
                          void* const* comp, uint8_t* const* comp_scales, const int64_t* comp_cap,
                          void* const* win, int32_t* n_tokens,
                          int32_t* dev_status, void* stream);
+
+/*
+ * csa2_window_linear — the FP8 window rows a prefill chunk's queries attend to,
+ * laid out linearly ("DeepSeek-V4.1-Flash-NVFP4" §3.1: the window holds the
+ * newest 128 raw tokens, FP8). Call it before csa2_compress_append appends the
+ * chunk. For each sequence b with T = n_tokens[b] tokens so far, writes
+ * out[b] rows i = 0 .. W-1+n_new-1 with row i = raw position T-(W-1)+i:
+ * the last W-1 positions before the chunk copied from the ring win[b] (rows of
+ * positions < 0 are zero) followed by the n_new chunk tokens cast to E4M3 (RNE,
+ * saturating). The query at raw position p then finds its window (positions
+ * p-W+1..p) at row p-T of out[b], in the CSA2_WIN_LINEAR layout.
+ *   kv_new [B, n_new, D] fp32; win: device array [B] of rings; n_tokens [B];
+ *   out [B, W-1+n_new, D] bytes (E4M3 windows only).
+ */
+int csa2_window_linear(const csa2_params* p, int B, int n_new, const float* kv_new,
+                       const void* const* win, const int32_t* n_tokens, uint8_t* out,
+                       void* stream);
 
 /*
  * csa2_nvfp4_quantize — quantise n_rows rows of row_len fp32 values to NVFP4

@@ -96,3 +96,28 @@ def test_config5_sampled_over_16_steps():
     assert run.dev_status.item() == 0
     for s in (int(np.argmin(T0)), int(np.argmax(T0)), 7):
         _check(run, 0, s, cfg.steps - 1, readers=[0, 3, 5])
+
+
+def test_config4_prefill_sampled_queries():
+    """Prefill chunk: 8,192 queries on a 262,144-token context (135,168 compressed
+    positions visible at the end), per-query causal Indexer, selection and
+    attention with a causal 128-token window."""
+    cfg = inputs.PREFILL
+    run = workloads.PrefillRun(cfg)
+    run.run()
+    torch.cuda.synchronize()
+    assert run.dev_status.item() == 0
+    assert int(run.src.n_tokens.item()) == cfg.T0 + cfg.chunk
+    for i in (0, 1, 4096, cfg.chunk - 1):
+        ref = reference.decode_step(cfg, 0, 0, i, readers=[0])
+        n_c = ref["n_c"]
+        assert n_c == (cfg.T0 + i + 1) // 2 and ref["inexact"] == 0
+        got = run.scores[i, :n_c].cpu().numpy()
+        assert np.array_equal(got, ref["scores"]), (i, np.nonzero(got != ref["scores"])[0][:5])
+        assert np.array_equal(run.idx[i].cpu().numpy(), ref["idx"]), i
+        o = run.out[0, i].float().cpu().numpy().astype(np.float64)
+        e = ref["out"][0]
+        err = np.abs(o - e).max()
+        rel = np.linalg.norm(o - e) / np.linalg.norm(e)
+        assert err <= 1.5e-2 and rel <= 4e-3, (i, err, rel)
+    assert int(run.n_sel.min().item()) == 512
