@@ -44,6 +44,26 @@ def peaks():
         return 6800.0, "fallback"
 
 
+# DRAM bytes per scanned position of k_index_scores_tc, from one ncu capture of
+# the decode workload B=32, T=131072 (151.44 MB read + 6.07 MB written over
+# 2,097,152 positions per launch). The figure belongs to that build of the
+# kernel: it is reported only while the kernel source hashes to the same value.
+INDEX_TRAFFIC_PER_POS = (151.44e6 + 6.07e6) / 2097152
+INDEX_TRAFFIC_SRC_SHA256 = "7a0195e74de7b193c501cc87564824f30b541501191090cb7e98e998d1246050"
+
+
+def index_traffic(positions: float):
+    import hashlib
+    src = os.path.join(ROOT, "csa2_compressed_sparse_02_gb300", "csrc", "index_scores.cu")
+    try:
+        with open(src, "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != INDEX_TRAFFIC_SRC_SHA256:
+                return None
+    except OSError:
+        return None
+    return INDEX_TRAFFIC_PER_POS * positions
+
+
 # ----------------------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi clock/throttle samples every 200 ms while running."""
@@ -313,7 +333,8 @@ def main():
                    "parallelism": "replicas x%d (sequences sharded, no collective)" % world},
         "roofline": {"kernel": "index_scores (Indexer scan, fused block max)", "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None,
+                     "frac": achieved / hbm_peak, "traffic": index_traffic(scan_b / 76.5),
+                     "traffic_source": "ncu dram bytes of a B=32 T=131072 launch, scaled per position",
                      "peak_source": peak_kind, "launch_ms": 1000.0 * scan_s,
                      "bytes_per_launch": scan_b},
         "path_hbm": {"algorithmic_bytes_per_step": step_alg_bytes,
