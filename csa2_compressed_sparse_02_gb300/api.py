@@ -120,14 +120,16 @@ def sparse_attn(params, q, sink, win_ptrs, n_tokens, comp_ptrs, comp_scale_ptrs,
 
 
 def sparse_attn_layers(params, q, sink, win_ptrs, n_tokens, comp_ptrs, comp_scale_ptrs, idx, out,
-                       dev_status=None, stream=None):
+                       dev_status=None, stream=None, mma_sync=False):
     """L layers sharing one compressed cache and selection: q/out [L, B, H, D] bf16,
-    sink [L, H], win_ptrs [L*B] (layer-major), n_tokens [B]."""
+    sink [L, H], win_ptrs [L*B] (layer-major), n_tokens [B]. mma_sync=True runs
+    the legacy warp-level tensor-core implementation of the same contract."""
     L, B = q.shape[0], q.shape[1]
-    check(lib().csa2_sparse_attn_layers(
+    fn = lib().csa2_sparse_attn_layers_mma if mma_sync else lib().csa2_sparse_attn_layers
+    check(fn(
         ctypes.byref(params), L, B, _ptr(q), _ptr(sink), _ptr(win_ptrs), _ptr(n_tokens),
         _ptr(comp_ptrs), _ptr(comp_scale_ptrs), _ptr(idx), _ptr(out), _ptr(dev_status),
-        _stream(stream)), "sparse_attn_layers")
+        _stream(stream)), "sparse_attn_layers_mma" if mma_sync else "sparse_attn_layers")
 
 
 def sparse_attn_noalloc(params, q, sink, win_ptrs, n_tokens, comp_ptrs, comp_scale_ptrs, idx, out,

@@ -731,36 +731,36 @@ extern "C" size_t csa2_sparse_attn_workspace_size(const csa2_params* p, int B) {
     return ws_o_bytes(B) + ws_ml_bytes(B);
 }
 
-extern "C" int csa2_sparse_attn_layers(const csa2_params* p, int L, int B, const void* q,
+extern "C" int csa2_sparse_attn_layers_mma(const csa2_params* p, int L, int B, const void* q,
                                        const float* sink, const void* const* win,
                                        const int32_t* n_tokens, const void* const* comp,
                                        const uint8_t* const* comp_scales, const int32_t* idx,
                                        void* out, int32_t* dev_status, void* stream) {
     CSA2_CHECK_PARAMS(p);
-    if (L < 0 || B < 0) return fail(CSA2_ERR_INVALID_ARG, "sparse_attn_layers: negative size");
+    if (L < 0 || B < 0) return fail(CSA2_ERR_INVALID_ARG, "sparse_attn_layers_mma: negative size");
     if (L == 0 || B == 0) return CSA2_OK;
     if (p->heads != kH || p->head_dim != kD || p->window != kW || p->topk_pos != kKp ||
         p->compress_ratio < 1)
-        return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn_layers: built for 64 heads x 512, W=128, k=512");
+        return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn_layers_mma: built for 64 heads x 512, W=128, k=512");
     if (p->kv_format != CSA2_NVFP4 || p->win_format != CSA2_E4M3 || p->q_format != CSA2_BF16)
-        return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn_layers: formats must be NVFP4, E4M3, BF16");
+        return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn_layers_mma: formats must be NVFP4, E4M3, BF16");
     if (!q || !sink || !win || !n_tokens || !comp || !comp_scales || !idx || !out)
-        return fail(CSA2_ERR_INVALID_ARG, "sparse_attn_layers: NULL buffer");
+        return fail(CSA2_ERR_INVALID_ARG, "sparse_attn_layers_mma: NULL buffer");
     if (!aligned16(q) || !aligned16(out))
-        return fail(CSA2_ERR_ALIGN, "sparse_attn_layers: q, out must be 16-byte aligned");
-    if (L > 65535 || B > 65535) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn_layers: grid too large");
+        return fail(CSA2_ERR_ALIGN, "sparse_attn_layers_mma: q, out must be 16-byte aligned");
+    if (L > 65535 || B > 65535) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn_layers_mma: grid too large");
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(k_sparse_attn_fd, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kSmemFd) != cudaSuccess)
-            return check_launch("sparse_attn_layers: smem attribute");
+            return check_launch("sparse_attn_layers_mma: smem attribute");
         attr = true;
     }
     k_sparse_attn_fd<<<dim3(L, B), kFdThreads, kSmemFd, static_cast<cudaStream_t>(stream)>>>(
         B, static_cast<const __nv_bfloat16*>(q), sink, win, n_tokens, comp, comp_scales, idx,
         p->compress_ratio, p->softmax_scale * kLog2e, static_cast<__nv_bfloat16*>(out), dev_status,
         p->win_layout == CSA2_WIN_LINEAR);
-    return check_launch("sparse_attn_layers");
+    return check_launch("sparse_attn_layers_mma");
 }
 
 extern "C" int csa2_sparse_attn(const csa2_params* p, int B, const void* q, const float* sink,

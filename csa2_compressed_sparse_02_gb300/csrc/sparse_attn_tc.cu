@@ -1,0 +1,574 @@
+// Fused multi-layer sparse attention on the 5th-generation tensor cores
+// (tcgen05): the decode query of each sequence attends to its 128-slot window
+// and its 512 selected compressed positions, with a per-head sink logit in the
+// denominator ("DeepSeek-V4.1-Flash-NVFP4" §3.4 gather + online softmax +
+// attn_sink, §三 640 positions per query, §3.1 FP8 window, §一 one shared
+// 512-d KV head so K = V = the latent, §四 reader layers share the source
+// layer's compressed cache and selection).
+//
+// Work unit: one (layer, sequence); a persistent CTA per SM walks its units.
+// The 640 positions are 5 tiles of 128 (tile 0 = the window ring, tiles 1..4 =
+// idx[0..512) in 128s). Per tile, with the positions as the MMA's M:
+//   S^T[128 x 64]  = K_tile[128 x 512] . Q^T            (TMEM, 64 columns)
+//   O^T[512 x 64] += V_tile^T[512 x 128] . P^T[128 x 64] (TMEM, 4 x 64 columns)
+// The tile is decoded exactly into f16 in shared memory once and is the A
+// operand of both products: K-major for S (rows = positions), MN-major for PV
+// (the latent dims run along the rows). E2M1 x E4M3 has at most 5 significant
+// bits and E4M3 4, so both are exact in f16. The query is scaled per head by a
+// power of two into f16 (exact except below 2^-24 of the head's largest
+// element) and the factor is folded into the logit scale.
+//
+// Roles: 8 producer warps gather and decode rows (and stage Q), one thread
+// issues every MMA, 8 softmax warps (4 TMEM lane quarters x 2 head halves)
+// turn S into P in shared memory and finally read O out. The softmax keeps a
+// per-head running maximum that only moves when a tile's maximum exceeds it by
+// more than 2^8 (then the O columns of those heads are rescaled in TMEM), so P
+// stays <= 256 and the common path never touches O. Every wait is bounded.
+#include <mutex>
+
+#include "common.cuh"
+#include "sm100.cuh"
+
+namespace csa2 {
+namespace {
+using namespace sm100;
+
+constexpr int kTiles = (kW + kKp) / 128;  // 5
+constexpr int kSoftWarps = 8;
+constexpr int kProdWarps = 8;
+constexpr int kMmaWarp = kSoftWarps + kProdWarps;  // 16
+constexpr int kAttnThreads = 32 * (kMmaWarp + 1);  // 544
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLazyMax = 8.0f;  // log2 of the largest P the lazy maximum allows
+
+constexpr uint32_t kQChunk = 64 * 128;    // 64 heads x 64 dims (f16), one 128-byte row per head
+constexpr uint32_t kKVChunk = 128 * 128;  // 128 positions x 64 dims
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColO = 0;    // O^T: 4 blocks of 128 dims x 64 heads
+constexpr uint32_t kColS = 256;  // S^T: 128 positions x 64 heads
+
+// Instruction descriptors (kind::f16): D fp32 (bits 4..5 = 1), A and B f16
+// (bits 7..9, 10..12 = 0), N = 64 (N>>3 in bits 17..22), M = 128 (M>>4 in
+// bits 24..28); bits 15 / 16 select MN-major A / B.
+constexpr uint32_t kIdescS = (1u << 4) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t kIdescPV = kIdescS | (1u << 15) | (1u << 16);
+
+struct AttnShared {
+    uint8_t q[8][kQChunk];    // B operand of S: Q[64 heads x 512] f16, 128-byte swizzle, K-major
+    uint8_t kv[8][kKVChunk];  // the decoded tile [128 x 512] f16 in 8 column chunks, 128-byte swizzle
+    uint8_t p[128 * 128];     // B operand of PV: P[128 positions x 64 heads] f16, MN-major
+    float col_scale[2][64];   // per-head logit factor (softmax scale x log2 e / query scale), by unit parity
+    float red_max[4][64];     // per lane quarter: the tile's maximum of each head
+    float red_sum[4][64];     // per lane quarter: the running sum of each head
+    uint64_t q_full, q_empty, s_full, p_full, o_full, drain;
+    uint64_t chunk_full[4], chunk_empty[4], red_max_bar[2], red_sum_bar[2];
+    uint32_t tmem_base;
+    int abort;
+};
+constexpr int kAttnSmem = (int)sizeof(AttnShared) + 1024;
+
+// 16-byte unit u of row r in a 128-byte-swizzled region (8 units per row).
+__device__ __forceinline__ uint32_t sw128(int r, int u) {
+    return (uint32_t)(r * 128 + ((u ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t h2_lo(uint32_t h2) { return __byte_perm(h2, 0u, 0x1010); }
+__device__ __forceinline__ uint32_t h2_hi(uint32_t h2) { return __byte_perm(h2, 0u, 0x3232); }
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+__device__ __forceinline__ uint32_t f32x2_to_h2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ bool win_row_valid(int r, int64_t T, int linear) {
+    return T > 0 && (linear ? T - kW + r >= 0 : (T >= kW || (int64_t)r < T));
+}
+
+// Reduce 32 per-head values across the 32 lanes of a warp; lane h returns the
+// result for head h. Each step hands half of the remaining heads to the
+// partner lane, so the whole transpose-reduce takes 31 shuffles.
+template <bool kMax>
+__device__ __forceinline__ float xreduce32(float (&v)[32], int lane) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int i = 0; i < o; ++i) {
+            const float keep = up ? v[i + o] : v[i];
+            const float give = up ? v[i] : v[i + o];
+            const float got = __shfl_xor_sync(0xffffffffu, give, o);
+            v[i] = kMax ? fmaxf(keep, got) : keep + got;
+        }
+    }
+    return v[0];
+}
+
+// 32 S^T columns of this lane's row from TMEM, times the per-head logit factor.
+__device__ __forceinline__ void load_logits(uint32_t taddr, const float* col_scale, bool valid,
+                                            float (&x)[32]) {
+    uint32_t sv[32];
+    tmem_ld_32x32b_x32(taddr, sv);
+    const float4* cs = reinterpret_cast<const float4*>(col_scale);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 c4 = cs[i];
+        x[4 * i] = valid ? __uint_as_float(sv[4 * i]) * c4.x : -INFINITY;
+        x[4 * i + 1] = valid ? __uint_as_float(sv[4 * i + 1]) * c4.y : -INFINITY;
+        x[4 * i + 2] = valid ? __uint_as_float(sv[4 * i + 2]) * c4.z : -INFINITY;
+        x[4 * i + 3] = valid ? __uint_as_float(sv[4 * i + 3]) * c4.w : -INFINITY;
+    }
+}
+
+struct UnitArgs {
+    int L, B, ratio, win_linear;
+    float scale_log2;
+    const __nv_bfloat16* q;
+    const float* sink;
+    const void* const* win;
+    const int32_t* n_tokens;
+    const void* const* comp;
+    const uint8_t* const* comp_scales;
+    const int32_t* idx;
+    __nv_bfloat16* out;
+    int32_t* dev_status;
+};
+
+__device__ __forceinline__ bool unit_aligned(const UnitArgs& a, int u, int b) {
+    const uintptr_t w = reinterpret_cast<uintptr_t>(a.win[u]);
+    const uintptr_t c = reinterpret_cast<uintptr_t>(a.comp[b]);
+    const uintptr_t s = reinterpret_cast<uintptr_t>(a.comp_scales[b]);
+    return ((w | c) & 15u) == 0 && (s & 3u) == 0;
+}
+
+// ---------------------------------------------------------------- producers
+// Thread (r, hf) of the 256 producer threads owns row r of every tile and the
+// column chunk 2*pair + hf of each pair of chunks (64 dims).
+__device__ void producer_role(AttnShared& sh, const UnitArgs& a, int pt, int lane,
+                              volatile int* abort) {
+    const int pw = pt >> 5, r = pt >> 1, hf = pt & 1;
+    const int n_units = a.L * a.B;
+    int it = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
+        const int b = u % a.B;
+        const int64_t T = a.n_tokens[b];
+        const int64_t n_c = T > 0 ? T / a.ratio : 0;
+        const bool aligned = unit_aligned(a, u, b);
+        if (!aligned && pt == 0) raise_status(a.dev_status, CSA2_DEV_BAD_ALIGN);
+
+        // selected positions of this thread's row in tiles 1..4
+        int32_t xs[kTiles - 1];
+#pragma unroll
+        for (int j = 0; j < kTiles - 1; ++j) xs[j] = a.idx[(int64_t)b * kKp + 128 * j + r];
+
+        // ---- query: warp pw stages heads 8pw..8pw+7, lane = dims 16*lane..+15
+        {
+            const uint4* qu = reinterpret_cast<const uint4*>(a.q + (int64_t)u * kH * kD);
+            uint4 qa[4], qb[4];
+#pragma unroll
+            for (int hi = 0; hi < 4; ++hi) {
+                const uint4* src = qu + (int64_t)(8 * pw + hi) * (kD / 8) + 2 * lane;
+                qa[hi] = __ldg(src);
+                qb[hi] = __ldg(src + 1);
+            }
+            if (it > 0 && !mbar_wait(&sh.q_empty, (uint32_t)((it - 1) & 1), abort)) return;
+#pragma unroll
+            for (int hi = 0; hi < 8; ++hi) {
+                const int h = 8 * pw + hi;
+                const uint32_t w[8] = {qa[hi & 3].x, qa[hi & 3].y, qa[hi & 3].z, qa[hi & 3].w,
+                                       qb[hi & 3].x, qb[hi & 3].y, qb[hi & 3].z, qb[hi & 3].w};
+                if (hi < 4) {  // the second half of the heads: issue its loads now
+                    const uint4* src = qu + (int64_t)(8 * pw + hi + 4) * (kD / 8) + 2 * lane;
+                    qa[hi] = __ldg(src);
+                    qb[hi] = __ldg(src + 1);
+                }
+                float f[16];
+                float mx = 0.f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    f[2 * k] = __uint_as_float(w[k] << 16);
+                    f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+                    mx = fmaxf(mx, fmaxf(fabsf(f[2 * k]), fabsf(f[2 * k + 1])));
+                }
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                // 2^s with the head's largest |q| in [2^14, 2^15): f16 keeps 11 bits down to 2^-14
+                int s = 14 - ((int)((__float_as_uint(mx) >> 23) & 0xffu) - 127);
+                s = max(-126, min(126, s));
+                const float two_s = __uint_as_float((uint32_t)(s + 127) << 23);
+                uint32_t hq[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) hq[k] = f32x2_to_h2(f[2 * k] * two_s, f[2 * k + 1] * two_s);
+                uint8_t* row = sh.q[lane >> 2];
+                const int u0 = (lane & 3) * 2;
+                *reinterpret_cast<uint4*>(row + sw128(h, u0)) = make_uint4(hq[0], hq[1], hq[2], hq[3]);
+                *reinterpret_cast<uint4*>(row + sw128(h, u0 + 1)) = make_uint4(hq[4], hq[5], hq[6], hq[7]);
+                if (lane == 0)
+                    sh.col_scale[it & 1][h] = a.scale_log2 * __uint_as_float((uint32_t)(127 - s) << 23);
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.q_full);
+
+        // ---- the 5 tiles
+        const uint8_t* winb = static_cast<const uint8_t*>(a.win[u]);
+        const uint8_t* compb = static_cast<const uint8_t*>(a.comp[b]);
+        const uint8_t* compsb = a.comp_scales[b];
+        for (int j = 0; j < kTiles; ++j) {
+            const int gt = it * kTiles + j;
+            // window: two pairs in flight (4 x 16 B each); compressed: all four (2 x 16 B + scales)
+            uint4 raw[8];
+            uint32_t scw[4];
+            bool valid;
+            const uint4* wsrc = nullptr;
+            if (j == 0) {
+                valid = aligned && win_row_valid(r, T, a.win_linear);
+                wsrc = reinterpret_cast<const uint4*>(winb + (int64_t)r * kD + 64 * hf);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    raw[k] = valid ? __ldg(wsrc + 8 * (k >> 2) + (k & 3)) : make_uint4(0u, 0u, 0u, 0u);
+            } else {
+                const int64_t x0 = xs[j - 1];
+                if (x0 >= n_c && hf == 0) raise_status(a.dev_status, CSA2_DEV_BAD_INDEX);
+                valid = aligned && x0 >= 0 && x0 < n_c;
+                const int64_t x = valid ? x0 : 0;
+                const uint4* src = reinterpret_cast<const uint4*>(compb + x * (kD / 2) + 32 * hf);
+                const uint32_t* ssrc = reinterpret_cast<const uint32_t*>(compsb + x * (kD / kGroup) + 4 * hf);
+#pragma unroll
+                for (int pr = 0; pr < 4; ++pr) {
+                    raw[2 * pr] = valid ? __ldg(src + 4 * pr) : make_uint4(0u, 0u, 0u, 0u);
+                    raw[2 * pr + 1] = valid ? __ldg(src + 4 * pr + 1) : make_uint4(0u, 0u, 0u, 0u);
+                    scw[pr] = valid ? __ldg(ssrc + 2 * pr) : 0u;
+                }
+            }
+#pragma unroll
+            for (int pr = 0; pr < 4; ++pr) {
+                if (gt > 0 && !mbar_wait(&sh.chunk_empty[pr], (uint32_t)((gt - 1) & 1), abort)) return;
+                uint32_t o[32];
+                if (!valid) {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0u;
+                } else if (j == 0) {  // 64 E4M3 bytes -> 64 f16
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint4 v = raw[4 * (pr & 1) + k];
+                        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            o[8 * k + 2 * i] = e4m3x2_to_h2(w4[i]);
+                            o[8 * k + 2 * i + 1] = e4m3x2_to_h2(w4[i] >> 16);
+                        }
+                    }
+                    if (pr + 2 < 4) {  // refill the slot with pair pr + 2
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) raw[4 * (pr & 1) + k] = __ldg(wsrc + 8 * (pr + 2) + k);
+                    }
+                } else {  // 32 E2M1 bytes (4 groups of 16) x E4M3 group scale -> 64 f16
+                    const uint32_t w8[8] = {raw[2 * pr].x,     raw[2 * pr].y,     raw[2 * pr].z,
+                                            raw[2 * pr].w,     raw[2 * pr + 1].x, raw[2 * pr + 1].y,
+                                            raw[2 * pr + 1].z, raw[2 * pr + 1].w};
+                    const uint32_t s01 = e4m3x2_to_h2(scw[pr]), s23 = e4m3x2_to_h2(scw[pr] >> 16);
+                    const uint32_t sg[4] = {h2_lo(s01), h2_hi(s01), h2_lo(s23), h2_hi(s23)};
+#pragma unroll
+                    for (int g = 0; g < 4; ++g)
+#pragma unroll
+                        for (int bi = 0; bi < 8; ++bi)
+                            o[8 * g + bi] = hmul2(
+                                e2m1x2_to_half2((w8[2 * g + (bi >> 2)] >> (8 * (bi & 3))) & 0xffu), sg[g]);
+                }
+                uint8_t* dst = sh.kv[2 * pr + hf];
+#pragma unroll
+                for (int un = 0; un < 8; ++un)
+                    *reinterpret_cast<uint4*>(dst + sw128(r, un)) =
+                        make_uint4(o[4 * un], o[4 * un + 1], o[4 * un + 2], o[4 * un + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.chunk_full[pr]);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- MMA issuer
+__device__ void mma_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, volatile int* abort) {
+    const uint32_t sQ = smem_u32(sh.q[0]), sKV = smem_u32(sh.kv[0]), sP = smem_u32(sh.p);
+    const int n_units = a.L * a.B;
+    int it = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
+        if (!mbar_wait(&sh.q_full, (uint32_t)(it & 1), abort)) return;
+        tc_fence_after();
+        for (int j = 0; j < kTiles; ++j) {
+            const int gt = it * kTiles + j;
+            // S^T = K . Q^T over the 512 dims, chunk pair by chunk pair as they land
+            for (int pr = 0; pr < 4; ++pr) {
+                if (!mbar_wait(&sh.chunk_full[pr], (uint32_t)(gt & 1), abort)) return;
+                tc_fence_after();
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c = 2 * pr + cc;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t ad = smem_desc(sKV + c * kKVChunk + 32 * k, 16, 1024, kLayoutSw128);
+                        const uint64_t bd = smem_desc(sQ + c * kQChunk + 32 * k, 16, 1024, kLayoutSw128);
+                        mma_f16(tmem + kColS, ad, bd, kIdescS, (pr | cc | k) != 0);
+                    }
+                }
+            }
+            tc_commit(&sh.s_full);
+            if (j == kTiles - 1) tc_commit(&sh.q_empty);
+            // O^T += V^T . P^T, one block of 128 dims (= one chunk pair) at a time
+            if (!mbar_wait(&sh.p_full, (uint32_t)(gt & 1), abort)) return;
+            tc_fence_after();
+            for (int mb = 0; mb < 4; ++mb) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint64_t ad =
+                        smem_desc(sKV + 2 * mb * kKVChunk + k * 2048, kKVChunk, 1024, kLayoutSw128);
+                    const uint64_t bd = smem_desc(sP + k * 2048, 1024, 1024, kLayoutSw128);
+                    mma_f16(tmem + kColO + 64 * mb, ad, bd, kIdescPV, (j | k) != 0);
+                }
+                tc_commit(&sh.chunk_empty[mb]);
+            }
+        }
+        tc_commit(&sh.o_full);
+    }
+}
+
+// ---------------------------------------------------------------- softmax + epilogue
+__device__ void softmax_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, int warp, int lane,
+                             volatile int* abort) {
+    const int qd = warp & 3, hh = warp >> 2;
+    const int r = 32 * qd + lane;                   // position row of the tile
+    const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);  // this warp's TMEM lane quarter
+    const int n_units = a.L * a.B;
+    int it = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
+        const int l = u / a.B, b = u % a.B;
+        const int64_t T = a.n_tokens[b];
+        const int64_t n_c = T > 0 ? T / a.ratio : 0;
+        const bool aligned = unit_aligned(a, u, b);
+        if (!mbar_wait(&sh.q_full, (uint32_t)(it & 1), abort)) return;
+        float m_run = -INFINITY, l_run = 0.f;  // of head 32hh + lane, over this quarter's rows
+        for (int j = 0; j < kTiles; ++j) {
+            const int gt = it * kTiles + j;
+            bool valid;
+            if (j == 0) {
+                valid = aligned && win_row_valid(r, T, a.win_linear);
+            } else {
+                const int64_t x = a.idx[(int64_t)b * kKp + 128 * (j - 1) + r];
+                valid = aligned && x >= 0 && x < n_c;
+            }
+            if (!mbar_wait(&sh.s_full, (uint32_t)(gt & 1), abort)) return;
+            tc_fence_after();
+            // logits of this row (log2 domain), head 32hh + i; invalid rows -inf
+            float x[32];
+            load_logits(tl + kColS + 32 * hh, &sh.col_scale[it & 1][32 * hh], valid, x);
+            // tile maximum of head 32hh + lane over all 128 rows
+            sh.red_max[qd][32 * hh + lane] = xreduce32<true>(x, lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.red_max_bar[hh]);
+            if (!mbar_wait(&sh.red_max_bar[hh], (uint32_t)(gt & 1), abort)) return;
+            const float tm = fmaxf(fmaxf(sh.red_max[0][32 * hh + lane], sh.red_max[1][32 * hh + lane]),
+                                   fmaxf(sh.red_max[2][32 * hh + lane], sh.red_max[3][32 * hh + lane]));
+            load_logits(tl + kColS + 32 * hh, &sh.col_scale[it & 1][32 * hh], valid, x);  // again: the reduction consumed x
+            // lazy maximum: move only when this tile would push P above 2^kLazyMax
+            const float m_new = tm > m_run + kLazyMax ? tm : m_run;
+            const float alpha = (m_new != m_run && m_run != -INFINITY) ? ex2(m_run - m_new) : 1.f;
+            const bool rescale = __any_sync(0xffffffffu, alpha != 1.f);
+            l_run *= alpha;
+            m_run = m_new;
+            const float mfix = m_run == -INFINITY ? 0.f : m_run;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) x[i] = ex2(x[i] - __shfl_sync(0xffffffffu, mfix, i));
+            uint8_t* prow = sh.p;
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+                *reinterpret_cast<uint4*>(prow + sw128(r, 4 * hh + q4)) =
+                    make_uint4(f32x2_to_h2(x[8 * q4], x[8 * q4 + 1]), f32x2_to_h2(x[8 * q4 + 2], x[8 * q4 + 3]),
+                               f32x2_to_h2(x[8 * q4 + 4], x[8 * q4 + 5]),
+                               f32x2_to_h2(x[8 * q4 + 6], x[8 * q4 + 7]));
+            l_run += xreduce32<false>(x, lane);
+            if (rescale) {  // O holds tiles < j (complete: S of tile j was issued after them)
+#pragma unroll 1
+                for (int mb = 0; mb < 4; ++mb) {
+                    uint32_t ov[32];
+                    tmem_ld_32x32b_x32(tl + kColO + 64 * mb + 32 * hh, ov);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        ov[i] = __float_as_uint(__uint_as_float(ov[i]) * __shfl_sync(0xffffffffu, alpha, i));
+                    tmem_st_32x32b_x32(tl + kColO + 64 * mb + 32 * hh, ov);
+                }
+                tmem_wait_st();
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.p_full);
+        }
+        // ---- epilogue: o_h = O_h 2^{m-M} / (l 2^{m-M} + 2^{sink2-M}), M = max(m, sink2)
+        if (!mbar_wait(&sh.o_full, (uint32_t)(it & 1), abort)) return;
+        tc_fence_after();
+        sh.red_sum[qd][32 * hh + lane] = l_run;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sh.red_sum_bar[hh]);
+        if (!mbar_wait(&sh.red_sum_bar[hh], (uint32_t)(it & 1), abort)) return;
+        const float lsum = (sh.red_sum[0][32 * hh + lane] + sh.red_sum[1][32 * hh + lane]) +
+                           (sh.red_sum[2][32 * hh + lane] + sh.red_sum[3][32 * hh + lane]);
+        const float sink2 = a.sink[(int64_t)l * kH + 32 * hh + lane] * kLog2e;
+        const float M = fmaxf(m_run, sink2);
+        const float sc = m_run == -INFINITY ? 0.f : exp2f(m_run - M);
+        const float fin = sc / (lsum * sc + exp2f(sink2 - M));
+        __nv_bfloat16* ob = a.out + (int64_t)u * kH * kD + 32 * hh * kD;
+#pragma unroll 1
+        for (int mb = 0; mb < 4; ++mb) {
+            uint32_t ov[32];
+            tmem_ld_32x32b_x32(tl + kColO + 64 * mb + 32 * hh, ov);
+            const int d = 128 * mb + 32 * qd + lane;
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                ob[i * kD + d] =
+                    __float2bfloat16_rn(__uint_as_float(ov[i]) * __shfl_sync(0xffffffffu, fin, i));
+        }
+        tc_fence_before();
+    }
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 1) k_sparse_attn_tc(UnitArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    AttnShared& sh = *reinterpret_cast<AttnShared*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    volatile int* abort = &sh.abort;
+    if (tid == 0) {
+        mbar_init(&sh.q_full, kProdWarps);
+        mbar_init(&sh.q_empty, 1);
+        mbar_init(&sh.s_full, 1);
+        mbar_init(&sh.p_full, kSoftWarps);
+        mbar_init(&sh.o_full, 1);
+        mbar_init(&sh.drain, 1);
+        for (int i = 0; i < 4; ++i) {
+            mbar_init(&sh.chunk_full[i], kProdWarps);
+            mbar_init(&sh.chunk_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sh.red_max_bar[i], 4);
+            mbar_init(&sh.red_sum_bar[i], 4);
+        }
+        sh.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&sh.tmem_base, kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+
+    if (warp < kSoftWarps) {
+        softmax_role(sh, a, tmem, warp, lane, abort);
+    } else if (warp < kMmaWarp) {
+        producer_role(sh, a, tid - 32 * kSoftWarps, lane, abort);
+    } else if (lane == 0) {
+        mma_role(sh, a, tmem, abort);
+        // every MMA issued must finish before TMEM and shared memory are released
+        tc_commit(&sh.drain);
+        if (!mbar_wait_drain(&sh.drain, 0)) *abort = 1;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && sh.abort) raise_status(a.dev_status, CSA2_DEV_TIMEOUT);
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+int sm_count(int dev) {
+    static int n[64] = {0};
+    if (dev < 0 || dev >= 64) return 1;
+    if (!n[dev]) {
+        int v = 0;
+        cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev);
+        n[dev] = v > 0 ? v : 1;
+    }
+    return n[dev];
+}
+
+}  // namespace
+}  // namespace csa2
+
+using namespace csa2;
+
+extern "C" int csa2_sparse_attn_layers(const csa2_params* p, int L, int B, const void* q,
+                                       const float* sink, const void* const* win,
+                                       const int32_t* n_tokens, const void* const* comp,
+                                       const uint8_t* const* comp_scales, const int32_t* idx,
+                                       void* out, int32_t* dev_status, void* stream) {
+    CSA2_CHECK_PARAMS(p);
+    if (L < 0 || B < 0) return fail(CSA2_ERR_INVALID_ARG, "sparse_attn_layers: negative size");
+    if (L == 0 || B == 0) return CSA2_OK;
+    if (p->heads != kH || p->head_dim != kD || p->window != kW || p->topk_pos != kKp ||
+        p->compress_ratio < 1)
+        return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn_layers: built for 64 heads x 512, W=128, k=512");
+    if (p->kv_format != CSA2_NVFP4 || p->win_format != CSA2_E4M3 || p->q_format != CSA2_BF16)
+        return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn_layers: formats must be NVFP4, E4M3, BF16");
+    if (!q || !sink || !win || !n_tokens || !comp || !comp_scales || !idx || !out)
+        return fail(CSA2_ERR_INVALID_ARG, "sparse_attn_layers: NULL buffer");
+    if (!aligned16(q) || !aligned16(out))
+        return fail(CSA2_ERR_ALIGN, "sparse_attn_layers: q, out must be 16-byte aligned");
+    if ((int64_t)L * B > (int64_t)1 << 30)
+        return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn_layers: too many (layer, sequence) units");
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return check_launch("sparse_attn_layers: device");
+    {
+        static std::mutex mu;
+        static uint64_t attr_set = 0;
+        std::lock_guard<std::mutex> g(mu);
+        if (dev >= 0 && dev < 64 && !((attr_set >> dev) & 1u)) {
+            if (cudaFuncSetAttribute(k_sparse_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kAttnSmem) != cudaSuccess)
+                return check_launch("sparse_attn_layers: smem attribute");
+            attr_set |= 1ull << dev;
+        }
+    }
+    UnitArgs a;
+    a.L = L;
+    a.B = B;
+    a.ratio = p->compress_ratio;
+    a.win_linear = p->win_layout == CSA2_WIN_LINEAR;
+    a.scale_log2 = p->softmax_scale * kLog2e;
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.sink = sink;
+    a.win = win;
+    a.n_tokens = n_tokens;
+    a.comp = comp;
+    a.comp_scales = comp_scales;
+    a.idx = idx;
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.dev_status = dev_status;
+    const int64_t units = (int64_t)L * B;
+    const int64_t sms = sm_count(dev);
+    const int grid = (int)(units < sms ? units : sms);
+    k_sparse_attn_tc<<<grid, kAttnThreads, kAttnSmem, static_cast<cudaStream_t>(stream)>>>(a);
+    return check_launch("sparse_attn_layers");
+}

@@ -56,6 +56,7 @@ extern "C" {
 #define CSA2_DEV_BAD_INDEX 1   /* a selected index >= the sequence's compressed length */
 #define CSA2_DEV_BAD_LENGTH 2  /* a sequence length beyond the stated capacity, or < 0 */
 #define CSA2_DEV_TIMEOUT 4     /* a pipeline wait gave up (the kernel returned early) */
+#define CSA2_DEV_BAD_ALIGN 8   /* a per-sequence buffer base is misaligned (its rows read as empty) */
 
 /* ---- formats ---- */
 #define CSA2_F32 0   /* fp32 */
@@ -281,12 +282,18 @@ int csa2_sparse_attn(const csa2_params* p, int B,
  * compressed cache and one selection ("DeepSeek-V4.1-Flash-NVFP4" §四: the
  * KV-source layers' compressed cache is read by the layers in between; §3.3:
  * a published top-k is reused), each with its own query, window and sink.
- * Same arithmetic as csa2_sparse_attn; one CTA per (layer, sequence) streams
- * all 640 positions with an online softmax, so it needs no workspace.
+ * Same arithmetic as csa2_sparse_attn, on the tcgen05 tensor cores: a
+ * persistent CTA per SM takes (layer, sequence) units and streams their 640
+ * positions with an online softmax, so it needs no workspace. Decoded rows
+ * and P are 16-bit (f16) MMA operands with fp32 accumulation; the query is
+ * scaled per head by a power of two into f16.
  *   q    [L, B, H, D] bf16      sink [L, H] fp32      out [L, B, H, D] bf16
  *   win  device array [L*B] of ring bases, layer-major (entry l*B + b)
  *   n_tokens [B]: raw tokens of sequence b (the same in every layer: the layers
  *        process one token stream); comp, comp_scales [B]; idx [B, topk_pos].
+ *   Bases win[l*B+b] and comp[b] must be 16-byte aligned and comp_scales[b]
+ *   4-byte aligned; a misaligned base sets CSA2_DEV_BAD_ALIGN and that unit's
+ *   rows read as empty. q and out 16-byte aligned (else CSA2_ERR_ALIGN).
  * Constraints: H == 64, D == 512, W == 128, topk_pos == 512, NVFP4 cache,
  * E4M3 window, bf16 query/output.
  */
@@ -296,6 +303,19 @@ int csa2_sparse_attn_layers(const csa2_params* p, int L, int B,
                             const void* const* comp, const uint8_t* const* comp_scales,
                             const int32_t* idx, void* out,
                             int32_t* dev_status, void* stream);
+
+/*
+ * csa2_sparse_attn_layers_mma — the same contract as csa2_sparse_attn_layers on
+ * the legacy warp-level tensor-core path (mma.sync bf16, P rounded to bf16),
+ * one CTA per (layer, sequence) with the output accumulator in registers.
+ * Kept as a second, independent implementation of the fused reader attention.
+ */
+int csa2_sparse_attn_layers_mma(const csa2_params* p, int L, int B,
+                                const void* q, const float* sink,
+                                const void* const* win, const int32_t* n_tokens,
+                                const void* const* comp, const uint8_t* const* comp_scales,
+                                const int32_t* idx, void* out,
+                                int32_t* dev_status, void* stream);
 
 /*
  * csa2_sparse_attn_noalloc — csa2_sparse_attn without a caller workspace.

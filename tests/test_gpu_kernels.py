@@ -387,7 +387,8 @@ def test_sparse_attn_out_of_range_index_is_skipped_and_flagged():
     assert ok, e
 
 
-def test_sparse_attn_layers_matches_oracle_per_layer():
+@pytest.mark.parametrize("mma_sync", [False, True], ids=["tcgen05", "mma_sync"])
+def test_sparse_attn_layers_matches_oracle_per_layer(mma_sync):
     """L layers share one compressed cache and one selection; each has its own
     window ring, query and sink (the KV-sharing readers of a source layer)."""
     rng = np.random.default_rng(31)
@@ -428,9 +429,9 @@ def test_sparse_attn_layers_matches_oracle_per_layer():
     out = torch.empty(L, B, 64, 512, dtype=torch.bfloat16, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     api.sparse_attn_layers(p, q_dev, t(sink), win_all, src.n_tokens, src.comp_ptrs,
-                           src.comp_scale_ptrs, t(idx), out, status)
+                           src.comp_scale_ptrs, t(idx), out, status, mma_sync=mma_sync)
     torch.cuda.synchronize()
-    assert status.item() & 1
+    assert status.item() == 1
     got = out.float().cpu().numpy().astype(np.float64)
     q64 = synth.bf16_to_f64(qb)
     for l in range(L):
@@ -442,5 +443,81 @@ def test_sparse_attn_layers_matches_oracle_per_layer():
             ref, _ = orc.sparse_attn(q64[l, b], sink[l].astype(np.float64), 1 / math.sqrt(512), T,
                                      128, win_u8=win, comp_vals=s.comp_vals,
                                      comp_scales=s.comp_scales, idx=keep)
+            ok, e = close_bf16(got[l, b], ref)
+            assert ok, (l, b, T, e)
+
+
+def _e4m3_small_bytes(rng, shape):
+    """E4M3 bytes of magnitude < 4 (exponent field <= 8), random sign."""
+    e = rng.integers(0, 9, shape)
+    m = rng.integers(0, 8, shape)
+    sgn = rng.integers(0, 2, shape)
+    return ((sgn << 7) | (e << 3) | m).astype(np.uint8)
+
+
+@pytest.mark.parametrize("mma_sync", [False, True], ids=["tcgen05", "mma_sync"])
+def test_sparse_attn_layers_rescale_and_many_units(mma_sync):
+    """192 (layer, sequence) units (more than one per SM), partial windows, empty
+    and out-of-range selections, NaN bytes in window slots that are not yet
+    valid, and planted compressed rows aligned with a query head whose logits
+    jump far above the window's in tiles 2 and 4, so the running maximum moves
+    in the middle of the stream (the output must not depend on where)."""
+    rng = np.random.default_rng(77)
+    L, B = 4, 48
+    Ts = [int(x) for x in rng.choice([40, 127, 128, 300, 1000, 2049, 5000], B)]
+    p = api.default_params()
+    n_cs = [T // 2 for T in Ts]
+    src = api.LayerCache(B, [max(1, n) for n in n_cs], p)
+    wins = [api.LayerCache(B, [1] * B, p, has_comp=False) for _ in range(L - 1)]
+    q = rng.standard_normal((L, B, 64, 512)).astype(np.float32)
+    qb = synth.bf16_bits_rne(q)
+    q64 = synth.bf16_to_f64(qb)
+    idx = np.full((B, 512), -1, np.int32)
+    comp_v, comp_s, win_b = [], [], [[None] * B for _ in range(L)]
+    for b, T in enumerate(Ts):
+        n_c = n_cs[b]
+        rows = rng.standard_normal((max(1, n_c), 512)).astype(np.float32)
+        k = min(512, n_c)
+        if k:
+            idx[b, :k] = np.sort(rng.choice(n_c, k, replace=False))
+        if n_c >= 512 and b % 3 != 2:  # plant: head h0 of layer 0 aligned with two selected rows
+            h0 = b % 64
+            sign = np.where(q64[0, b, h0] >= 0, 1.0, -1.0).astype(np.float32)
+            rows[idx[b, 200]] = sign
+            rows[idx[b, 450]] = 3 * sign
+        if b % 5 == 4 and k:
+            idx[b, k // 2:] = -1  # a short selection
+        if b == 7 and k:
+            idx[b, 3] = n_c + 5  # out of range: skipped, flagged
+        v, sc = orc.nvfp4_quantize(rows)
+        comp_v.append(v)
+        comp_s.append(sc)
+        src.comp[b][: v.shape[0]].copy_(t(v))
+        src.comp_scales[b][: sc.shape[0]].copy_(t(sc))
+        for l in range(L):
+            w = _e4m3_small_bytes(rng, (128, 512))
+            if T < 128:
+                w[T:] = 0x7F  # E4M3 NaN in slots that hold no token yet
+            win_b[l][b] = w
+            (src.win[b] if l == 0 else wins[l - 1].win[b]).copy_(t(w))
+    src.n_tokens.copy_(t(np.array(Ts, np.int32)))
+    q_dev = torch.from_numpy(qb.view(np.int16)).to(DEV).view(torch.bfloat16)
+    sink = rng.standard_normal((L, 64)).astype(np.float32)
+    win_all = torch.cat([src.win_ptrs] + [w.win_ptrs for w in wins])
+    out = torch.empty(L, B, 64, 512, dtype=torch.bfloat16, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    api.sparse_attn_layers(p, q_dev, t(sink), win_all, src.n_tokens, src.comp_ptrs,
+                           src.comp_scale_ptrs, t(idx), out, status, mma_sync=mma_sync)
+    torch.cuda.synchronize()
+    assert status.item() == 1  # the planted out-of-range index only
+    got = out.float().cpu().numpy().astype(np.float64)
+    assert np.isfinite(got).all()
+    for l in range(L):
+        for b, T in enumerate(Ts):
+            keep = idx[b].copy()
+            keep[keep >= n_cs[b]] = -1
+            ref, _ = orc.sparse_attn(q64[l, b], sink[l].astype(np.float64), 1 / math.sqrt(512), T,
+                                     128, win_u8=win_b[l][b], comp_vals=comp_v[b],
+                                     comp_scales=comp_s[b], idx=keep)
             ok, e = close_bf16(got[l, b], ref)
             assert ok, (l, b, T, e)
