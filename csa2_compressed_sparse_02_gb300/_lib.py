@@ -27,7 +27,7 @@ class Params(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "heads", "head_dim", "index_heads", "index_dim", "window", "block_size", "topk_blocks",
         "topk_pos", "compress_ratio", "kv_format", "win_format", "q_format")] + [
-        ("softmax_scale", ctypes.c_float), ("win_layout", ctypes.c_int)]
+        ("softmax_scale", ctypes.c_float), ("win_layout", ctypes.c_int), ("max_ctas", ctypes.c_int)]
 
 
 PP = ctypes.POINTER(Params)

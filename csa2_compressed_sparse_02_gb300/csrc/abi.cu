@@ -39,6 +39,7 @@ extern "C" void csa2_default_params(csa2_params* p) {
     p->q_format = CSA2_BF16;
     p->softmax_scale = 1.0f / std::sqrt((float)csa2::kD);
     p->win_layout = CSA2_WIN_RING;
+    p->max_ctas = 0;
 }
 
 extern "C" int csa2_version(void) { return 200; }

@@ -510,7 +510,9 @@ extern "C" int csa2_index_scores(const csa2_params* p, int B, int64_t max_ncomp,
         attr = true;
     }
     const int64_t tiles_max = (int64_t)B * ((max_ncomp + kTilesPerStage * kKeyTile - 1) / (kTilesPerStage * kKeyTile));
-    const int grid = (int)std::min<int64_t>(tiles_max, num_sms());
+    int64_t ctas = num_sms();
+    if (p->max_ctas > 0 && p->max_ctas < ctas) ctas = p->max_ctas;
+    const int grid = (int)std::min<int64_t>(tiles_max, ctas);
     k_index_scores_tc<<<grid, kTcThreads, kTcSmem, static_cast<cudaStream_t>(stream)>>>(
         B, max_ncomp, p->compress_ratio, q_vals, q_scales, w, key_cache, n_tokens, scores,
         block_max, dev_status);

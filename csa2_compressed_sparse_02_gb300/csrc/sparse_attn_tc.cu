@@ -59,7 +59,7 @@ struct AttnShared {
     uint8_t p[128 * 128];     // B operand of PV: P[128 positions x 64 heads] f16, MN-major
     float col_scale[2][64];   // per-head logit factor (softmax scale x log2 e / query scale), by unit parity
     float red_max[4][64];     // per lane quarter: the tile's maximum of each head
-    float red_sum[4][64];     // per lane quarter: the running sum of each head
+    float red_sum[4][64];     // per lane quarter: the sum over its 32 rows of each head
     uint64_t q_full, q_empty, s_full, p_full, o_full, drain;
     uint64_t chunk_full[4], chunk_empty[4], red_max_bar[2], red_sum_bar[2];
     uint32_t tmem_base;
@@ -81,9 +81,21 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
     return d;
 }
 
-__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xffffu), __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// Eight E2M1 codes (one word, element 0 in the low nibble) -> four f16 pairs, exact.
+__device__ __forceinline__ void e2m1x8_to_h2x4(uint32_t w, uint32_t* o) {
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+        " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+        : "r"(w));
+}
+
+// Four E4M3 bytes (one word) -> two f16 pairs, exact.
+__device__ __forceinline__ void e4m3x4_to_h2x2(uint32_t w, uint32_t* o) {
+    asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n"
+        " cvt.rn.f16x2.e4m3x2 %0, lo;\n cvt.rn.f16x2.e4m3x2 %1, hi;\n}"
+        : "=r"(o[0]), "=r"(o[1])
+        : "r"(w));
 }
 
 __device__ __forceinline__ uint32_t f32x2_to_h2(float lo, float hi) {
@@ -101,27 +113,32 @@ __device__ __forceinline__ bool win_row_valid(int r, int64_t T, int linear) {
     return T > 0 && (linear ? T - kW + r >= 0 : (T >= kW || (int64_t)r < T));
 }
 
-// Reduce 32 per-head values across the 32 lanes of a warp; lane h returns the
-// result for head h. Each step hands half of the remaining heads to the
-// partner lane, so the whole transpose-reduce takes 31 shuffles.
-template <bool kMax>
-__device__ __forceinline__ float xreduce32(float (&v)[32], int lane) {
+// Sum 16 per-head values over the 32 lanes of a warp; lane h returns head
+// h mod 16. Each step hands half of the remaining heads to the partner lane,
+// a last exchange adds the two lane halves (16 shuffles).
+__device__ __forceinline__ float xreduce_sum16(float* v, int lane) {
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
+    for (int o = 8; o >= 1; o >>= 1) {
         const bool up = (lane & o) != 0;
 #pragma unroll
         for (int i = 0; i < o; ++i) {
             const float keep = up ? v[i + o] : v[i];
             const float give = up ? v[i] : v[i + o];
-            const float got = __shfl_xor_sync(0xffffffffu, give, o);
-            v[i] = kMax ? fmaxf(keep, got) : keep + got;
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, give, o);
         }
     }
-    return v[0];
+    return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 16);
 }
 
-// 32 S^T columns of this lane's row from TMEM, times the per-head logit factor.
-__device__ __forceinline__ void load_logits(uint32_t taddr, const float* col_scale, bool valid,
+__device__ __forceinline__ float warp_max(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;\n" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// 32 S^T columns of this lane's row from TMEM times the per-head logit factor,
+// plus the row's bias (0, or -inf for a row that holds no position).
+__device__ __forceinline__ void load_logits(uint32_t taddr, const float* col_scale, float bias,
                                             float (&x)[32]) {
     uint32_t sv[32];
     tmem_ld_32x32b_x32(taddr, sv);
@@ -129,10 +146,10 @@ __device__ __forceinline__ void load_logits(uint32_t taddr, const float* col_sca
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const float4 c4 = cs[i];
-        x[4 * i] = valid ? __uint_as_float(sv[4 * i]) * c4.x : -INFINITY;
-        x[4 * i + 1] = valid ? __uint_as_float(sv[4 * i + 1]) * c4.y : -INFINITY;
-        x[4 * i + 2] = valid ? __uint_as_float(sv[4 * i + 2]) * c4.z : -INFINITY;
-        x[4 * i + 3] = valid ? __uint_as_float(sv[4 * i + 3]) * c4.w : -INFINITY;
+        x[4 * i] = fmaf(__uint_as_float(sv[4 * i]), c4.x, bias);
+        x[4 * i + 1] = fmaf(__uint_as_float(sv[4 * i + 1]), c4.y, bias);
+        x[4 * i + 2] = fmaf(__uint_as_float(sv[4 * i + 2]), c4.z, bias);
+        x[4 * i + 3] = fmaf(__uint_as_float(sv[4 * i + 3]), c4.w, bias);
     }
 }
 
@@ -261,20 +278,22 @@ __device__ void producer_role(AttnShared& sh, const UnitArgs& a, int pt, int lan
 #pragma unroll
             for (int pr = 0; pr < 4; ++pr) {
                 if (gt > 0 && !mbar_wait(&sh.chunk_empty[pr], (uint32_t)((gt - 1) & 1), abort)) return;
-                uint32_t o[32];
+                uint8_t* dst = sh.kv[2 * pr + hf];
                 if (!valid) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = 0u;
-                } else if (j == 0) {  // 64 E4M3 bytes -> 64 f16
+                    for (int un = 0; un < 8; ++un)
+                        *reinterpret_cast<uint4*>(dst + sw128(r, un)) = make_uint4(0u, 0u, 0u, 0u);
+                } else if (j == 0) {  // 64 E4M3 bytes -> 64 f16, unit un = bytes 8un..8un+7
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const uint4 v = raw[4 * (pr & 1) + k];
-                        const uint32_t w4[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            o[8 * k + 2 * i] = e4m3x2_to_h2(w4[i]);
-                            o[8 * k + 2 * i + 1] = e4m3x2_to_h2(w4[i] >> 16);
-                        }
+                        uint32_t o[8];
+                        e4m3x4_to_h2x2(v.x, &o[0]);
+                        e4m3x4_to_h2x2(v.y, &o[2]);
+                        e4m3x4_to_h2x2(v.z, &o[4]);
+                        e4m3x4_to_h2x2(v.w, &o[6]);
+                        *reinterpret_cast<uint4*>(dst + sw128(r, 2 * k)) = make_uint4(o[0], o[1], o[2], o[3]);
+                        *reinterpret_cast<uint4*>(dst + sw128(r, 2 * k + 1)) = make_uint4(o[4], o[5], o[6], o[7]);
                     }
                     if (pr + 2 < 4) {  // refill the slot with pair pr + 2
 #pragma unroll
@@ -284,20 +303,18 @@ __device__ void producer_role(AttnShared& sh, const UnitArgs& a, int pt, int lan
                     const uint32_t w8[8] = {raw[2 * pr].x,     raw[2 * pr].y,     raw[2 * pr].z,
                                             raw[2 * pr].w,     raw[2 * pr + 1].x, raw[2 * pr + 1].y,
                                             raw[2 * pr + 1].z, raw[2 * pr + 1].w};
-                    const uint32_t s01 = e4m3x2_to_h2(scw[pr]), s23 = e4m3x2_to_h2(scw[pr] >> 16);
-                    const uint32_t sg[4] = {h2_lo(s01), h2_hi(s01), h2_lo(s23), h2_hi(s23)};
+                    uint32_t s4[2];
+                    e4m3x4_to_h2x2(scw[pr], s4);
+                    const uint32_t sg[4] = {h2_lo(s4[0]), h2_hi(s4[0]), h2_lo(s4[1]), h2_hi(s4[1])};
 #pragma unroll
-                    for (int g = 0; g < 4; ++g)
-#pragma unroll
-                        for (int bi = 0; bi < 8; ++bi)
-                            o[8 * g + bi] = hmul2(
-                                e2m1x2_to_half2((w8[2 * g + (bi >> 2)] >> (8 * (bi & 3))) & 0xffu), sg[g]);
+                    for (int wi = 0; wi < 8; ++wi) {  // word wi = 8 codes of group wi / 2 = unit wi
+                        uint32_t o[4];
+                        e2m1x8_to_h2x4(w8[wi], o);
+                        *reinterpret_cast<uint4*>(dst + sw128(r, wi)) =
+                            make_uint4(hmul2(o[0], sg[wi >> 1]), hmul2(o[1], sg[wi >> 1]),
+                                       hmul2(o[2], sg[wi >> 1]), hmul2(o[3], sg[wi >> 1]));
+                    }
                 }
-                uint8_t* dst = sh.kv[2 * pr + hf];
-#pragma unroll
-                for (int un = 0; un < 8; ++un)
-                    *reinterpret_cast<uint4*>(dst + sw128(r, un)) =
-                        make_uint4(o[4 * un], o[4 * un + 1], o[4 * un + 2], o[4 * un + 3]);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh.chunk_full[pr]);
@@ -308,7 +325,12 @@ __device__ void producer_role(AttnShared& sh, const UnitArgs& a, int pt, int lan
 
 // ---------------------------------------------------------------- MMA issuer
 __device__ void mma_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, volatile int* abort) {
-    const uint32_t sQ = smem_u32(sh.q[0]), sKV = smem_u32(sh.kv[0]), sP = smem_u32(sh.p);
+    // Descriptors are built once; a K step or a chunk moves only the start
+    // address field (bits 0..13, address >> 4), which never carries out.
+    const uint64_t dKV = smem_desc(smem_u32(sh.kv[0]), 16, 1024, kLayoutSw128);
+    const uint64_t dQ = smem_desc(smem_u32(sh.q[0]), 16, 1024, kLayoutSw128);
+    const uint64_t dV = smem_desc(smem_u32(sh.kv[0]), kKVChunk, 1024, kLayoutSw128);
+    const uint64_t dP = smem_desc(smem_u32(sh.p), 1024, 1024, kLayoutSw128);
     const int n_units = a.L * a.B;
     int it = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
@@ -317,33 +339,30 @@ __device__ void mma_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, volat
         for (int j = 0; j < kTiles; ++j) {
             const int gt = it * kTiles + j;
             // S^T = K . Q^T over the 512 dims, chunk pair by chunk pair as they land
+#pragma unroll
             for (int pr = 0; pr < 4; ++pr) {
                 if (!mbar_wait(&sh.chunk_full[pr], (uint32_t)(gt & 1), abort)) return;
                 tc_fence_after();
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    const int c = 2 * pr + cc;
+                for (int cc = 0; cc < 2; ++cc)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const uint64_t ad = smem_desc(sKV + c * kKVChunk + 32 * k, 16, 1024, kLayoutSw128);
-                        const uint64_t bd = smem_desc(sQ + c * kQChunk + 32 * k, 16, 1024, kLayoutSw128);
-                        mma_f16(tmem + kColS, ad, bd, kIdescS, (pr | cc | k) != 0);
+                        const int c = 2 * pr + cc;
+                        mma_f16(tmem + kColS, dKV + ((c * kKVChunk + 32 * k) >> 4),
+                                dQ + ((c * kQChunk + 32 * k) >> 4), kIdescS, (pr | cc | k) != 0);
                     }
-                }
             }
             tc_commit(&sh.s_full);
             if (j == kTiles - 1) tc_commit(&sh.q_empty);
             // O^T += V^T . P^T, one block of 128 dims (= one chunk pair) at a time
             if (!mbar_wait(&sh.p_full, (uint32_t)(gt & 1), abort)) return;
             tc_fence_after();
+#pragma unroll
             for (int mb = 0; mb < 4; ++mb) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint64_t ad =
-                        smem_desc(sKV + 2 * mb * kKVChunk + k * 2048, kKVChunk, 1024, kLayoutSw128);
-                    const uint64_t bd = smem_desc(sP + k * 2048, 1024, 1024, kLayoutSw128);
-                    mma_f16(tmem + kColO + 64 * mb, ad, bd, kIdescPV, (j | k) != 0);
-                }
+                for (int k = 0; k < 8; ++k)
+                    mma_f16(tmem + kColO + 64 * mb, dV + ((2 * mb * kKVChunk + k * 2048) >> 4),
+                            dP + ((k * 2048) >> 4), kIdescPV, (j | k) != 0);
                 tc_commit(&sh.chunk_empty[mb]);
             }
         }
@@ -364,56 +383,83 @@ __device__ void softmax_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, i
         const int64_t T = a.n_tokens[b];
         const int64_t n_c = T > 0 ? T / a.ratio : 0;
         const bool aligned = unit_aligned(a, u, b);
+        const float sink2 = a.sink[(int64_t)l * kH + 32 * hh + lane] * kLog2e;  // needed at the end
+        int32_t xs[kTiles - 1];  // this row's selected positions in tiles 1..4
+#pragma unroll
+        for (int j = 0; j < kTiles - 1; ++j) xs[j] = a.idx[(int64_t)b * kKp + 128 * j + r];
         if (!mbar_wait(&sh.q_full, (uint32_t)(it & 1), abort)) return;
-        float m_run = -INFINITY, l_run = 0.f;  // of head 32hh + lane, over this quarter's rows
+        float m_run = -INFINITY;  // running maximum of head 32hh + lane
+        float lpart[32];          // this row's share of the sum of P, head 32hh + i
+#pragma unroll
+        for (int i = 0; i < 32; ++i) lpart[i] = 0.f;
         for (int j = 0; j < kTiles; ++j) {
             const int gt = it * kTiles + j;
-            bool valid;
-            if (j == 0) {
-                valid = aligned && win_row_valid(r, T, a.win_linear);
-            } else {
-                const int64_t x = a.idx[(int64_t)b * kKp + 128 * (j - 1) + r];
-                valid = aligned && x >= 0 && x < n_c;
-            }
+            const bool valid = j == 0 ? aligned && win_row_valid(r, T, a.win_linear)
+                                      : aligned && xs[j - 1] >= 0 && xs[j - 1] < n_c;
             if (!mbar_wait(&sh.s_full, (uint32_t)(gt & 1), abort)) return;
             tc_fence_after();
-            // logits of this row (log2 domain), head 32hh + i; invalid rows -inf
-            float x[32];
-            load_logits(tl + kColS + 32 * hh, &sh.col_scale[it & 1][32 * hh], valid, x);
-            // tile maximum of head 32hh + lane over all 128 rows
-            sh.red_max[qd][32 * hh + lane] = xreduce32<true>(x, lane);
+            const float bias = valid ? 0.f : -INFINITY;
+            {  // warp maximum of every head (uniform in the warp); lane 0 publishes this quarter's
+                float x[32];  // logits (log2 domain) of this row, head 32hh + i; -inf for an empty row
+                load_logits(tl + kColS + 32 * hh, &sh.col_scale[it & 1][32 * hh], bias, x);
+#pragma unroll
+                for (int i = 0; i < 32; i += 4) {
+                    const float4 r4 = make_float4(warp_max(x[i]), warp_max(x[i + 1]), warp_max(x[i + 2]),
+                                                  warp_max(x[i + 3]));
+                    if (lane == 0) *reinterpret_cast<float4*>(&sh.red_max[qd][32 * hh + i]) = r4;
+                }
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.red_max_bar[hh]);
             if (!mbar_wait(&sh.red_max_bar[hh], (uint32_t)(gt & 1), abort)) return;
             const float tm = fmaxf(fmaxf(sh.red_max[0][32 * hh + lane], sh.red_max[1][32 * hh + lane]),
                                    fmaxf(sh.red_max[2][32 * hh + lane], sh.red_max[3][32 * hh + lane]));
-            load_logits(tl + kColS + 32 * hh, &sh.col_scale[it & 1][32 * hh], valid, x);  // again: the reduction consumed x
             // lazy maximum: move only when this tile would push P above 2^kLazyMax
             const float m_new = tm > m_run + kLazyMax ? tm : m_run;
             const float alpha = (m_new != m_run && m_run != -INFINITY) ? ex2(m_run - m_new) : 1.f;
             const bool rescale = __any_sync(0xffffffffu, alpha != 1.f);
-            l_run *= alpha;
             m_run = m_new;
             const float mfix = m_run == -INFINITY ? 0.f : m_run;
+            if (rescale) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) x[i] = ex2(x[i] - __shfl_sync(0xffffffffu, mfix, i));
-            uint8_t* prow = sh.p;
+                for (int i = 0; i < 32; ++i) lpart[i] *= __shfl_sync(0xffffffffu, alpha, i);
+            }
+            // P = 2^(x - m) in two halves of 16 heads, read again from TMEM (keeps registers low)
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4)
-                *reinterpret_cast<uint4*>(prow + sw128(r, 4 * hh + q4)) =
-                    make_uint4(f32x2_to_h2(x[8 * q4], x[8 * q4 + 1]), f32x2_to_h2(x[8 * q4 + 2], x[8 * q4 + 3]),
-                               f32x2_to_h2(x[8 * q4 + 4], x[8 * q4 + 5]),
-                               f32x2_to_h2(x[8 * q4 + 6], x[8 * q4 + 7]));
-            l_run += xreduce32<false>(x, lane);
+            for (int hf = 0; hf < 2; ++hf) {
+                uint32_t sv[16];
+                tmem_ld_32x32b_x16(tl + kColS + 32 * hh + 16 * hf, sv);
+                const float4* cs = reinterpret_cast<const float4*>(&sh.col_scale[it & 1][32 * hh + 16 * hf]);
+                float pv[16];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float4 c4 = cs[i];
+                    const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int hi = 4 * i + e;
+                        pv[hi] = ex2(fmaf(__uint_as_float(sv[hi]), cc[e], bias) -
+                                     __shfl_sync(0xffffffffu, mfix, 16 * hf + hi));
+                        lpart[16 * hf + hi] += pv[hi];
+                    }
+                }
+#pragma unroll
+                for (int q2 = 0; q2 < 2; ++q2)
+                    *reinterpret_cast<uint4*>(sh.p + sw128(r, 4 * hh + 2 * hf + q2)) =
+                        make_uint4(f32x2_to_h2(pv[8 * q2], pv[8 * q2 + 1]), f32x2_to_h2(pv[8 * q2 + 2], pv[8 * q2 + 3]),
+                                   f32x2_to_h2(pv[8 * q2 + 4], pv[8 * q2 + 5]),
+                                   f32x2_to_h2(pv[8 * q2 + 6], pv[8 * q2 + 7]));
+            }
             if (rescale) {  // O holds tiles < j (complete: S of tile j was issued after them)
 #pragma unroll 1
-                for (int mb = 0; mb < 4; ++mb) {
+                for (int blk = 0; blk < 4; ++blk) {
+                    const uint32_t col = kColO + 64 * blk + 32 * hh;
                     uint32_t ov[32];
-                    tmem_ld_32x32b_x32(tl + kColO + 64 * mb + 32 * hh, ov);
+                    tmem_ld_32x32b_x32(tl + col, ov);
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
                         ov[i] = __float_as_uint(__uint_as_float(ov[i]) * __shfl_sync(0xffffffffu, alpha, i));
-                    tmem_st_32x32b_x32(tl + kColO + 64 * mb + 32 * hh, ov);
+                    tmem_st_32x32b_x32(tl + col, ov);
                 }
                 tmem_wait_st();
             }
@@ -425,26 +471,38 @@ __device__ void softmax_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, i
         // ---- epilogue: o_h = O_h 2^{m-M} / (l 2^{m-M} + 2^{sink2-M}), M = max(m, sink2)
         if (!mbar_wait(&sh.o_full, (uint32_t)(it & 1), abort)) return;
         tc_fence_after();
-        sh.red_sum[qd][32 * hh + lane] = l_run;
+        {
+            const float lo = xreduce_sum16(lpart, lane), hi = xreduce_sum16(lpart + 16, lane);
+            sh.red_sum[qd][32 * hh + lane] = lane < 16 ? lo : hi;
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.red_sum_bar[hh]);
         if (!mbar_wait(&sh.red_sum_bar[hh], (uint32_t)(it & 1), abort)) return;
         const float lsum = (sh.red_sum[0][32 * hh + lane] + sh.red_sum[1][32 * hh + lane]) +
                            (sh.red_sum[2][32 * hh + lane] + sh.red_sum[3][32 * hh + lane]);
-        const float sink2 = a.sink[(int64_t)l * kH + 32 * hh + lane] * kLog2e;
         const float M = fmaxf(m_run, sink2);
         const float sc = m_run == -INFINITY ? 0.f : exp2f(m_run - M);
         const float fin = sc / (lsum * sc + exp2f(sink2 - M));
+        // lane holds dim d of 32 heads; lanes 2k and 2k+1 trade halves so each
+        // stores a bf16 pair (dims d, d+1) of 16 heads: even lanes the even heads
         __nv_bfloat16* ob = a.out + (int64_t)u * kH * kD + 32 * hh * kD;
+        const bool odd = lane & 1;
 #pragma unroll 1
         for (int mb = 0; mb < 4; ++mb) {
             uint32_t ov[32];
             tmem_ld_32x32b_x32(tl + kColO + 64 * mb + 32 * hh, ov);
-            const int d = 128 * mb + 32 * qd + lane;
+            const int d0 = 128 * mb + 32 * qd + (lane & ~1);
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                ob[i * kD + d] =
-                    __float2bfloat16_rn(__uint_as_float(ov[i]) * __shfl_sync(0xffffffffu, fin, i));
+            for (int i = 0; i < 32; i += 2) {
+                const float v0 = __uint_as_float(ov[i]) * __shfl_sync(0xffffffffu, fin, i);
+                const float v1 = __uint_as_float(ov[i + 1]) * __shfl_sync(0xffffffffu, fin, i + 1);
+                // even lane keeps head i and sends head i+1; odd lane the reverse
+                const float mine = odd ? v1 : v0, give = odd ? v0 : v1;
+                const float got = __shfl_xor_sync(0xffffffffu, give, 1);
+                const __nv_bfloat162 pr2 = odd ? __floats2bfloat162_rn(got, mine)
+                                               : __floats2bfloat162_rn(mine, got);
+                *reinterpret_cast<__nv_bfloat162*>(ob + (i + (odd ? 1 : 0)) * kD + d0) = pr2;
+            }
         }
         tc_fence_before();
     }
@@ -567,7 +625,8 @@ extern "C" int csa2_sparse_attn_layers(const csa2_params* p, int L, int B, const
     a.out = static_cast<__nv_bfloat16*>(out);
     a.dev_status = dev_status;
     const int64_t units = (int64_t)L * B;
-    const int64_t sms = sm_count(dev);
+    int64_t sms = sm_count(dev);
+    if (p->max_ctas > 0 && p->max_ctas < sms) sms = p->max_ctas;
     const int grid = (int)(units < sms ? units : sms);
     k_sparse_attn_tc<<<grid, kAttnThreads, kAttnSmem, static_cast<cudaStream_t>(stream)>>>(a);
     return check_launch("sparse_attn_layers");

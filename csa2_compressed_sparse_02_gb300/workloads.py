@@ -200,9 +200,11 @@ class DecodeRun:
         torch.cuda.synchronize()
 
     # ------------------------------------------------------------------ one step
-    def _timed(self, timers, cat, st, fn):
+    def _timed(self, timers, cat, st, fn, *args):
+        """Run fn(st, *args) (which enqueues on stream st), bracketed by timing
+        events on st when timers is a dict."""
         if timers is None:
-            fn()
+            fn(st, *args)
             return
         torch = self.torch
         kw = {"enable_timing": True}
@@ -210,54 +212,55 @@ class DecodeRun:
             kw["external"] = True
         e0, e1 = torch.cuda.Event(**kw), torch.cuda.Event(**kw)
         e0.record(st)
-        fn()
+        fn(st, *args)
         e1.record(st)
         timers.setdefault(cat, []).append((e0, e1))
+
+    # the four calls of a group's step, each enqueued on stream s
+    def _compress(self, s, grp, k):
+        src, cfg = grp["src"], self.cfg
+        src.append(grp["kv"][k], grp["gate"][k], self.dev_status, s)
+        if cfg.readers > 1:
+            grp["rd"].append(grp["kv_rd"][k], None, self.dev_status, s)
+
+    def _index(self, s, grp, k, params):
+        self.api.index_scores(params, self.max_ncomp, grp["iq"][k], grp["iqs"][k], grp["iw"][k],
+                              grp["keys"].ptrs, grp["src"].n_tokens, grp["scores"], grp["bmax"],
+                              self.dev_status, s, cuda_cores=self.cuda_core_indexer)
+
+    def _select(self, s, grp, k):
+        self.api.select_topk(self.params, self.max_ncomp, grp["scores"], grp["bmax"],
+                             grp["src"].n_tokens, grp["idx"], grp["n_sel"], self.dev_status, s)
+
+    def _attn(self, s, grp, k, params):
+        api, cfg, src = self.api, self.cfg, grp["src"]
+        if cfg.quant and self.fused_attention:
+            api.sparse_attn_layers(params, grp["q"][k], grp["sink_all"], grp["win_all"],
+                                   src.n_tokens, src.comp_ptrs, src.comp_scale_ptrs, grp["idx"],
+                                   grp["out_all"], self.dev_status, s)
+            return
+        for r in range(cfg.readers):
+            if r == 0:
+                win_ptrs, n_tok = src.win_ptrs, src.n_tokens
+            else:
+                sl = slice((r - 1) * self.B, r * self.B)
+                win_ptrs, n_tok = grp["rd"].win_ptrs[sl], grp["rd"].n_tokens[sl]
+            api.sparse_attn(self.params, grp["q"][k, r], grp["sink"][r], win_ptrs, n_tok,
+                            src.comp_ptrs, src.comp_scale_ptrs, grp["idx"], grp["out"][r],
+                            self.workspace, self.dev_status, s)
 
     def _enqueue(self, k, stream=None, timers=None):
         """Enqueue one decode step (every group, every layer) using input slot k.
         timers: optional dict receiving (start, end) CUDA events per call category
-        ("compress", "index", "select", "attn"), recorded on the launching stream."""
-        api, cfg, p, torch = self.api, self.cfg, self.params, self.torch
-        st = torch.cuda.current_stream() if stream is None else stream
-        ds = self.dev_status
+        ("compress", "index", "select", "attn"), recorded on the launching stream.
+        Groups run in layer order: group g+1's index query comes from the hidden
+        state after group g's layers, so its scan cannot start earlier."""
+        st = self.torch.cuda.current_stream() if stream is None else stream
         for grp in self.groups:
-            src = grp["src"]
-
-            def compress():
-                src.append(grp["kv"][k], grp["gate"][k], ds, stream)
-                if cfg.readers > 1:
-                    grp["rd"].append(grp["kv_rd"][k], None, ds, stream)
-
-            def index():
-                api.index_scores(p, self.max_ncomp, grp["iq"][k], grp["iqs"][k], grp["iw"][k],
-                                 grp["keys"].ptrs, src.n_tokens, grp["scores"], grp["bmax"], ds,
-                                 stream, cuda_cores=self.cuda_core_indexer)
-
-            def select():
-                api.select_topk(p, self.max_ncomp, grp["scores"], grp["bmax"], src.n_tokens,
-                                grp["idx"], grp["n_sel"], ds, stream)
-
-            def attn():
-                if cfg.quant and self.fused_attention:
-                    api.sparse_attn_layers(p, grp["q"][k], grp["sink_all"], grp["win_all"],
-                                           src.n_tokens, src.comp_ptrs, src.comp_scale_ptrs,
-                                           grp["idx"], grp["out_all"], ds, stream)
-                    return
-                for r in range(cfg.readers):
-                    if r == 0:
-                        win_ptrs, n_tok = src.win_ptrs, src.n_tokens
-                    else:
-                        sl = slice((r - 1) * self.B, r * self.B)
-                        win_ptrs, n_tok = grp["rd"].win_ptrs[sl], grp["rd"].n_tokens[sl]
-                    api.sparse_attn(p, grp["q"][k, r], grp["sink"][r], win_ptrs, n_tok,
-                                    src.comp_ptrs, src.comp_scale_ptrs, grp["idx"], grp["out"][r],
-                                    self.workspace, ds, stream)
-
-            self._timed(timers, "compress", st, compress)
-            self._timed(timers, "index", st, index)
-            self._timed(timers, "select", st, select)
-            self._timed(timers, "attn", st, attn)
+            self._timed(timers, "compress", st, self._compress, grp, k)
+            self._timed(timers, "index", st, self._index, grp, k, self.params)
+            self._timed(timers, "select", st, self._select, grp, k)
+            self._timed(timers, "attn", st, self._attn, grp, k, self.params)
 
     def step(self, stream=None, timers=None):
         """Enqueue the next decode step eagerly (one launch per kernel)."""

@@ -82,6 +82,10 @@ typedef struct csa2_params {
                              newest raw position p < T with p mod W = r) or
                              CSA2_WIN_LINEAR (row r = raw position T-W+r; used by
                              prefill, where each query has its own window) */
+    int max_ctas;         /* upper bound on the CTAs of the persistent kernels
+                             (csa2_index_scores, csa2_sparse_attn_layers); 0 = one
+                             per SM. A caller that runs two of them concurrently on
+                             different streams splits the SMs with it. */
 } csa2_params;
 
 #define CSA2_WIN_RING 0
