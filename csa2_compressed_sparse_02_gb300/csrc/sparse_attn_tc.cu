@@ -136,23 +136,6 @@ __device__ __forceinline__ float warp_max(float v) {
     return r;
 }
 
-// 32 S^T columns of this lane's row from TMEM times the per-head logit factor,
-// plus the row's bias (0, or -inf for a row that holds no position).
-__device__ __forceinline__ void load_logits(uint32_t taddr, const float* col_scale, float bias,
-                                            float (&x)[32]) {
-    uint32_t sv[32];
-    tmem_ld_32x32b_x32(taddr, sv);
-    const float4* cs = reinterpret_cast<const float4*>(col_scale);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float4 c4 = cs[i];
-        x[4 * i] = fmaf(__uint_as_float(sv[4 * i]), c4.x, bias);
-        x[4 * i + 1] = fmaf(__uint_as_float(sv[4 * i + 1]), c4.y, bias);
-        x[4 * i + 2] = fmaf(__uint_as_float(sv[4 * i + 2]), c4.z, bias);
-        x[4 * i + 3] = fmaf(__uint_as_float(sv[4 * i + 3]), c4.w, bias);
-    }
-}
-
 struct UnitArgs {
     int L, B, ratio, win_linear;
     float scale_log2;
@@ -371,22 +354,33 @@ __device__ void mma_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, volat
 }
 
 // ---------------------------------------------------------------- softmax + epilogue
+// Per-unit values a softmax thread needs, loaded one unit ahead.
+struct SoftUnit {
+    int32_t T, n_c;  // raw tokens, compressed positions
+    bool aligned;
+    float sink2;     // sink logit of head 32hh + lane, log2 domain
+    int32_t xs[4];   // this row's selected positions in tiles 1..4
+    __device__ __forceinline__ void load(const UnitArgs& a, int u, int r, int hh, int lane) {
+        const int l = u / a.B, b = u % a.B;
+        T = a.n_tokens[b];
+        n_c = T > 0 ? T / a.ratio : 0;
+        aligned = unit_aligned(a, u, b);
+        sink2 = a.sink[(int64_t)l * kH + 32 * hh + lane] * kLog2e;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) xs[j] = a.idx[(int64_t)b * kKp + 128 * j + r];
+    }
+};
+
 __device__ void softmax_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, int warp, int lane,
                              volatile int* abort) {
     const int qd = warp & 3, hh = warp >> 2;
     const int r = 32 * qd + lane;                   // position row of the tile
     const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);  // this warp's TMEM lane quarter
     const int n_units = a.L * a.B;
+    SoftUnit cu, nx;
+    if ((int)blockIdx.x < n_units) cu.load(a, blockIdx.x, r, hh, lane);
     int it = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
-        const int l = u / a.B, b = u % a.B;
-        const int64_t T = a.n_tokens[b];
-        const int64_t n_c = T > 0 ? T / a.ratio : 0;
-        const bool aligned = unit_aligned(a, u, b);
-        const float sink2 = a.sink[(int64_t)l * kH + 32 * hh + lane] * kLog2e;  // needed at the end
-        int32_t xs[kTiles - 1];  // this row's selected positions in tiles 1..4
-#pragma unroll
-        for (int j = 0; j < kTiles - 1; ++j) xs[j] = a.idx[(int64_t)b * kKp + 128 * j + r];
         if (!mbar_wait(&sh.q_full, (uint32_t)(it & 1), abort)) return;
         float m_run = -INFINITY;  // running maximum of head 32hh + lane
         float lpart[32];          // this row's share of the sum of P, head 32hh + i
@@ -394,19 +388,32 @@ __device__ void softmax_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, i
         for (int i = 0; i < 32; ++i) lpart[i] = 0.f;
         for (int j = 0; j < kTiles; ++j) {
             const int gt = it * kTiles + j;
-            const bool valid = j == 0 ? aligned && win_row_valid(r, T, a.win_linear)
-                                      : aligned && xs[j - 1] >= 0 && xs[j - 1] < n_c;
+            const bool valid = j == 0 ? cu.aligned && win_row_valid(r, cu.T, a.win_linear)
+                                      : cu.aligned && cu.xs[j - 1] >= 0 && cu.xs[j - 1] < cu.n_c;
+            if (j == kTiles - 1 && u + (int)gridDim.x < n_units)  // next unit's scalars, early
+                nx.load(a, u + gridDim.x, r, hh, lane);
             if (!mbar_wait(&sh.s_full, (uint32_t)(gt & 1), abort)) return;
             tc_fence_after();
             const float bias = valid ? 0.f : -INFINITY;
-            {  // warp maximum of every head (uniform in the warp); lane 0 publishes this quarter's
-                float x[32];  // logits (log2 domain) of this row, head 32hh + i; -inf for an empty row
-                load_logits(tl + kColS + 32 * hh, &sh.col_scale[it & 1][32 * hh], bias, x);
+            // warp maximum of every head (uniform in the warp), 8 heads at a time;
+            // lane 0 publishes this quarter's
 #pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    const float4 r4 = make_float4(warp_max(x[i]), warp_max(x[i + 1]), warp_max(x[i + 2]),
-                                                  warp_max(x[i + 3]));
-                    if (lane == 0) *reinterpret_cast<float4*>(&sh.red_max[qd][32 * hh + i]) = r4;
+            for (int c8 = 0; c8 < 4; ++c8) {
+                uint32_t sv[8];
+                tmem_ld_32x32b_x8(tl + kColS + 32 * hh + 8 * c8, sv);
+                const float4* cs = reinterpret_cast<const float4*>(&sh.col_scale[it & 1][32 * hh + 8 * c8]);
+                const float4 ca = cs[0], cb = cs[1];
+                const float4 ra = make_float4(warp_max(fmaf(__uint_as_float(sv[0]), ca.x, bias)),
+                                              warp_max(fmaf(__uint_as_float(sv[1]), ca.y, bias)),
+                                              warp_max(fmaf(__uint_as_float(sv[2]), ca.z, bias)),
+                                              warp_max(fmaf(__uint_as_float(sv[3]), ca.w, bias)));
+                const float4 rb = make_float4(warp_max(fmaf(__uint_as_float(sv[4]), cb.x, bias)),
+                                              warp_max(fmaf(__uint_as_float(sv[5]), cb.y, bias)),
+                                              warp_max(fmaf(__uint_as_float(sv[6]), cb.z, bias)),
+                                              warp_max(fmaf(__uint_as_float(sv[7]), cb.w, bias)));
+                if (lane == 0) {
+                    *reinterpret_cast<float4*>(&sh.red_max[qd][32 * hh + 8 * c8]) = ra;
+                    *reinterpret_cast<float4*>(&sh.red_max[qd][32 * hh + 8 * c8 + 4]) = rb;
                 }
             }
             __syncwarp();
@@ -424,31 +431,25 @@ __device__ void softmax_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, i
 #pragma unroll
                 for (int i = 0; i < 32; ++i) lpart[i] *= __shfl_sync(0xffffffffu, alpha, i);
             }
-            // P = 2^(x - m) in two halves of 16 heads, read again from TMEM (keeps registers low)
+            // P = 2^(x - m) in four chunks of 8 heads (one 16-byte unit of the P row
+            // each), read again from TMEM: keeps the working set small
 #pragma unroll
-            for (int hf = 0; hf < 2; ++hf) {
-                uint32_t sv[16];
-                tmem_ld_32x32b_x16(tl + kColS + 32 * hh + 16 * hf, sv);
-                const float4* cs = reinterpret_cast<const float4*>(&sh.col_scale[it & 1][32 * hh + 16 * hf]);
-                float pv[16];
+            for (int c8 = 0; c8 < 4; ++c8) {
+                uint32_t sv[8];
+                tmem_ld_32x32b_x8(tl + kColS + 32 * hh + 8 * c8, sv);
+                const float4* cs = reinterpret_cast<const float4*>(&sh.col_scale[it & 1][32 * hh + 8 * c8]);
+                const float4 ca = cs[0], cb = cs[1];
+                const float cc[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+                float pv[8];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float4 c4 = cs[i];
-                    const float cc[4] = {c4.x, c4.y, c4.z, c4.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int hi = 4 * i + e;
-                        pv[hi] = ex2(fmaf(__uint_as_float(sv[hi]), cc[e], bias) -
-                                     __shfl_sync(0xffffffffu, mfix, 16 * hf + hi));
-                        lpart[16 * hf + hi] += pv[hi];
-                    }
+                for (int e = 0; e < 8; ++e) {
+                    pv[e] = ex2(fmaf(__uint_as_float(sv[e]), cc[e], bias) -
+                                __shfl_sync(0xffffffffu, mfix, 8 * c8 + e));
+                    lpart[8 * c8 + e] += pv[e];
                 }
-#pragma unroll
-                for (int q2 = 0; q2 < 2; ++q2)
-                    *reinterpret_cast<uint4*>(sh.p + sw128(r, 4 * hh + 2 * hf + q2)) =
-                        make_uint4(f32x2_to_h2(pv[8 * q2], pv[8 * q2 + 1]), f32x2_to_h2(pv[8 * q2 + 2], pv[8 * q2 + 3]),
-                                   f32x2_to_h2(pv[8 * q2 + 4], pv[8 * q2 + 5]),
-                                   f32x2_to_h2(pv[8 * q2 + 6], pv[8 * q2 + 7]));
+                *reinterpret_cast<uint4*>(sh.p + sw128(r, 4 * hh + c8)) =
+                    make_uint4(f32x2_to_h2(pv[0], pv[1]), f32x2_to_h2(pv[2], pv[3]),
+                               f32x2_to_h2(pv[4], pv[5]), f32x2_to_h2(pv[6], pv[7]));
             }
             if (rescale) {  // O holds tiles < j (complete: S of tile j was issued after them)
 #pragma unroll 1
@@ -480,30 +481,36 @@ __device__ void softmax_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, i
         if (!mbar_wait(&sh.red_sum_bar[hh], (uint32_t)(it & 1), abort)) return;
         const float lsum = (sh.red_sum[0][32 * hh + lane] + sh.red_sum[1][32 * hh + lane]) +
                            (sh.red_sum[2][32 * hh + lane] + sh.red_sum[3][32 * hh + lane]);
+        const float sink2 = cu.sink2;
         const float M = fmaxf(m_run, sink2);
         const float sc = m_run == -INFINITY ? 0.f : exp2f(m_run - M);
         const float fin = sc / (lsum * sc + exp2f(sink2 - M));
-        // lane holds dim d of 32 heads; lanes 2k and 2k+1 trade halves so each
-        // stores a bf16 pair (dims d, d+1) of 16 heads: even lanes the even heads
-        __nv_bfloat16* ob = a.out + (int64_t)u * kH * kD + 32 * hh * kD;
-        const bool odd = lane & 1;
+        // Lane = dim d of 32 heads. The warp stages its 32 heads x 32 dims as bf16
+        // (head i -> row 32qd + i, its 64 bytes -> the units 4hh..4hh+3 of that
+        // row): exactly the bytes of the P buffer this warp writes itself, so no
+        // other warp touches them. Then 16-byte stores of 64-byte row pieces.
+        float fh[32];  // the factor of every head of this half, in every lane
+#pragma unroll
+        for (int i = 0; i < 32; ++i) fh[i] = __shfl_sync(0xffffffffu, fin, i);
+        uint8_t* ob = reinterpret_cast<uint8_t*>(a.out + (int64_t)u * kH * kD + 32 * hh * kD);
 #pragma unroll 1
         for (int mb = 0; mb < 4; ++mb) {
             uint32_t ov[32];
             tmem_ld_32x32b_x32(tl + kColO + 64 * mb + 32 * hh, ov);
-            const int d0 = 128 * mb + 32 * qd + (lane & ~1);
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                const float v0 = __uint_as_float(ov[i]) * __shfl_sync(0xffffffffu, fin, i);
-                const float v1 = __uint_as_float(ov[i + 1]) * __shfl_sync(0xffffffffu, fin, i + 1);
-                // even lane keeps head i and sends head i+1; odd lane the reverse
-                const float mine = odd ? v1 : v0, give = odd ? v0 : v1;
-                const float got = __shfl_xor_sync(0xffffffffu, give, 1);
-                const __nv_bfloat162 pr2 = odd ? __floats2bfloat162_rn(got, mine)
-                                               : __floats2bfloat162_rn(mine, got);
-                *reinterpret_cast<__nv_bfloat162*>(ob + (i + (odd ? 1 : 0)) * kD + d0) = pr2;
+            for (int i = 0; i < 32; ++i)
+                *reinterpret_cast<__nv_bfloat16*>(sh.p + sw128(32 * qd + i, 4 * hh + (lane >> 3)) + 2 * (lane & 7)) =
+                    __float2bfloat16_rn(__uint_as_float(ov[i]) * fh[i]);
+            __syncwarp();
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int q = lane + 32 * c, row = q >> 2, piece = q & 3;
+                const uint4 v = *reinterpret_cast<const uint4*>(sh.p + sw128(32 * qd + row, 4 * hh + piece));
+                *reinterpret_cast<uint4*>(ob + (int64_t)row * kD * 2 + (128 * mb + 32 * qd) * 2 + 16 * piece) = v;
             }
+            __syncwarp();
         }
+        cu = nx;
         tc_fence_before();
     }
 }
