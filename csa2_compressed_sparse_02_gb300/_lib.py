@@ -48,6 +48,7 @@ SIGNATURES = {
     "csa2_sparse_attn_noalloc": (I32, [PP, I32, P, P, P, P, P, P, P, P, P, P]),
     "csa2_sparse_attn_layers": (I32, [PP, I32, I32, P, P, P, P, P, P, P, P, P, P]),
     "csa2_sparse_attn_layers_mma": (I32, [PP, I32, I32, P, P, P, P, P, P, P, P, P, P]),
+    "csa2_sparse_attn_layers_part": (I32, [PP, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P, P]),
 }
 
 

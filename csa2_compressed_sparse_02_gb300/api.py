@@ -132,6 +132,17 @@ def sparse_attn_layers(params, q, sink, win_ptrs, n_tokens, comp_ptrs, comp_scal
         _stream(stream)), "sparse_attn_layers_mma" if mma_sync else "sparse_attn_layers")
 
 
+def sparse_attn_layers_part(params, b0, nb, q, sink, win_ptrs, n_tokens, comp_ptrs, comp_scale_ptrs,
+                            idx, out, dev_status=None, stream=None):
+    """sparse_attn_layers for the sequences [b0, b0 + nb) only; every array keeps
+    its full-batch shape (q/out [L, B, H, D], win_ptrs [L*B], n_tokens [B], ...)."""
+    L, B = q.shape[0], q.shape[1]
+    check(lib().csa2_sparse_attn_layers_part(
+        ctypes.byref(params), L, B, b0, nb, _ptr(q), _ptr(sink), _ptr(win_ptrs), _ptr(n_tokens),
+        _ptr(comp_ptrs), _ptr(comp_scale_ptrs), _ptr(idx), _ptr(out), _ptr(dev_status),
+        _stream(stream)), "sparse_attn_layers_part")
+
+
 def sparse_attn_noalloc(params, q, sink, win_ptrs, n_tokens, comp_ptrs, comp_scale_ptrs, idx, out,
                         dev_status=None, stream=None):
     """csa2_sparse_attn without a workspace: for callers that cannot allocate device

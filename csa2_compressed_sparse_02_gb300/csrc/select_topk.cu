@@ -31,6 +31,7 @@ constexpr int kSample = 2048;
 constexpr int kMaxFiltered = 8192;
 constexpr int kSample2 = 1024;       // level 2 sample (stored at the end of cand_idx)
 constexpr int kMaxFiltered2 = 4096;
+constexpr int kStagePerWarp = 256;   // kept pairs a warp stages during the vector filter's pass
 
 struct SelShared {
     uint32_t hist[256];
@@ -40,6 +41,8 @@ struct SelShared {
     uint32_t cand[kMaxCand];        // level 2 keys; level 1: filtered keys, sample at the end
     int32_t cand_idx[kMaxFiltered];  // index of each filtered key; level 2 sample at the end
     uint32_t cand2[kMaxFiltered2];   // level 2 filtered keys
+    uint32_t stage_key[kWarps * kStagePerWarp];  // level 1 filter: kept pairs per warp, in order
+    int32_t stage_idx[kWarps * kStagePerWarp];
 };
 
 __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
@@ -228,6 +231,88 @@ __device__ int filter_ge(int n, uint32_t thr, KeyAt key_at, uint32_t* keys_out, 
     return (int)total;
 }
 
+// filter_ge over n block maxima read straight from global memory, for a
+// 16-byte aligned row. One pass of 16-byte loads (8 in flight per thread):
+// every warp walks its own contiguous range of 128-element chunks (lane l
+// covers elements 4l..4l+3 of a chunk) and stages its kept (key, index) pairs,
+// in index order, in its own slot of kStagePerWarp; a prefix over the warps'
+// counts then places every slot. Returns -1 when a slot overflowed (the caller
+// then uses filter_ge), else the count (which may exceed cap: then nothing was
+// written).
+__device__ int filter_ge_vec(int n, uint32_t thr, const float* __restrict__ bm, uint32_t* keys_out,
+                             int32_t* idx_out, int cap, SelShared& sh) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int chunks = (n + 127) / 128;
+    const int R = (chunks + kWarps - 1) / kWarps;
+    const int c0 = min(chunks, warp * R), c1 = min(chunks, c0 + R);
+    uint32_t* skey = sh.stage_key + warp * kStagePerWarp;
+    int32_t* sidx = sh.stage_idx + warp * kStagePerWarp;
+    // the value whose key is thr: key >= thr <=> value >= thr_f (keys are monotone)
+    const uint32_t tb = (thr & 0x80000000u) ? (thr & 0x7fffffffu) : ~thr;
+    const float thr_f = __uint_as_float(tb);
+    constexpr int U = 8;
+    uint32_t cnt = 0;
+    for (int cb = c0; cb < c1; cb += U) {
+        float4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = 128 * (cb + u) + 4 * lane;
+            if (cb + u < c1 && e + 3 < n) {
+                v[u] = __ldg(reinterpret_cast<const float4*>(bm + e));
+            } else {
+                v[u].x = (cb + u < c1 && e < n) ? bm[e] : -INFINITY;
+                v[u].y = (cb + u < c1 && e + 1 < n) ? bm[e + 1] : -INFINITY;
+                v[u].z = (cb + u < c1 && e + 2 < n) ? bm[e + 2] : -INFINITY;
+                v[u].w = -INFINITY;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e = 128 * (cb + u) + 4 * lane;
+            const int left = (cb + u < c1) ? n - e : 0;  // elements of this lane's four inside n
+            const uint32_t valid = left >= 4 ? 15u : (left > 0 ? (1u << left) - 1u : 0u);
+            const uint32_t m4 = valid & ((uint32_t)(v[u].x >= thr_f) | ((uint32_t)(v[u].y >= thr_f) << 1) |
+                                         ((uint32_t)(v[u].z >= thr_f) << 2) | ((uint32_t)(v[u].w >= thr_f) << 3));
+            const uint32_t c = __popc(m4);
+            uint32_t incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += t;
+            }
+            uint32_t at = cnt + incl - c;
+            if (m4) {
+                const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if ((m4 >> q) & 1u) {
+                        if (at < (uint32_t)kStagePerWarp) {
+                            skey[at] = score_key(f[q]);
+                            sidx[at] = e + q;
+                        }
+                        ++at;
+                    }
+                }
+            }
+            cnt += __shfl_sync(0xffffffffu, incl, 31);
+        }
+    }
+    uint32_t total;
+    const uint32_t o = warp_excl_scan(cnt, sh, &total);  // (its barriers also publish the stages)
+    sh.bcast[2] = 0;
+    __syncthreads();
+    if (cnt > (uint32_t)kStagePerWarp && lane == 0) sh.bcast[2] = 1;
+    __syncthreads();
+    if (sh.bcast[2]) return -1;
+    if ((int)total > cap) return (int)total;
+    for (uint32_t i = lane; i < cnt; i += 32) {
+        keys_out[o + i] = skey[i];
+        idx_out[o + i] = sidx[i];
+    }
+    __syncthreads();
+    return (int)total;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 k_select_topk(int64_t max_ncomp, int ratio, const float* __restrict__ scores,
               const float* __restrict__ block_max, const int32_t* __restrict__ n_tokens,
@@ -255,6 +340,7 @@ k_select_topk(int64_t max_ncomp, int ratio, const float* __restrict__ scores,
     } else {
         // best K_b - 1 among blocks [0, n_b - 1), then the newest block n_b - 1
         const int n1 = n_b - 1, K1 = kKb - 1;
+        const bool vec_ok = (reinterpret_cast<uintptr_t>(bm) & 15u) == 0;
         // (a) threshold from a strided sample: the r-th largest sample key, r chosen so
         //     that about 1.5 K1 blocks of all n1 reach it
         for (int i = tid; i < kSample; i += kThreads)
@@ -268,9 +354,11 @@ k_select_topk(int64_t max_ncomp, int ratio, const float* __restrict__ scores,
             // the top 16 bits of the r-th largest sample key: a slightly lower threshold
             const uint32_t thr = radix_kth(kSample, r, [&](int i) { return sh.cand[kMaxCand - kSample + i]; },
                                            sh, &unused, 2);
-            const int total = filter_ge(
-                n1, thr, [&](int i) { return score_key(bm[i]); }, sh.cand, sh.cand_idx,
-                kMaxFiltered, sh);
+            int total = vec_ok ? filter_ge_vec(n1, thr, bm, sh.cand, sh.cand_idx, kMaxFiltered, sh) : -1;
+            if (total < 0)
+                total = filter_ge(
+                    n1, thr, [&](int i) { return score_key(bm[i]); }, sh.cand, sh.cand_idx,
+                    kMaxFiltered, sh);
             if (total < K1) {          // threshold too high: take a lower sample rank
                 r = r * 2 + 8;
                 continue;
@@ -299,8 +387,23 @@ k_select_topk(int64_t max_ncomp, int ratio, const float* __restrict__ scores,
     // ---- level 2: positions of the kept blocks ----
     // the last kept block is block n_b - 1, the only one that may be partial
     const int n_cand = n_kept == 0 ? 0 : (n_kept - 1) * kBlk + (n_c - (n_b - 1) * kBlk);
-    for (int i = tid; i < n_cand; i += kThreads)
-        sh.cand[i] = score_key(sc[sh.kept[i / kBlk] * kBlk + (i % kBlk)]);
+    if ((reinterpret_cast<uintptr_t>(sc) & 15u) == 0) {
+        // blocks are 8 consecutive scores (32 bytes): two 16-byte loads per block
+        for (int q = tid; q < 2 * n_kept; q += kThreads) {
+            const int i = 4 * q;  // candidate index of the load's first score
+            const int64_t pos = (int64_t)sh.kept[i / kBlk] * kBlk + (i % kBlk);
+            if (i + 3 < n_cand) {
+                const float4 v = __ldg(reinterpret_cast<const float4*>(sc + pos));
+                *reinterpret_cast<uint4*>(&sh.cand[i]) =
+                    make_uint4(score_key(v.x), score_key(v.y), score_key(v.z), score_key(v.w));
+            } else {
+                for (int c = 0; c < 4 && i + c < n_cand; ++c) sh.cand[i + c] = score_key(sc[pos + c]);
+            }
+        }
+    } else {
+        for (int i = tid; i < n_cand; i += kThreads)
+            sh.cand[i] = score_key(sc[sh.kept[i / kBlk] * kBlk + (i % kBlk)]);
+    }
     for (int i = tid; i < kKp; i += kThreads) out[i] = -1;
     __syncthreads();
     auto pos_of = [&](int i) { return sh.kept[i / kBlk] * kBlk + i % kBlk; };

@@ -138,6 +138,7 @@ __device__ __forceinline__ float warp_max(float v) {
 
 struct UnitArgs {
     int L, B, ratio, win_linear;
+    int b0, nb;  // the sequences [b0, b0 + nb) of the batch of B are processed; units = L * nb
     float scale_log2;
     const __nv_bfloat16* q;
     const float* sink;
@@ -150,8 +151,21 @@ struct UnitArgs {
     int32_t* dev_status;
 };
 
-__device__ __forceinline__ bool unit_aligned(const UnitArgs& a, int u, int b) {
-    const uintptr_t w = reinterpret_cast<uintptr_t>(a.win[u]);
+// Unit u of a launch -> layer l, sequence b and the flat index l * B + b of the
+// layer-major q / out / window arrays.
+struct UnitIdx {
+    int l, b, f;
+};
+__device__ __forceinline__ UnitIdx unit_idx(const UnitArgs& a, int u) {
+    UnitIdx x;
+    x.l = u / a.nb;
+    x.b = a.b0 + u % a.nb;
+    x.f = x.l * a.B + x.b;
+    return x;
+}
+
+__device__ __forceinline__ bool unit_aligned(const UnitArgs& a, int f, int b) {
+    const uintptr_t w = reinterpret_cast<uintptr_t>(a.win[f]);
     const uintptr_t c = reinterpret_cast<uintptr_t>(a.comp[b]);
     const uintptr_t s = reinterpret_cast<uintptr_t>(a.comp_scales[b]);
     return ((w | c) & 15u) == 0 && (s & 3u) == 0;
@@ -163,13 +177,14 @@ __device__ __forceinline__ bool unit_aligned(const UnitArgs& a, int u, int b) {
 __device__ void producer_role(AttnShared& sh, const UnitArgs& a, int pt, int lane,
                               volatile int* abort) {
     const int pw = pt >> 5, r = pt >> 1, hf = pt & 1;
-    const int n_units = a.L * a.B;
+    const int n_units = a.L * a.nb;
     int it = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
-        const int b = u % a.B;
+        const UnitIdx ui = unit_idx(a, u);
+        const int b = ui.b;
         const int64_t T = a.n_tokens[b];
         const int64_t n_c = T > 0 ? T / a.ratio : 0;
-        const bool aligned = unit_aligned(a, u, b);
+        const bool aligned = unit_aligned(a, ui.f, b);
         if (!aligned && pt == 0) raise_status(a.dev_status, CSA2_DEV_BAD_ALIGN);
 
         // selected positions of this thread's row in tiles 1..4
@@ -179,7 +194,7 @@ __device__ void producer_role(AttnShared& sh, const UnitArgs& a, int pt, int lan
 
         // ---- query: warp pw stages heads 8pw..8pw+7, lane = dims 16*lane..+15
         {
-            const uint4* qu = reinterpret_cast<const uint4*>(a.q + (int64_t)u * kH * kD);
+            const uint4* qu = reinterpret_cast<const uint4*>(a.q + (int64_t)ui.f * kH * kD);
             uint4 qa[4], qb[4];
 #pragma unroll
             for (int hi = 0; hi < 4; ++hi) {
@@ -228,7 +243,7 @@ __device__ void producer_role(AttnShared& sh, const UnitArgs& a, int pt, int lan
         if (lane == 0) mbar_arrive(&sh.q_full);
 
         // ---- the 5 tiles
-        const uint8_t* winb = static_cast<const uint8_t*>(a.win[u]);
+        const uint8_t* winb = static_cast<const uint8_t*>(a.win[ui.f]);
         const uint8_t* compb = static_cast<const uint8_t*>(a.comp[b]);
         const uint8_t* compsb = a.comp_scales[b];
         for (int j = 0; j < kTiles; ++j) {
@@ -314,7 +329,7 @@ __device__ void mma_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, volat
     const uint64_t dQ = smem_desc(smem_u32(sh.q[0]), 16, 1024, kLayoutSw128);
     const uint64_t dV = smem_desc(smem_u32(sh.kv[0]), kKVChunk, 1024, kLayoutSw128);
     const uint64_t dP = smem_desc(smem_u32(sh.p), 1024, 1024, kLayoutSw128);
-    const int n_units = a.L * a.B;
+    const int n_units = a.L * a.nb;
     int it = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
         if (!mbar_wait(&sh.q_full, (uint32_t)(it & 1), abort)) return;
@@ -361,10 +376,11 @@ struct SoftUnit {
     float sink2;     // sink logit of head 32hh + lane, log2 domain
     int32_t xs[4];   // this row's selected positions in tiles 1..4
     __device__ __forceinline__ void load(const UnitArgs& a, int u, int r, int hh, int lane) {
-        const int l = u / a.B, b = u % a.B;
+        const UnitIdx ui = unit_idx(a, u);
+        const int l = ui.l, b = ui.b;
         T = a.n_tokens[b];
         n_c = T > 0 ? T / a.ratio : 0;
-        aligned = unit_aligned(a, u, b);
+        aligned = unit_aligned(a, ui.f, b);
         sink2 = a.sink[(int64_t)l * kH + 32 * hh + lane] * kLog2e;
 #pragma unroll
         for (int j = 0; j < 4; ++j) xs[j] = a.idx[(int64_t)b * kKp + 128 * j + r];
@@ -376,7 +392,7 @@ __device__ void softmax_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, i
     const int qd = warp & 3, hh = warp >> 2;
     const int r = 32 * qd + lane;                   // position row of the tile
     const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);  // this warp's TMEM lane quarter
-    const int n_units = a.L * a.B;
+    const int n_units = a.L * a.nb;
     SoftUnit cu, nx;
     if ((int)blockIdx.x < n_units) cu.load(a, blockIdx.x, r, hh, lane);
     int it = 0;
@@ -489,10 +505,7 @@ __device__ void softmax_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, i
         // (head i -> row 32qd + i, its 64 bytes -> the units 4hh..4hh+3 of that
         // row): exactly the bytes of the P buffer this warp writes itself, so no
         // other warp touches them. Then 16-byte stores of 64-byte row pieces.
-        float fh[32];  // the factor of every head of this half, in every lane
-#pragma unroll
-        for (int i = 0; i < 32; ++i) fh[i] = __shfl_sync(0xffffffffu, fin, i);
-        uint8_t* ob = reinterpret_cast<uint8_t*>(a.out + (int64_t)u * kH * kD + 32 * hh * kD);
+        uint8_t* ob = reinterpret_cast<uint8_t*>(a.out + (int64_t)unit_idx(a, u).f * kH * kD + 32 * hh * kD);
 #pragma unroll 1
         for (int mb = 0; mb < 4; ++mb) {
             uint32_t ov[32];
@@ -500,7 +513,7 @@ __device__ void softmax_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, i
 #pragma unroll
             for (int i = 0; i < 32; ++i)
                 *reinterpret_cast<__nv_bfloat16*>(sh.p + sw128(32 * qd + i, 4 * hh + (lane >> 3)) + 2 * (lane & 7)) =
-                    __float2bfloat16_rn(__uint_as_float(ov[i]) * fh[i]);
+                    __float2bfloat16_rn(__uint_as_float(ov[i]) * __shfl_sync(0xffffffffu, fin, i));
             __syncwarp();
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -584,14 +597,16 @@ int sm_count(int dev) {
 
 using namespace csa2;
 
-extern "C" int csa2_sparse_attn_layers(const csa2_params* p, int L, int B, const void* q,
+extern "C" int csa2_sparse_attn_layers_part(const csa2_params* p, int L, int B, int b0, int nb,
+                                            const void* q,
                                        const float* sink, const void* const* win,
                                        const int32_t* n_tokens, const void* const* comp,
                                        const uint8_t* const* comp_scales, const int32_t* idx,
                                        void* out, int32_t* dev_status, void* stream) {
     CSA2_CHECK_PARAMS(p);
-    if (L < 0 || B < 0) return fail(CSA2_ERR_INVALID_ARG, "sparse_attn_layers: negative size");
-    if (L == 0 || B == 0) return CSA2_OK;
+    if (L < 0 || B < 0 || b0 < 0 || nb < 0 || b0 + nb > B)
+        return fail(CSA2_ERR_INVALID_ARG, "sparse_attn_layers: bad size or sequence range");
+    if (L == 0 || nb == 0) return CSA2_OK;
     if (p->heads != kH || p->head_dim != kD || p->window != kW || p->topk_pos != kKp ||
         p->compress_ratio < 1)
         return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn_layers: built for 64 heads x 512, W=128, k=512");
@@ -619,6 +634,8 @@ extern "C" int csa2_sparse_attn_layers(const csa2_params* p, int L, int B, const
     UnitArgs a;
     a.L = L;
     a.B = B;
+    a.b0 = b0;
+    a.nb = nb;
     a.ratio = p->compress_ratio;
     a.win_linear = p->win_layout == CSA2_WIN_LINEAR;
     a.scale_log2 = p->softmax_scale * kLog2e;
@@ -631,10 +648,19 @@ extern "C" int csa2_sparse_attn_layers(const csa2_params* p, int L, int B, const
     a.idx = idx;
     a.out = static_cast<__nv_bfloat16*>(out);
     a.dev_status = dev_status;
-    const int64_t units = (int64_t)L * B;
+    const int64_t units = (int64_t)L * nb;
     int64_t sms = sm_count(dev);
     if (p->max_ctas > 0 && p->max_ctas < sms) sms = p->max_ctas;
     const int grid = (int)(units < sms ? units : sms);
     k_sparse_attn_tc<<<grid, kAttnThreads, kAttnSmem, static_cast<cudaStream_t>(stream)>>>(a);
     return check_launch("sparse_attn_layers");
+}
+
+extern "C" int csa2_sparse_attn_layers(const csa2_params* p, int L, int B, const void* q,
+                                       const float* sink, const void* const* win,
+                                       const int32_t* n_tokens, const void* const* comp,
+                                       const uint8_t* const* comp_scales, const int32_t* idx,
+                                       void* out, int32_t* dev_status, void* stream) {
+    return csa2_sparse_attn_layers_part(p, L, B, 0, B, q, sink, win, n_tokens, comp, comp_scales,
+                                        idx, out, dev_status, stream);
 }

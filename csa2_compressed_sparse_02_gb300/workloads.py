@@ -47,7 +47,8 @@ class DecodeRun:
         self.comp_caps = [t // 2 + 1 for t in last]
         self.n_c_max = max(t // 2 for t in last)
         self.key_rows = [max(1, t // 2) for t in last]
-        self.max_ncomp = self.n_c_max
+        # rows of the score and block-max arrays 16-byte aligned: vector loads in the selection
+        self.max_ncomp = -(-self.n_c_max // 32) * 32
         self.n_b_max = math.ceil(self.max_ncomp / 8)
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
         ws = api.sparse_attn_workspace_size(self.params, self.B)

@@ -309,6 +309,21 @@ int csa2_sparse_attn_layers(const csa2_params* p, int L, int B,
                             int32_t* dev_status, void* stream);
 
 /*
+ * csa2_sparse_attn_layers_part — csa2_sparse_attn_layers restricted to the
+ * sequences [b0, b0 + nb) of the batch of B: all arrays keep their full-batch
+ * shapes and layouts (q/out [L, B, H, D], win [L*B], n_tokens/comp/
+ * comp_scales [B], idx [B, topk_pos]) and only the rows of those sequences are
+ * read or written. Lets a caller pipeline micro-batches of one decode step.
+ * Requires 0 <= b0, 0 <= nb, b0 + nb <= B.
+ */
+int csa2_sparse_attn_layers_part(const csa2_params* p, int L, int B, int b0, int nb,
+                                 const void* q, const float* sink,
+                                 const void* const* win, const int32_t* n_tokens,
+                                 const void* const* comp, const uint8_t* const* comp_scales,
+                                 const int32_t* idx, void* out,
+                                 int32_t* dev_status, void* stream);
+
+/*
  * csa2_sparse_attn_layers_mma — the same contract as csa2_sparse_attn_layers on
  * the legacy warp-level tensor-core path (mma.sync bf16, P rounded to bf16),
  * one CTA per (layer, sequence) with the output accumulator in registers.

@@ -62,5 +62,9 @@ def test_host_side_rejections_without_launching(L):
     assert L.csa2_select_topk(ctypes.byref(bad), 1, 10, *([None] * 7)) == 4
     assert L.csa2_sparse_attn(pp, 1, *([None] * 8), None, 0, None, None) == 1
     assert L.csa2_nvfp4_quantize(None, 4, 24, None, None, None) == 2  # row_len % 16
+    assert L.csa2_sparse_attn_layers(pp, 2, 4, *([None] * 10)) == 1  # NULL buffers
+    assert L.csa2_sparse_attn_layers_part(pp, 2, 4, 3, 2, *([None] * 10)) == 1  # range past B
+    assert L.csa2_sparse_attn_layers_part(pp, 2, 4, -1, 1, *([None] * 10)) == 1
+    assert L.csa2_sparse_attn_layers_part(pp, 2, 4, 1, 0, *([None] * 10)) == 0  # empty range
     # nothing to do is not an error
     assert L.csa2_compress_append(pp, 0, 1, *([None] * 11)) == 0

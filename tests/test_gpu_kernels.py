@@ -260,11 +260,13 @@ def test_index_scores_clip_and_status_when_length_exceeds_max():
 
 
 # --------------------------------------------------------------------------- selection
-@pytest.mark.parametrize("levels", [3, 50, 0])
-def test_select_topk_exact_with_ties(levels):
+@pytest.mark.parametrize("levels,pad", [(3, 0), (50, 0), (0, 0), (0, 4)])
+def test_select_topk_exact_with_ties(levels, pad):
+    """pad = 0: every row 16-byte aligned (vector loads where a sequence has at most
+    65,536 blocks); pad = 4: odd rows misaligned (scalar loads)."""
     rng = np.random.default_rng(levels + 5)
-    n_cs = [0, 1, 5, 511, 512, 513, 4095, 16384, 16385, 20000, 70001, 524288]
-    B, max_nc = len(n_cs), max(n_cs)
+    n_cs = [0, 1, 5, 511, 512, 513, 4095, 16384, 16385, 20000, 70001, 524288, 600000]
+    B, max_nc = len(n_cs), max(n_cs) + pad
     scores = np.zeros((B, max_nc), np.float32)
     for b, n in enumerate(n_cs):
         if levels:
