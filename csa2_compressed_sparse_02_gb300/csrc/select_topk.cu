@@ -252,50 +252,59 @@ __device__ int filter_ge_vec(int n, uint32_t thr, const float* __restrict__ bm, 
     const float thr_f = __uint_as_float(tb);
     constexpr int U = 8;
     uint32_t cnt = 0;
-    for (int cb = c0; cb < c1; cb += U) {
-        float4 v[U];
+    // one chunk's four values of this lane -> kept flags, staged pairs, count
+    auto chunk = [&](int cbu, float4 v) {
+        const int e = 128 * cbu + 4 * lane;
+        const int left = n - e;  // elements of this lane's four inside n
+        const uint32_t valid = left >= 4 ? 15u : (left > 0 ? (1u << left) - 1u : 0u);
+        const uint32_t m4 = valid & ((uint32_t)(v.x >= thr_f) | ((uint32_t)(v.y >= thr_f) << 1) |
+                                     ((uint32_t)(v.z >= thr_f) << 2) | ((uint32_t)(v.w >= thr_f) << 3));
+        const uint32_t c = __popc(m4);
+        uint32_t incl = c;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int e = 128 * (cb + u) + 4 * lane;
-            if (cb + u < c1 && e + 3 < n) {
-                v[u] = __ldg(reinterpret_cast<const float4*>(bm + e));
-            } else {
-                v[u].x = (cb + u < c1 && e < n) ? bm[e] : -INFINITY;
-                v[u].y = (cb + u < c1 && e + 1 < n) ? bm[e + 1] : -INFINITY;
-                v[u].z = (cb + u < c1 && e + 2 < n) ? bm[e + 2] : -INFINITY;
-                v[u].w = -INFINITY;
-            }
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += t;
         }
+        uint32_t at = cnt + incl - c;
+        if (m4) {
+            const float f[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int e = 128 * (cb + u) + 4 * lane;
-            const int left = (cb + u < c1) ? n - e : 0;  // elements of this lane's four inside n
-            const uint32_t valid = left >= 4 ? 15u : (left > 0 ? (1u << left) - 1u : 0u);
-            const uint32_t m4 = valid & ((uint32_t)(v[u].x >= thr_f) | ((uint32_t)(v[u].y >= thr_f) << 1) |
-                                         ((uint32_t)(v[u].z >= thr_f) << 2) | ((uint32_t)(v[u].w >= thr_f) << 3));
-            const uint32_t c = __popc(m4);
-            uint32_t incl = c;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += t;
-            }
-            uint32_t at = cnt + incl - c;
-            if (m4) {
-                const float f[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    if ((m4 >> q) & 1u) {
-                        if (at < (uint32_t)kStagePerWarp) {
-                            skey[at] = score_key(f[q]);
-                            sidx[at] = e + q;
-                        }
-                        ++at;
+            for (int q = 0; q < 4; ++q) {
+                if ((m4 >> q) & 1u) {
+                    if (at < (uint32_t)kStagePerWarp) {
+                        skey[at] = score_key(f[q]);
+                        sidx[at] = e + q;
                     }
+                    ++at;
                 }
             }
-            cnt += __shfl_sync(0xffffffffu, incl, 31);
         }
+        cnt += __shfl_sync(0xffffffffu, incl, 31);
+    };
+    // whole batches of U chunks inside n: the loads carry no condition
+    const int c_full = min(c1, n / 128);  // chunks entirely inside n
+    int cb = c0;
+    for (; cb + U <= c_full; cb += U) {
+        float4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            v[u] = __ldg(reinterpret_cast<const float4*>(bm + 128 * (cb + u) + 4 * lane));
+#pragma unroll
+        for (int u = 0; u < U; ++u) chunk(cb + u, v[u]);
+    }
+    for (; cb < c1; ++cb) {  // the rest, one chunk at a time, loads guarded
+        const int e = 128 * cb + 4 * lane;
+        float4 v;
+        if (e + 3 < n) {
+            v = __ldg(reinterpret_cast<const float4*>(bm + e));
+        } else {
+            v.x = e < n ? bm[e] : -INFINITY;
+            v.y = e + 1 < n ? bm[e + 1] : -INFINITY;
+            v.z = e + 2 < n ? bm[e + 2] : -INFINITY;
+            v.w = -INFINITY;
+        }
+        chunk(cb, v);
     }
     uint32_t total;
     const uint32_t o = warp_excl_scan(cnt, sh, &total);  // (its barriers also publish the stages)
