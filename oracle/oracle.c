@@ -114,6 +114,15 @@ int64_t orc_compress_append(int64_t T, int n_new, int D, int W,
                             float* pend_kv, float* pend_g,
                             uint8_t* comp_vals, uint8_t* comp_scales, float* comp_f32,
                             uint8_t* win_u8, float* win_f32) {
+    return orc_compress_append_ratio(T, n_new, D, W, 2, kv_new, g_new, pend_kv, pend_g,
+                                     comp_vals, comp_scales, comp_f32, win_u8, win_f32);
+}
+
+int64_t orc_compress_append_ratio(int64_t T, int n_new, int D, int W, int ratio,
+                                  const float* kv_new, const float* g_new,
+                                  float* pend_kv, float* pend_g,
+                                  uint8_t* comp_vals, uint8_t* comp_scales, float* comp_f32,
+                                  uint8_t* win_u8, float* win_f32) {
     int has_comp = (comp_vals != NULL) || (comp_f32 != NULL);
     float* row = (float*)malloc(sizeof(float) * (size_t)D);
     for (int i = 0; i < n_new; ++i) {
@@ -126,6 +135,13 @@ int64_t orc_compress_append(int64_t T, int n_new, int D, int W,
         if (win_f32)
             for (int d = 0; d < D; ++d) win_f32[slot * D + d] = kv[d];
         if (!has_comp) continue;
+        if (ratio == 1) { /* 1:1 layer: pooling skipped, raw token p is compressed row p */
+            if (comp_f32)
+                memcpy(comp_f32 + p * D, kv, sizeof(float) * (size_t)D);
+            else
+                orc_nvfp4_quantize(kv, D / 16, comp_vals + p * (D / 2), comp_scales + p * (D / 16));
+            continue;
+        }
         if ((p & 1) == 0) { /* first token of a pair: wait for its partner */
             memcpy(pend_kv, kv, sizeof(float) * (size_t)D);
             memcpy(pend_g, g, sizeof(float) * (size_t)D);

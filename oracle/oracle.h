@@ -74,6 +74,16 @@ int64_t orc_compress_append(int64_t T, int n_new, int D, int W,
                             uint8_t* comp_vals, uint8_t* comp_scales, float* comp_f32,
                             uint8_t* win_u8, float* win_f32);
 
+/* The same for a layer of compression ratio 1 or 2. Ratio 1 (the uncompressed
+ * 1:1 layers, [CFG] §2.2, [NVFP4] §3.2): pooling is skipped, raw token p is
+ * quantized (or copied, fp32) into compressed row p; gate and pending state are
+ * unused. Ratio 2 is orc_compress_append. */
+int64_t orc_compress_append_ratio(int64_t T, int n_new, int D, int W, int ratio,
+                                  const float* kv_new, const float* g_new,
+                                  float* pend_kv, float* pend_g,
+                                  uint8_t* comp_vals, uint8_t* comp_scales, float* comp_f32,
+                                  uint8_t* win_u8, float* win_f32);
+
 /* ---- Indexer ([NVFP4] §3.3, [CFG] §2.1) ---- */
 /*
  * s_t = sum_h w[h] * ReLU( sum_d q[h,d] * k[t,d] ),  t < n_c, fp64.

@@ -67,6 +67,10 @@ def lib():
             L.orc_compress_append.argtypes = [
                 ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, _f32p, _f32p,
                 _f32p, _f32p, _u8p, _u8p, _f32p, _u8p, _f32p]
+            L.orc_compress_append_ratio.restype = ctypes.c_int64
+            L.orc_compress_append_ratio.argtypes = [
+                ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _f32p,
+                _f32p, _f32p, _f32p, _u8p, _u8p, _f32p, _u8p, _f32p]
             L.orc_index_scores.restype = ctypes.c_int64
             L.orc_index_scores.argtypes = [
                 ctypes.c_int, ctypes.c_int, _u8p, _u8p, _f32p, ctypes.c_int64, _u8p, _u8p, _f32p]
@@ -148,8 +152,11 @@ class SeqState:
     """One sequence's cache for one layer, as the oracle keeps it (host arrays)."""
 
     def __init__(self, cap_comp: int, D: int = 512, W: int = 128,
-                 comp_f32: bool = False, win_f32: bool = False, has_comp: bool = True):
-        self.D, self.W, self.T = D, W, 0
+                 comp_f32: bool = False, win_f32: bool = False, has_comp: bool = True,
+                 ratio: int = 2):
+        """ratio 2: the 2:1 pooled layers; ratio 1: the 1:1 layers (pooling skipped)."""
+        assert ratio in (1, 2)
+        self.D, self.W, self.T, self.ratio = D, W, 0, ratio
         self.pend_kv = np.zeros(D, np.float32)
         self.pend_g = np.zeros(D, np.float32)
         self.comp_f32 = np.zeros((cap_comp, D), np.float32) if (has_comp and comp_f32) else None
@@ -164,15 +171,15 @@ class SeqState:
         kv = np.ascontiguousarray(kv, dtype=np.float32).reshape(-1, self.D)
         if g is not None:
             g = np.ascontiguousarray(g, dtype=np.float32).reshape(-1, self.D)
-        self.T = lib().orc_compress_append(
-            self.T, kv.shape[0], self.D, self.W, _p(kv, _f32p), _p(g, _f32p),
+        self.T = lib().orc_compress_append_ratio(
+            self.T, kv.shape[0], self.D, self.W, self.ratio, _p(kv, _f32p), _p(g, _f32p),
             _p(self.pend_kv, _f32p), _p(self.pend_g, _f32p), _p(self.comp_vals, _u8p),
             _p(self.comp_scales, _u8p), _p(self.comp_f32, _f32p), _p(self.win_u8, _u8p),
             _p(self.win_f32, _f32p))
 
     @property
     def n_comp(self) -> int:
-        return self.T // 2
+        return self.T // self.ratio
 
 
 # --------------------------------------------------------------------------- indexer

@@ -85,3 +85,47 @@ def test_window_only_layer_keeps_no_compressed_state():
     kv = np.ones((5, 32), np.float32)
     s.append(kv, None)
     assert s.T == 5 and s.comp_vals is None and s.win_u8.any()
+
+
+# --------------------------------------------------------------------------- 1:1 layers
+def test_ratio_one_rows_are_the_quantised_raw_tokens():
+    """1:1 layers ("CSA2稀疏注意力、384专家MoE与1M上下文" §2.2, "DeepSeek-V4.1-Flash-NVFP4"
+    §3.2): no pooling, so compressed row p is the NVFP4 encoding of raw token p, and
+    there are T compressed positions (not T/2). Checked against the quantiser, which
+    is pinned on its own (test_oracle_codecs)."""
+    rng = np.random.default_rng(11)
+    kv = (rng.standard_normal((37, 32)) * rng.choice([1e-3, 1, 50], (37, 1))).astype(np.float32)
+    st = orc.SeqState(cap_comp=64, D=32, W=8, ratio=1)
+    for a, b in [(0, 1), (1, 6), (6, 7), (7, 37)]:  # odd and even chunk boundaries
+        st.append(kv[a:b], None)
+    assert st.T == 37 and st.n_comp == 37
+    v, s = orc.nvfp4_quantize(kv)
+    assert np.array_equal(st.comp_vals[:37], v) and np.array_equal(st.comp_scales[:37], s)
+    assert not st.comp_vals[37:].any()
+
+
+def test_ratio_one_fp32_rows_and_window_match_the_raw_tokens():
+    rng = np.random.default_rng(12)
+    kv = rng.standard_normal((21, 32)).astype(np.float32)
+    st = orc.SeqState(cap_comp=32, D=32, W=8, ratio=1, comp_f32=True, win_f32=True)
+    st.append(kv, None)
+    assert np.array_equal(st.comp_f32[:21], kv)
+    for p in range(21 - 8, 21):  # ring slot p mod W holds the newest token with that slot
+        assert np.array_equal(st.win_f32[p % 8], kv[p])
+
+
+def test_ratio_two_is_unchanged_by_the_ratio_argument():
+    rng = np.random.default_rng(13)
+    kv = rng.standard_normal((19, 32)).astype(np.float32)
+    g = rng.standard_normal((19, 32)).astype(np.float32)
+    a = orc.SeqState(cap_comp=16, D=32, W=8)
+    b = orc.SeqState(cap_comp=16, D=32, W=8, ratio=2)
+    a.append(kv, g)
+    b.append(kv[:4], g[:4])
+    b.append(kv[4:], g[4:])
+    assert a.n_comp == 9 == b.n_comp
+    assert np.array_equal(a.comp_vals, b.comp_vals) and np.array_equal(a.comp_scales, b.comp_scales)
+    # row j is the pooled pair (2j, 2j+1): pin one against the pooling definition
+    row = np.array([orc.pool(kv[6, d], kv[7, d], g[6, d], g[7, d]) for d in range(32)], np.float32)
+    v, s = orc.nvfp4_quantize(row[None])
+    assert np.array_equal(a.comp_vals[3], v[0]) and np.array_equal(a.comp_scales[3], s[0])
