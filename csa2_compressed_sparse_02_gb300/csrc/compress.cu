@@ -47,7 +47,9 @@ __device__ __forceinline__ uint32_t e4m3x4(float4 v) {
     return lo | (hi << 16);
 }
 
-template <bool kNvfp4, bool kWinE4M3>
+// kRatio 2: the 2:1 layers (pairs pooled); kRatio 1: the 1:1 layers, where
+// pooling is skipped and raw token p is written as compressed row p.
+template <int kRatio, bool kNvfp4, bool kWinE4M3>
 __global__ void __launch_bounds__(kThreads)
 k_compress_append(int n_new, const float* __restrict__ kv_new, const float* __restrict__ gate_new,
                   float* pend_kv, float* pend_gate, void* const* comp,
@@ -68,26 +70,32 @@ k_compress_append(int n_new, const float* __restrict__ kv_new, const float* __re
 
     if (has_comp) {
         const int64_t cap = comp_cap[b];
-        // pairs (2j, 2j+1) completed by this call: j in [T/2, (T+n_new)/2)
-        const int64_t j_lo = T >> 1, j_hi = (T + n_new) >> 1;
+        // rows completed by this call: pairs (2j, 2j+1) with j in [T/2, (T+n_new)/2),
+        // or (ratio 1) the raw tokens j in [T, T+n_new)
+        const int64_t j_lo = kRatio == 2 ? T >> 1 : T;
+        const int64_t j_hi = kRatio == 2 ? (T + n_new) >> 1 : T + n_new;
         const int64_t j0 = j_lo + (int64_t)c * kPairsPerCta;
         const int64_t j1 = min(j_hi, j0 + kPairsPerCta);
         for (int64_t j = j0; j < j1; ++j) {
-            const int64_t t0 = 2 * j - T, t1 = t0 + 1;  // rows of kv_new; t0 = -1: pending
-            float4 k0, g0;
-            if (t0 < 0) {
-                k0 = ld4(pk + ch);
-                g0 = ld4(pg + ch);
-            } else {
-                k0 = ld4(kvb + t0 * kD + ch);
-                g0 = ld4(gb + t0 * kD + ch);
-            }
-            const float4 k1 = ld4(kvb + t1 * kD + ch), g1 = ld4(gb + t1 * kD + ch);
             float4 v;
-            v.x = pool1(k0.x, k1.x, g0.x, g1.x);
-            v.y = pool1(k0.y, k1.y, g0.y, g1.y);
-            v.z = pool1(k0.z, k1.z, g0.z, g1.z);
-            v.w = pool1(k0.w, k1.w, g0.w, g1.w);
+            if constexpr (kRatio == 1) {
+                v = ld4(kvb + (j - T) * kD + ch);
+            } else {
+                const int64_t t0 = 2 * j - T, t1 = t0 + 1;  // rows of kv_new; t0 = -1: pending
+                float4 k0, g0;
+                if (t0 < 0) {
+                    k0 = ld4(pk + ch);
+                    g0 = ld4(pg + ch);
+                } else {
+                    k0 = ld4(kvb + t0 * kD + ch);
+                    g0 = ld4(gb + t0 * kD + ch);
+                }
+                const float4 k1 = ld4(kvb + t1 * kD + ch), g1 = ld4(gb + t1 * kD + ch);
+                v.x = pool1(k0.x, k1.x, g0.x, g1.x);
+                v.y = pool1(k0.y, k1.y, g0.y, g1.y);
+                v.z = pool1(k0.z, k1.z, g0.z, g1.z);
+                v.w = pool1(k0.w, k1.w, g0.w, g1.w);
+            }
             if (j >= cap) {
                 if (tid == 0) raise_status(dev_status, CSA2_DEV_BAD_LENGTH);
                 continue;
@@ -114,7 +122,7 @@ k_compress_append(int n_new, const float* __restrict__ kv_new, const float* __re
             st4(static_cast<float*>(win[b]) + slot * kD + ch, k);
     }
 
-    if (has_comp && c == 0 && ((T + n_new) & 1) && n_new > 0) {
+    if (kRatio == 2 && has_comp && c == 0 && ((T + n_new) & 1) && n_new > 0) {
         // the last token starts a pair that completes later. The pending read
         // above (pair T/2 when T is odd) happened in this CTA, same channels.
         __syncthreads();
@@ -200,13 +208,14 @@ extern "C" int csa2_compress_append(const csa2_params* p, int B, int n_new,
     CSA2_CHECK_PARAMS(p);
     if (B < 0 || n_new < 0) return fail(CSA2_ERR_INVALID_ARG, "compress_append: negative size");
     if (B == 0 || n_new == 0) return CSA2_OK;
-    if (p->head_dim != kD || p->window != kW || p->compress_ratio != 2)
-        return fail(CSA2_ERR_UNSUPPORTED, "compress_append: built for D=512, W=128, ratio 2");
+    if (p->head_dim != kD || p->window != kW || (p->compress_ratio != 2 && p->compress_ratio != 1))
+        return fail(CSA2_ERR_UNSUPPORTED, "compress_append: built for D=512, W=128, ratio 2 or 1");
+    const int ratio = p->compress_ratio;
     if (!kv_new || !win || !n_tokens)
         return fail(CSA2_ERR_INVALID_ARG, "compress_append: kv_new, win, n_tokens are required");
-    if (comp && (!gate_new || !pend_kv || !pend_gate || !comp_cap))
+    if (comp && (!comp_cap || (ratio == 2 && (!gate_new || !pend_kv || !pend_gate))))
         return fail(CSA2_ERR_INVALID_ARG,
-                    "compress_append: gate, pending state and comp_cap required with comp");
+                    "compress_append: comp_cap (and at ratio 2 gate and pending state) required with comp");
     const bool nvfp4 = p->kv_format == CSA2_NVFP4;
     if (comp && !nvfp4 && p->kv_format != CSA2_F32)
         return fail(CSA2_ERR_UNSUPPORTED, "compress_append: kv_format must be NVFP4 or F32");
@@ -218,21 +227,28 @@ extern "C" int csa2_compress_append(const csa2_params* p, int B, int n_new,
         (pend_kv && !aligned16(pend_kv)) || (pend_gate && !aligned16(pend_gate)))
         return fail(CSA2_ERR_ALIGN, "compress_append: fp32 buffers must be 16-byte aligned");
 
-    const int pairs = n_new / 2 + 1;
-    const int gx = comp ? (pairs + kPairsPerCta - 1) / kPairsPerCta : 1;
+    const int rows = ratio == 2 ? n_new / 2 + 1 : n_new;  // compressed rows this call can complete
+    const int gx = comp ? (rows + kPairsPerCta - 1) / kPairsPerCta : 1;
     const int advance_here = gx == 1;
     const dim3 grid(gx, B);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool we = p->win_format == CSA2_E4M3;
-#define CSA2_LAUNCH(NV, WE)                                                              \
-    k_compress_append<NV, WE><<<grid, kThreads, 0, s>>>(n_new, kv_new, gate_new, pend_kv, \
-                                                         pend_gate, comp, comp_scales,   \
-                                                         comp_cap, win, n_tokens,        \
-                                                         advance_here, dev_status)
-    if (nvfp4 && we) CSA2_LAUNCH(true, true);
-    else if (nvfp4) CSA2_LAUNCH(true, false);
-    else if (we) CSA2_LAUNCH(false, true);
-    else CSA2_LAUNCH(false, false);
+#define CSA2_LAUNCH(R, NV, WE)                                                              \
+    k_compress_append<R, NV, WE><<<grid, kThreads, 0, s>>>(n_new, kv_new, gate_new, pend_kv, \
+                                                            pend_gate, comp, comp_scales,   \
+                                                            comp_cap, win, n_tokens,        \
+                                                            advance_here, dev_status)
+    if (ratio == 2) {
+        if (nvfp4 && we) CSA2_LAUNCH(2, true, true);
+        else if (nvfp4) CSA2_LAUNCH(2, true, false);
+        else if (we) CSA2_LAUNCH(2, false, true);
+        else CSA2_LAUNCH(2, false, false);
+    } else {
+        if (nvfp4 && we) CSA2_LAUNCH(1, true, true);
+        else if (nvfp4) CSA2_LAUNCH(1, true, false);
+        else if (we) CSA2_LAUNCH(1, false, true);
+        else CSA2_LAUNCH(1, false, false);
+    }
 #undef CSA2_LAUNCH
     if (!advance_here) k_advance<<<(B + 127) / 128, 128, 0, s>>>(n_tokens, B, n_new);
     return check_launch("compress_append");

@@ -40,6 +40,7 @@ class DecodeConfig:
     kscale_pow2: bool   # index-key group scales drawn from {1, 2} (else 1)
     T: int = 0          # context length (incl. the step's token) at step 0; 0 = ragged
     T_range: tuple = (4096, 1048576)
+    ratio: int = 2      # raw tokens per compressed position: 2 (pooled) or 1 (1:1 layers)
 
     @property
     def seed(self) -> int:
@@ -73,6 +74,10 @@ CONFIGS = {
     6: DecodeConfig(6, "decode B=32 T=131072 NVFP4, 1 group x 2 layers (profiling size)", B=32,
                     groups=1, readers=2, steps=1, quant=True, plants=16, kscale_pow2=True,
                     T=131072),
+    # the uncompressed 1:1 layers: n_c = T, pooling skipped (two layers share the cache)
+    7: DecodeConfig(7, "decode B=8 T=32768 1:1 layers (n_c = T) NVFP4, 1 group x 2 layers", B=8,
+                    groups=1, readers=2, steps=1, quant=True, plants=16, kscale_pow2=True,
+                    T=32768, ratio=1),
     5: DecodeConfig(5, "decode B=32 ragged T in [4096, 1048576], 1 index source + 5 readers, "
                        "16 steps", B=32, groups=1, readers=6, steps=16, quant=True, plants=16,
                     kscale_pow2=True),
@@ -151,7 +156,7 @@ def plants(cfg, g: int, s: int):
     """(positions, values row, scales row) of the planted index keys of one sequence."""
     if not cfg.plants:
         return np.zeros(0, np.int64), None, None
-    n_c0 = cfg.first_lengths()[s] // 2
+    n_c0 = cfg.first_lengths()[s] // cfg.ratio
     pos = synth.plant_positions(cfg.seed, g, s, n_c0, cfg.plants)
     qv, _, w = host_index_q(cfg, g, s, 0)
     rv, rs = synth.plant_row(qv, w)

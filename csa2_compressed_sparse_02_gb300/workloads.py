@@ -39,14 +39,15 @@ class DecodeRun:
         self.B = cfg.B
         self.n_prep = max(1, min(self.n_steps, self.max_prepared))
         if cfg.quant:
-            self.params = api.default_params()
+            self.params = api.default_params(compress_ratio=cfg.ratio)
         else:
             self.params = api.default_params(kv_format=api.F32, win_format=api.F32,
-                                             q_format=api.F32)
+                                             q_format=api.F32, compress_ratio=cfg.ratio)
         last = [T + self.n_steps - 1 for T in self.T0]          # T after the last step
-        self.comp_caps = [t // 2 + 1 for t in last]
-        self.n_c_max = max(t // 2 for t in last)
-        self.key_rows = [max(1, t // 2) for t in last]
+        rt = cfg.ratio
+        self.comp_caps = [t // rt + 1 for t in last]
+        self.n_c_max = max(t // rt for t in last)
+        self.key_rows = [max(1, t // rt) for t in last]
         # rows of the score and block-max arrays 16-byte aligned: vector loads in the selection
         self.max_ncomp = -(-self.n_c_max // 32) * 32
         self.n_b_max = math.ceil(self.max_ncomp / 8)
@@ -318,7 +319,7 @@ class DecodeRun:
     def scan_bytes(self) -> float:
         """Algorithmic bytes of one Indexer launch at the current step: 72 B of
         key read + 4 B score + 0.5 B block max written per position."""
-        return sum((T - 1 + self.step_done) // 2 for T in self.T0) * 76.5
+        return sum((T - 1 + self.step_done) // self.cfg.ratio for T in self.T0) * 76.5
 
     def attn_bytes_per_call(self) -> float:
         """Algorithmic bytes of one sparse-attention call: per sequence the

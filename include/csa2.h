@@ -73,7 +73,9 @@ typedef struct csa2_params {
     int block_size;       /* positions per candidate block: 8 */
     int topk_blocks;      /* blocks kept: 2048 */
     int topk_pos;         /* positions kept: 512 */
-    int compress_ratio;   /* raw tokens per compressed position: 2 */
+    int compress_ratio;   /* raw tokens per compressed position: 2 (the pooled 2:1
+                             layers) or 1 (the 1:1 layers: pooling skipped, raw token
+                             p is compressed row p) */
     int kv_format;        /* compressed cache: CSA2_NVFP4 (or CSA2_F32, unquantised) */
     int win_format;       /* window ring: CSA2_E4M3 (or CSA2_F32) */
     int q_format;         /* query and output: CSA2_BF16 (or CSA2_F32) */
@@ -118,10 +120,14 @@ const char* csa2_last_error(void);
  * Every new raw token p also writes ring slot p mod W of win[b] (D bytes E4M3,
  * RNE satfinite, or D floats) — only the newest W of them, as the ring keeps.
  * Afterwards n_tokens[b] = T_b + n_new.
+ * With compress_ratio 1 (the 1:1 layers, "CSA2稀疏注意力、384专家MoE与1M上下文"
+ * §2.2) pooling is skipped: new raw token p is written as compressed row p with
+ * the same encoding, and gate_new / pend_kv / pend_gate are not used.
  *
  *   kv_new, gate_new  [B, n_new, D] fp32, device. gate_new may be NULL when
- *                     comp is NULL.
- *   pend_kv, pend_gate [B, D] fp32, device; caller zero-initialises once.
+ *                     comp is NULL or compress_ratio is 1.
+ *   pend_kv, pend_gate [B, D] fp32, device; caller zero-initialises once
+ *                     (may be NULL at compress_ratio 1).
  *   comp              device array [B] of per-sequence row bases, or NULL for a
  *                     window-only layer (compress ratio 0, or a layer that reads
  *                     another layer's compressed cache).
@@ -130,7 +136,7 @@ const char* csa2_last_error(void);
  *                     j >= comp_cap[b] is not written and sets CSA2_DEV_BAD_LENGTH.
  *   win               device array [B] of ring bases ([W, D]).
  *   n_tokens          [B] int32, device, read and advanced.
- * Constraints: D == 512; n_new >= 0; 16-byte aligned rows.
+ * Constraints: D == 512; compress_ratio 2 or 1; n_new >= 0; 16-byte aligned rows.
  */
 int csa2_compress_append(const csa2_params* p, int B, int n_new,
                          const float* kv_new, const float* gate_new,

@@ -7,7 +7,8 @@ recipe (csa2_compressed_sparse_02_gb300.inputs, numpy only; no CUDA path).
 
 Only what the step's outputs depend on is recomputed: the compressed rows of
 the selected positions (pooling is per pair, so a pair lands in a compact row
-of its own) and the window's last W raw tokens of every attending layer.
+of its own; at ratio 1 a position is one raw token) and the window's last W raw
+tokens of every attending layer.
 """
 from __future__ import annotations
 
@@ -24,7 +25,7 @@ from . import oracle as orc
 def index_and_select(cfg, g: int, s: int, step: int):
     """Indexer scores, block maxima and selection of sequence s after `step`."""
     T = cfg.first_lengths()[s] + step
-    n_c = T // 2
+    n_c = T // cfg.ratio
     qv, qs, w = I.host_index_q(cfg, g, s, step)
     kv, ks = I.host_index_keys(cfg, g, s, n_c)
     t0 = time.perf_counter()
@@ -37,11 +38,12 @@ def index_and_select(cfg, g: int, s: int, step: int):
 
 def compressed_rows(cfg, layer: int, s: int, positions):
     """Compact cache whose row i is compressed position positions[i] of `layer`."""
+    rt = cfg.ratio
     st = orc.SeqState(cap_comp=max(1, len(positions)), D=I.D, W=I.W, comp_f32=not cfg.quant,
-                      win_f32=not cfg.quant)
-    for j in positions:
-        kv = I.host_kv(cfg, layer, s, 2 * j, 2 * j + 2)
-        g = I.host_gate(cfg, layer, s, 2 * j, 2 * j + 2)
+                      win_f32=not cfg.quant, ratio=rt)
+    for j in positions:  # position j is raw tokens rt*j .. rt*j + rt - 1
+        kv = I.host_kv(cfg, layer, s, rt * j, rt * j + rt)
+        g = I.host_gate(cfg, layer, s, rt * j, rt * j + rt) if rt == 2 else None
         st.append(kv, g)
     return st
 

@@ -66,5 +66,7 @@ def test_host_side_rejections_without_launching(L):
     assert L.csa2_sparse_attn_layers_part(pp, 2, 4, 3, 2, *([None] * 10)) == 1  # range past B
     assert L.csa2_sparse_attn_layers_part(pp, 2, 4, -1, 1, *([None] * 10)) == 1
     assert L.csa2_sparse_attn_layers_part(pp, 2, 4, 1, 0, *([None] * 10)) == 0  # empty range
+    bad_ratio = api.default_params(compress_ratio=3)
+    assert L.csa2_compress_append(ctypes.byref(bad_ratio), 1, 1, *([None] * 11)) == 4
     # nothing to do is not an error
     assert L.csa2_compress_append(pp, 0, 1, *([None] * 11)) == 0

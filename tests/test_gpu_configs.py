@@ -68,6 +68,20 @@ def test_config2_full():
         assert sc[pos].min() >= unpl.mean() + 8 * unpl.std()
 
 
+def test_config7_ratio_one_full():
+    """1:1 layers: n_c = T compressed positions, each one raw token quantised."""
+    cfg = inputs.CONFIGS[7]
+    run = workloads.DecodeRun(cfg, n_steps=1)
+    run.step()
+    torch.cuda.synchronize()
+    assert run.dev_status.item() == 0
+    for s in range(cfg.B):
+        ref = _check(run, 0, s, 0)
+        assert ref["n_c"] == cfg.T and ref["n_sel"] == 512
+        pos, _, _ = inputs.plants(cfg, 0, s)
+        assert set(pos.tolist()) <= set(ref["idx"].tolist())
+
+
 def test_config3_sampled():
     cfg = inputs.CONFIGS[3]
     run = workloads.DecodeRun(cfg, n_steps=1)
