@@ -99,6 +99,7 @@ class PrefillConfig:
     plants: int = 16
     kscale_pow2: bool = True
     B: int = 1
+    ratio: int = 2      # the prefill chunk runs on a pooled (2:1) layer
     groups: int = 1
     readers: int = 1
 
