@@ -45,11 +45,11 @@ def peaks():
 
 
 # DRAM bytes per scanned position of k_index_scores_tc, from one ncu capture of
-# the decode workload B=32, T=131072 (151.44 MB read + 6.07 MB written over
+# the decode workload B=32, T=131072 (151.44 MB read + 5.32 MB written over
 # 2,097,152 positions per launch). The figure belongs to that build of the
 # kernel: it is reported only while the kernel source hashes to the same value.
-INDEX_TRAFFIC_PER_POS = (151.44e6 + 6.07e6) / 2097152
-INDEX_TRAFFIC_SRC_SHA256 = "7a0195e74de7b193c501cc87564824f30b541501191090cb7e98e998d1246050"
+INDEX_TRAFFIC_PER_POS = (151436032 + 5317376) / 2097152
+INDEX_TRAFFIC_SRC_SHA256 = "6e3056a0e294c5c850f5baf43dd581935ebe08137768b33cb586294d817442d4"
 
 
 def index_traffic(positions: float):
