@@ -223,7 +223,14 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
 
-    from csa2_compressed_sparse_02_gb300.inputs import CONFIGS
+    from csa2_compressed_sparse_02_gb300.inputs import CONFIGS, PREFILL
+    if args.config == PREFILL.number:
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the "
+                              "decode step; the prefill chunk is a secondary measurement"}))
+            return
+        prefill_main(args)
+        return
     cfg = CONFIGS[args.config]
     if args.impl == "reference":
         run_reference(args, cfg, rank)
@@ -353,6 +360,49 @@ def main():
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def prefill_main(args):
+    """Configuration 4: one prefill chunk (8,192 queries on a 262,144-token context):
+    window and Compressor append, per-query Indexer, selection and attention. A
+    secondary line: prefill tokens per second, with the per-call split."""
+    import torch
+    from csa2_compressed_sparse_02_gb300 import workloads
+    from csa2_compressed_sparse_02_gb300.inputs import PREFILL
+    run = workloads.PrefillRun(PREFILL)
+    for _ in range(args.warmup):
+        run.reset()
+        run.run()
+    torch.cuda.synchronize()
+    K = max(1, min(args.steps, 10))
+    timers = {}
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(torch.cuda.current_device()).uuid)
+    except Exception:
+        pass
+    with ClockSampler(uuid) as clk:
+        torch.cuda.synchronize()
+        start.record()
+        for _ in range(K):
+            run.reset()
+            run.run(timers)
+        end.record()
+        torch.cuda.synchronize()
+    assert int(run.dev_status.item()) == 0, "device status %d" % int(run.dev_status.item())
+    el = start.elapsed_time(end) / 1000.0 / K
+    n = PREFILL.chunk
+    print(json.dumps({
+        "metric": "CSA2 prefill tokens/s, chunk of 8192 queries on a 262144-token context",
+        "value": n / el, "unit": "tok/s", "n_gpus": 1, "steps": K, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * el, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "nvfp4/e4m3/bf16 in, fp32 accumulate",
+        "data": "synthetic (seeded counter-based generator)",
+        "config": {"workload": PREFILL.workload, "T0": PREFILL.T0, "chunk": n},
+        "ms_per_step_by_call": {c: sum(a.elapsed_time(b) for a, b in evs) / K
+                                for c, evs in timers.items()},
+        "clocks": clk.summary(), "gpu_launches": None}), flush=True)
 
 
 def run_e2e(run, K, stream, barrier):

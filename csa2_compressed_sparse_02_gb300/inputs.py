@@ -74,6 +74,11 @@ CONFIGS = {
     6: DecodeConfig(6, "decode B=32 T=131072 NVFP4, 1 group x 2 layers (profiling size)", B=32,
                     groups=1, readers=2, steps=1, quant=True, plants=16, kscale_pow2=True,
                     T=131072),
+    # the 8-index-source reading of the step: 8 scans + 8 selections + 40 attention
+    # calls (each index source published to 5 layers), against configuration 3's 4
+    8: DecodeConfig(8, "decode B=32 T=1048576 NVFP4, 8 index sources x 5 layers", B=32,
+                    groups=8, readers=5, steps=1, quant=True, plants=16, kscale_pow2=True,
+                    T=1048576),
     # the uncompressed 1:1 layers: n_c = T, pooling skipped (two layers share the cache)
     7: DecodeConfig(7, "decode B=8 T=32768 1:1 layers (n_c = T) NVFP4, 1 group x 2 layers", B=8,
                     groups=1, readers=2, steps=1, quant=True, plants=16, kscale_pow2=True,

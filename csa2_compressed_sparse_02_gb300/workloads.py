@@ -425,16 +425,43 @@ class PrefillRun:
         self.out = torch.empty(1, n, H, D, dtype=torch.bfloat16, device=dev)
         torch.cuda.synchronize()
 
+    def reset(self):
+        """Back to the state before run() (the chunk's rows are then rewritten with
+        the same values), so the chunk can be timed repeatedly."""
+        self.src.n_tokens.fill_(self.cfg.T0)
+
     def run(self, timers=None):
-        api, n, ds = self.api, self.cfg.chunk, self.dev_status
-        api.window_linear(self.params, self.kv, self.src.win_ptrs, self.src.n_tokens, self.winbuf)
-        self.src.append(self.kv, self.gate, ds)
-        for s0 in range(0, n, self.index_batch):
-            s1 = min(n, s0 + self.index_batch)
-            api.index_scores(self.params, self.n_c_final, self.iq[s0:s1], self.iqs[s0:s1],
-                             self.iw[s0:s1], self.key_ptrs[s0:s1], self.n_tok_q[s0:s1],
-                             self.scores[s0:s1], self.bmax[s0:s1], ds)
-        api.select_topk(self.params, self.n_c_final, self.scores, self.bmax, self.n_tok_q, self.idx,
-                        self.n_sel, ds)
-        api.sparse_attn_layers(self.params_lin, self.q, self.sink, self.win_q, self.n_tok_q,
-                               self.comp_ptrs, self.comp_scale_ptrs, self.idx, self.out, ds)
+        """The chunk on the current stream. timers: optional dict receiving
+        (start, end) CUDA events per call category ("append", "index", "select",
+        "attn")."""
+        api, n, ds, torch = self.api, self.cfg.chunk, self.dev_status, self.torch
+        st = torch.cuda.current_stream()
+
+        def timed(cat, fn):
+            if timers is None:
+                fn()
+                return
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            fn()
+            e1.record(st)
+            timers.setdefault(cat, []).append((e0, e1))
+
+        def append():
+            api.window_linear(self.params, self.kv, self.src.win_ptrs, self.src.n_tokens, self.winbuf)
+            self.src.append(self.kv, self.gate, ds)
+
+        def index():
+            for s0 in range(0, n, self.index_batch):
+                s1 = min(n, s0 + self.index_batch)
+                api.index_scores(self.params, self.n_c_final, self.iq[s0:s1], self.iqs[s0:s1],
+                                 self.iw[s0:s1], self.key_ptrs[s0:s1], self.n_tok_q[s0:s1],
+                                 self.scores[s0:s1], self.bmax[s0:s1], ds)
+
+        timed("append", append)
+        timed("index", index)
+        timed("select", lambda: api.select_topk(self.params, self.n_c_final, self.scores, self.bmax,
+                                                self.n_tok_q, self.idx, self.n_sel, ds))
+        timed("attn", lambda: api.sparse_attn_layers(self.params_lin, self.q, self.sink, self.win_q,
+                                                     self.n_tok_q, self.comp_ptrs,
+                                                     self.comp_scale_ptrs, self.idx, self.out, ds))
