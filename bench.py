@@ -216,6 +216,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--nvtx", action="store_true", help="mark the timed steps with an NVTX range")
     ap.add_argument("--eager", action="store_true", help="launch kernels one by one (no CUDA graph)")
+    ap.add_argument("--chunk", type=int, default=0,
+                    help="configuration 4 only: queries in the prefill chunk (default 8192)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
@@ -366,10 +368,13 @@ def prefill_main(args):
     """Configuration 4: one prefill chunk (8,192 queries on a 262,144-token context):
     window and Compressor append, per-query Indexer, selection and attention. A
     secondary line: prefill tokens per second, with the per-call split."""
+    import dataclasses
+
     import torch
     from csa2_compressed_sparse_02_gb300 import workloads
     from csa2_compressed_sparse_02_gb300.inputs import PREFILL
-    run = workloads.PrefillRun(PREFILL)
+    cfg = dataclasses.replace(PREFILL, chunk=args.chunk) if args.chunk > 0 else PREFILL
+    run = workloads.PrefillRun(cfg)
     for _ in range(args.warmup):
         run.reset()
         run.run()
@@ -392,14 +397,16 @@ def prefill_main(args):
         torch.cuda.synchronize()
     assert int(run.dev_status.item()) == 0, "device status %d" % int(run.dev_status.item())
     el = start.elapsed_time(end) / 1000.0 / K
-    n = PREFILL.chunk
+    n = cfg.chunk
     print(json.dumps({
-        "metric": "CSA2 prefill tokens/s, chunk of 8192 queries on a 262144-token context",
+        "metric": "CSA2 prefill tokens/s, chunk of %d queries on a %d-token context" % (n, cfg.T0),
         "value": n / el, "unit": "tok/s", "n_gpus": 1, "steps": K, "warmup": args.warmup,
         "ms_per_step": 1000.0 * el, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "nvfp4/e4m3/bf16 in, fp32 accumulate",
         "data": "synthetic (seeded counter-based generator)",
-        "config": {"workload": PREFILL.workload, "T0": PREFILL.T0, "chunk": n},
+        "config": {"workload": cfg.workload if cfg is PREFILL else
+                   "prefill chunk of %d queries on a %d-token context, NVFP4" % (n, cfg.T0),
+                   "T0": cfg.T0, "chunk": n},
         "ms_per_step_by_call": {c: sum(a.elapsed_time(b) for a, b in evs) / K
                                 for c, evs in timers.items()},
         "clocks": clk.summary(), "gpu_launches": None}), flush=True)

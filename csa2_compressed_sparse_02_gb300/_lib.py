@@ -42,6 +42,7 @@ SIGNATURES = {
     "csa2_index_keys_write": (I32, [PP, I32, I64, P, P, P, P, P, P, P]),
     "csa2_index_scores": (I32, [PP, I32, I64, P, P, P, P, P, P, P, P, P]),
     "csa2_index_scores_cuda_cores": (I32, [PP, I32, I64, P, P, P, P, P, P, P, P, P]),
+    "csa2_index_scores_shared": (I32, [PP, I32, I64, P, P, P, P, P, P, P, P, P]),
     "csa2_select_topk": (I32, [PP, I32, I64, P, P, P, P, P, P, P]),
     "csa2_sparse_attn_workspace_size": (SZ, [PP, I32]),
     "csa2_sparse_attn": (I32, [PP, I32, P, P, P, P, P, P, P, P, P, SZ, P, P]),

@@ -97,6 +97,17 @@ def index_scores(params, max_ncomp, q_vals, q_scales, w, key_cache_ptrs, n_token
             _stream(stream)), "index_scores")
 
 
+def index_scores_shared(params, max_ncomp, q_vals, q_scales, w, key_cache, n_tokens, scores,
+                        block_max, dev_status=None, stream=None):
+    """Q queries against ONE tiled key cache (a uint8 device tensor): the prefill
+    Indexer. q_vals [Q,32,64], q_scales [Q,32,8], w [Q,32], n_tokens [Q]."""
+    Q = n_tokens.numel()
+    check(lib().csa2_index_scores_shared(
+        ctypes.byref(params), Q, max_ncomp, _ptr(q_vals), _ptr(q_scales), _ptr(w), _ptr(key_cache),
+        _ptr(n_tokens), _ptr(scores), _ptr(block_max), _ptr(dev_status), _stream(stream)),
+        "index_scores_shared")
+
+
 def select_topk(params, max_ncomp, scores, block_max, n_tokens, idx, n_sel=None, dev_status=None,
                 stream=None):
     B = n_tokens.numel()

@@ -55,6 +55,72 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     return false;
 }
 
+// try_wait with a suspend-time hint: a waiting thread sleeps until the phase
+// completes (or the hint runs out) instead of polling, which leaves the issue
+// slots to the warps doing work. Bounded by the global timer: after about two
+// seconds without the phase the wait sets *abort and gives up; an abort raised
+// by another role ends it too.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// the same on a barrier given by its shared-memory address (hot loops keep the
+// addresses in registers instead of converting generic pointers each time)
+__device__ __forceinline__ bool mbar_try_wait_hint_at(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ void mbar_arrive_at(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ bool mbar_wait_sleep_at(uint32_t bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait_hint_at(bar, parity, 20000u)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1; i < kSpinLimit; ++i) {
+        if (mbar_try_wait_hint_at(bar, parity, 20000u)) return true;
+        if ((i & 15u) == 0u) {
+            if (*abort) return false;
+            if (global_ns() - t0 > 2000000000ull) break;
+        }
+    }
+    *abort = 1;
+    return false;
+}
+
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1; i < kSpinLimit; ++i) {
+        if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+        if ((i & 15u) == 0u) {
+            if (*abort) return false;
+            if (global_ns() - t0 > 2000000000ull) break;
+        }
+    }
+    *abort = 1;
+    return false;
+}
+
 // ---- bulk copy global -> shared, completion counted on an mbarrier ----
 __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint32_t bytes,
                                          uint64_t* bar) {
@@ -138,6 +204,11 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
             smem_u32(bar))
         : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_at(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
+                 : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns (lane quarter of the calling warp).

@@ -351,12 +351,16 @@ class PrefillRun:
     sees, its two-level selection and its sparse attention (window rows from a
     linear buffer built before the append)."""
 
-    def __init__(self, cfg, device="cuda", index_batch=1024):
+    def __init__(self, cfg, device="cuda", index_batch=1024, shared_indexer=True):
         import torch
 
         from . import api
         self.torch, self.api, self.cfg, self.device = torch, api, cfg, device
         self.index_batch = index_batch
+        # shared_indexer: every query of the chunk against the one key stream as an FP4
+        # GEMM (csa2_index_scores_shared); else the decode Indexer with one "sequence"
+        # per query (csa2_index_scores, index_batch queries per call)
+        self.shared_indexer = shared_indexer
         T0, n = cfg.T0, cfg.chunk
         self.n_c_final = (T0 + n) // 2
         self.params = api.default_params()
@@ -452,6 +456,10 @@ class PrefillRun:
             self.src.append(self.kv, self.gate, ds)
 
         def index():
+            if self.shared_indexer:
+                api.index_scores_shared(self.params, self.n_c_final, self.iq, self.iqs, self.iw,
+                                        self.keys.buf[0], self.n_tok_q, self.scores, self.bmax, ds)
+                return
             for s0 in range(0, n, self.index_batch):
                 s1 = min(n, s0 + self.index_batch)
                 api.index_scores(self.params, self.n_c_final, self.iq[s0:s1], self.iqs[s0:s1],

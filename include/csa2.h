@@ -236,6 +236,29 @@ int csa2_index_scores(const csa2_params* p, int B, int64_t max_ncomp,
                       int32_t* dev_status, void* stream);
 
 /*
+ * csa2_index_scores_shared — the Indexer for Q queries that all score ONE key
+ * stream (the prefill chunk: every query of the chunk reads the same
+ * sequence's index keys, up to its own causal length). Same per-query
+ * contract as csa2_index_scores ("DeepSeek-V4.1-Flash-NVFP4" §3.3): for query
+ * i, n_c(i) = n_tokens[i] / compress_ratio (clipped to max_ncomp with
+ * CSA2_DEV_BAD_LENGTH), s_t = sum_h w[i,h] * ReLU(q_i,h . k_t) for t < n_c(i),
+ * scores [Q, max_ncomp] fp32 and block_max [Q, ceil(max_ncomp/8)] fp32 written
+ * for t < n_c(i) and its blocks. Because the keys are shared, scoring is a
+ * dense block-scaled FP4 GEMM on the tensor cores: each 128-position key tile is
+ * loaded once per 16 queries and multiplied with 4 queries x 32 heads per MMA.
+ *   q_vals [Q, 32, 64] u8, q_scales [Q, 32, 8] u8 (E4M3), w [Q, 32] fp32
+ *   key_cache  ONE tiled key cache (the layout of csa2_index_keys_write), device,
+ *              16-byte aligned, with at least ceil(max n_c / 128) tiles.
+ *   n_tokens   [Q] int32, device: raw context length seen by each query.
+ * Work spans ceil(Q / 16) query blocks x ceil(max_ncomp / 512) key super-tiles;
+ * the super-tiles past a block's longest query are skipped.
+ */
+int csa2_index_scores_shared(const csa2_params* p, int Q, int64_t max_ncomp,
+                             const uint8_t* q_vals, const uint8_t* q_scales, const float* w,
+                             const uint8_t* key_cache, const int32_t* n_tokens,
+                             float* scores, float* block_max, int32_t* dev_status, void* stream);
+
+/*
  * csa2_index_scores_cuda_cores — the same Indexer on CUDA cores (fp32 FMA, one
  * thread per position). Same arguments and results; kept to validate the
  * tensor-core build and as its ablation.

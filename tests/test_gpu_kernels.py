@@ -217,6 +217,45 @@ def test_index_scores_bit_exact_ragged(cuda_cores):
         assert np.array_equal(gb[b, :nb], orc.block_max(ref, 8)), b
 
 
+@pytest.mark.parametrize("pow2", [True, False])
+def test_index_scores_shared_key_stream_bit_exact(pow2):
+    """Many queries against one key stream (the prefill Indexer): ragged causal
+    lengths (0, partial blocks and tiles, the full stream, past max_ncomp -> clipped
+    and flagged), a query count that is not a multiple of 16."""
+    n = 5003
+    qv, qs, w, kvs, kss, rng = _index_case(8, [n], pow2=pow2)
+    Q = 37
+    key = synth.stream_key(17, synth.IDX_Q)
+    qv = synth.e2m1_bytes(key, np.arange(Q * 32 * 64, dtype=np.uint64)).reshape(Q, 32, 64)
+    qs = np.full((Q, 32, 8), 0x38, np.uint8)
+    w = synth.w_pow2(key ^ 5, np.arange(Q * 32, dtype=np.uint64)).reshape(Q, 32)
+    lens = np.array([0, 1, 7, 8, 9, 127, 128, 129, 511, 512, 513, 2048, 4999, n, n + 40] +
+                    [int(x) for x in rng.integers(0, n + 1, Q - 15)], np.int64)
+    p = api.default_params()
+    cache = _tiled_caches(p, [kvs[0]], [kss[0]])
+    n_tok = t((2 * lens).astype(np.int32))
+    scores = torch.full((Q, n), -7.0, device=DEV)
+    bmax = torch.full((Q, math.ceil(n / 8)), -7.0, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    api.index_scores_shared(p, n, t(qv), t(qs), t(w), cache.buf[0], n_tok, scores, bmax, st)
+    torch.cuda.synchronize()
+    assert st.item() == 2  # the query past max_ncomp is clipped and flagged
+    gs, gb = scores.cpu().numpy(), bmax.cpu().numpy()
+    for i in range(Q):
+        m = int(min(lens[i], n))
+        ref, inexact = orc.index_scores(qv[i], qs[i], w[i], kvs[0][:m], kss[0][:m])
+        if pow2:
+            assert inexact == 0
+            bad = np.nonzero(gs[i, :m] != ref)[0]
+            assert bad.size == 0, (i, m, bad[:5], gs[i, bad[:5]], ref[bad[:5]])
+        else:
+            assert np.all(gs[i, :m] == ref) or np.abs(gs[i, :m] - ref).max() <= 1e-5 * max(1, np.abs(ref).max())
+        assert np.all(gs[i, m:] == -7.0)
+        nb = math.ceil(m / 8)
+        assert np.array_equal(gb[i, :nb], orc.block_max(gs[i, :m], 8)), i
+        assert np.all(gb[i, nb:] == -7.0)
+
+
 def test_index_scores_general_e4m3_scales_match_cuda_cores():
     """Non-power-of-two E4M3 scales (mantissa bits): the tensor-core and CUDA-core
     builds must agree with the oracle to fp32 rounding."""
