@@ -212,8 +212,9 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
                   float* scores, float* block_max, int32_t* dev_status) {
     using namespace sm100;
     extern __shared__ uint8_t smem_raw[];
-    TcShared& sh = *reinterpret_cast<TcShared*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // aligned by offsetting the shared array itself, so that accesses through sh
+    // stay shared-space loads and stores
+    TcShared& sh = *reinterpret_cast<TcShared*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int* abort = &sh.abort;
 

@@ -11,7 +11,7 @@
 // D[128 x 128] = K . Q^T takes two tcgen05.mma.kind::mxf4nvf4 (K = 64 each). A
 // persistent CTA walks a contiguous range of (query block of 16, key super-tile
 // of 4 tiles) items: each 36 KB super-tile is loaded once per 16 queries. The
-// epilogue (16 warps: one TMEM lane quarter x one query of the group each) reads
+// epilogue (8 warps: one TMEM lane quarter x two queries of the group each) reads
 // one key per lane, applies ReLU and the head weights,
 // mask positions past each query's own length, and write the score and the
 // block maximum (8 adjacent lanes). Every wait is bounded.
@@ -35,10 +35,11 @@ constexpr int kTilesPerStage = 4;
 constexpr int kStageBytes = kTilesPerStage * kKeyTileBytes;  // 36,864
 constexpr int kPosPerStage = kTilesPerStage * kKeyTile;      // 512
 constexpr int kStages = 4;
-constexpr int kEpiGroups = kQPerGroup;              // epilogue warpgroup e: query e of every group
+constexpr int kQPerWarp = 2;                        // queries of a group per epilogue warp
+constexpr int kEpiWarps = 4 * kQPerGroup / kQPerWarp;  // 8: lane quarter x query pair
 constexpr int kAcc = 3;                             // accumulators in flight
-constexpr int kLoadWarp = 4 * kEpiGroups, kMmaWarp = kLoadWarp + 1;
-constexpr int kThreadsSh = 32 * (kMmaWarp + 1);     // 576
+constexpr int kLoadWarp = kEpiWarps, kMmaWarp = kLoadWarp + 1;
+constexpr int kThreadsSh = 32 * (kMmaWarp + 1);     // 320
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColD = 0;                       // kAcc x 128 columns
 constexpr uint32_t kColSFA = kN * kAcc;             // 2 super-tile slots x kTilesPerStage x 8
@@ -80,14 +81,39 @@ __device__ __forceinline__ int tiles_in(int64_t g, int32_t ncmax) {
     return left <= 0 ? 0 : (left < kTilesPerStage ? (int)left : kTilesPerStage);
 }
 
+// sum over heads of w ReLU(d): a max and an FMA for the first kHRelu heads, (w/2) d
+// + (w/2) |d| (two FMAs, the weights stored halved) for the rest; four independent
+// chains. Every partial sum is exact when the products are (power-of-two scales),
+// so the order of the chains does not change the result there.
+__device__ __forceinline__ float head_sum(const float (&w)[kHi], const uint32_t* r) {
+    float c0 = 0.0f, c1 = 0.0f, c2 = 0.0f, c3 = 0.0f;
+#pragma unroll
+    for (int h = 0; h < kHRelu; h += 4) {
+        c0 = __fmaf_rn(w[h], fmaxf(__uint_as_float(r[h]), 0.0f), c0);
+        c1 = __fmaf_rn(w[h + 1], fmaxf(__uint_as_float(r[h + 1]), 0.0f), c1);
+        c2 = __fmaf_rn(w[h + 2], fmaxf(__uint_as_float(r[h + 2]), 0.0f), c2);
+        c3 = __fmaf_rn(w[h + 3], fmaxf(__uint_as_float(r[h + 3]), 0.0f), c3);
+    }
+#pragma unroll
+    for (int h = kHRelu; h < kHi; h += 2) {
+        const float d0 = __uint_as_float(r[h]), d1 = __uint_as_float(r[h + 1]);
+        c0 = __fmaf_rn(w[h], d0, c0);
+        c1 = __fmaf_rn(w[h], fabsf(d0), c1);
+        c2 = __fmaf_rn(w[h + 1], d1, c2);
+        c3 = __fmaf_rn(w[h + 1], fabsf(d1), c3);
+    }
+    return (c0 + c1) + (c2 + c3);
+}
+
 __global__ void __launch_bounds__(kThreadsSh, 1)
 k_index_shared_tc(int Q, Work wk, int64_t max_ncomp, int ratio, const uint8_t* __restrict__ q_vals,
                   const uint8_t* __restrict__ q_scales, const float* __restrict__ w,
                   const uint8_t* __restrict__ keys, const int32_t* __restrict__ n_tokens,
                   float* scores, float* block_max, int32_t* dev_status) {
     extern __shared__ uint8_t smem_raw[];
-    ShShared& sh = *reinterpret_cast<ShShared*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // aligned by offsetting the shared array itself, so that accesses through sh
+    // stay shared-space loads and stores
+    ShShared& sh = *reinterpret_cast<ShShared*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int* abort = &sh.abort;
     if (tid == 0) {
@@ -97,11 +123,11 @@ k_index_shared_tc(int Q, Work wk, int64_t max_ncomp, int ratio, const uint8_t* _
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sh.qfull[i], 1);
-            mbar_init(&sh.qempty[i], 1 + 4 * kEpiGroups);  // the MMA thread and every epilogue warp
+            mbar_init(&sh.qempty[i], 1 + kEpiWarps);  // the MMA thread and every epilogue warp
         }
         for (int i = 0; i < kAcc; ++i) {
             mbar_init(&sh.accf[i], 1);
-            mbar_init(&sh.acce[i], 4 * kEpiGroups);
+            mbar_init(&sh.acce[i], 32 * kEpiWarps);  // every epilogue thread
         }
         mbar_init(&sh.done, 1);
         sh.abort = 0;
@@ -192,92 +218,107 @@ k_index_shared_tc(int Q, Work wk, int64_t max_ncomp, int ratio, const uint8_t* _
                 if (mbar_try_wait(&sh.full[j % kStages], (uint32_t)((j / kStages) & 1))) break;
         }
     } else if (warp == kMmaWarp) {
-        // ---------------- MMA issuer (one thread): per tile two scale copies, then two
-        // MMAs per query group into the next accumulator
-        if (lane == 0) {
-            int seg = -1, prev_k = -1;
-            int s = 0, a = 0;             // stage and accumulator slots
-            uint32_t sph = 0, aph = 0;    // their phase parities
-            const uint32_t full0 = smem_u32(&sh.full[0]), accf0 = smem_u32(&sh.accf[0]);
-            const uint32_t acce0 = smem_u32(&sh.acce[0]), stage0 = smem_u32(sh.stage[0]);
-            const uint64_t dA0 = smem_desc(stage0, 16, 512, kLayoutSw64);
-            const uint64_t dB0 = smem_desc(smem_u32(sh.q[0][0]), 16, 512, kLayoutSw64);
-            int tile_par = 0;
-            bool ok = true;
-            int k = (int)(f0 / wk.st_per_block);
-            int g = (int)(f0 - (int64_t)k * wk.st_per_block);
-            for (int64_t f = f0; f < f1 && ok; ++f, g = (g + 1 == wk.st_per_block) ? (++k, 0) : g + 1) {
-                if (k != prev_k) {
-                    if (seg >= 0) tc_commit(&sh.qempty[seg & 1]);
-                    ++seg;
-                    const int qs = seg & 1;
-                    if (!mbar_wait_sleep(&sh.qfull[qs], (uint32_t)((seg >> 1) & 1), abort)) break;
-                    tc_fence_after();
+        // ---------------- MMA issuer: the whole warp runs the loop (its values stay
+        // warp-uniform) and waits; one elected lane issues every copy, MMA and commit.
+        // Per tile two scale copies, then per query group two MMAs into the next
+        // accumulator.
+        const bool leader = elect_one();
+        int seg = -1, prev_k = -1;
+        int s = 0, a = 0;             // stage and accumulator slots
+        uint32_t sph = 0, aph = 0;    // their phase parities
+        const uint32_t full0 = smem_u32(&sh.full[0]), empty0 = smem_u32(&sh.empty[0]);
+        const uint32_t accf0 = smem_u32(&sh.accf[0]), acce0 = smem_u32(&sh.acce[0]);
+        const uint32_t stage0 = smem_u32(sh.stage[0]);
+        const uint64_t dA0 = smem_desc(stage0, 16, 512, kLayoutSw64);
+        const uint64_t dB0 = smem_desc(smem_u32(sh.q[0][0]), 16, 512, kLayoutSw64);
+        int tile_par = 0;
+        bool ok = true;
+        int k = (int)(f0 / wk.st_per_block);
+        int g = (int)(f0 - (int64_t)k * wk.st_per_block);
+        const int spb = (int)wk.st_per_block;
+        for (int left = (int)(f1 - f0); left > 0 && ok; --left, g = (g + 1 == spb) ? (++k, 0) : g + 1) {
+            if (k != prev_k) {
+                if (seg >= 0 && leader) tc_commit(&sh.qempty[seg & 1]);
+                ++seg;
+                const int qs = seg & 1;
+                if (!mbar_wait_sleep(&sh.qfull[qs], (uint32_t)((seg >> 1) & 1), abort)) break;
+                tc_fence_after();
+                if (leader) {
                     for (int gi = 0; gi < kGroups; ++gi) {
                         const uint32_t sfb = smem_u32(sh.sfb[qs][gi]);
                         const uint32_t col = tmem + kColSFB + 32 * qs + 8 * gi;
                         tmem_cp_32x128b_x4(col, smem_desc(sfb, 128, 128, kLayoutNone));
                         tmem_cp_32x128b_x4(col + 4, smem_desc(sfb + 512, 128, 128, kLayoutNone));
                     }
-                    prev_k = k;
                 }
-                const int qs = seg & 1;
-                const int nt = tiles_in(g, sh.ncmax[qs]);
-                if (nt == 0) continue;
-                if (!mbar_wait_sleep_at(full0 + 8u * s, sph, abort)) break;
-                tc_fence_after();
-                // the key scales of every tile of the super-tile, in the slot of this
-                // super-tile's parity: the other slot may still feed the previous one
-                const uint32_t sfa0 = tmem + kColSFA + 8 * kTilesPerStage * tile_par;
-                tile_par ^= 1;
-                const uint32_t st0 = stage0 + (uint32_t)s * kStageBytes;
+                __syncwarp();
+                prev_k = k;
+            }
+            const int qs = seg & 1;
+            const int nt = tiles_in(g, sh.ncmax[qs]);
+            if (nt == 0) continue;
+            if (!mbar_wait_sleep_at(full0 + 8u * s, sph, abort)) break;
+            tc_fence_after();
+            // the key scales of every tile of the super-tile, in the slot of this
+            // super-tile's parity: the other slot may still feed the previous one
+            const uint32_t sfa0 = tmem + kColSFA + 8 * kTilesPerStage * tile_par;
+            tile_par ^= 1;
+            const uint32_t st0 = stage0 + (uint32_t)s * kStageBytes;
+            if (leader) {
                 for (int j = 0; j < nt; ++j) {
                     const uint32_t sf = st0 + j * kKeyTileBytes + kKeyValBytes;
                     tmem_cp_32x128b_x4(sfa0 + 8 * j, smem_desc(sf, 128, 128, kLayoutNone));
                     tmem_cp_32x128b_x4(sfa0 + 8 * j + 4, smem_desc(sf + 512, 128, 128, kLayoutNone));
                 }
-                // group-major: the epilogue keeps one query's weights across the tiles.
-                // Descriptors advance by (byte offset >> 4) in their start-address field.
-                const uint64_t dA_s = dA0 + (uint64_t)(((uint32_t)s * kStageBytes) >> 4);
-                for (int gi = 0; gi < kGroups && ok; ++gi) {
-                    const uint64_t dB = dB0 + (uint64_t)(((uint32_t)(qs * kGroups + gi) * (kN * 64)) >> 4);
-                    const uint32_t sfb = tmem + kColSFB + 32 * qs + 8 * gi;
-                    uint64_t dA = dA_s;
-                    uint32_t sfa = sfa0;
-                    for (int j = 0; j < nt; ++j, dA += kKeyTileBytes >> 4, sfa += 8) {
-                        if (!mbar_wait_sleep_at(acce0 + 8u * a, aph ^ 1u, abort)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
+            }
+            __syncwarp();
+            // group-major: the epilogue keeps one query's weights across the tiles.
+            // Descriptors advance by (byte offset >> 4) in their start-address field.
+            const uint64_t dA_s = dA0 + (uint64_t)(((uint32_t)s * kStageBytes) >> 4);
+            for (int gi = 0; gi < kGroups && ok; ++gi) {
+                const uint64_t dB = dB0 + (uint64_t)(((uint32_t)(qs * kGroups + gi) * (kN * 64)) >> 4);
+                const uint32_t sfb = tmem + kColSFB + 32 * qs + 8 * gi;
+                uint64_t dA = dA_s;
+                uint32_t sfa = sfa0;
+                for (int j = 0; j < nt; ++j, dA += kKeyTileBytes >> 4, sfa += 8) {
+                    if (!mbar_wait_sleep_at(acce0 + 8u * a, aph ^ 1u, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    if (leader) {
                         const uint32_t d = tmem + kColD + kN * a;
                         mma_mxf4nvf4(d, dA, dB, kIdesc, sfa, sfb, 0);
                         mma_mxf4nvf4(d, dA + 2, dB + 2, kIdesc, sfa + 4, sfb + 4, 1);  // K 64..127
                         tc_commit_at(accf0 + 8u * a);
-                        a = (a + 1 == kAcc) ? 0 : a + 1;
-                        aph ^= (a == 0) ? 1u : 0u;
                     }
-                }
-                tc_commit(&sh.empty[s]);
-                if (++s == kStages) {
-                    s = 0;
-                    sph ^= 1u;
+                    __syncwarp();
+                    a = (a + 1 == kAcc) ? 0 : a + 1;
+                    aph ^= (a == 0) ? 1u : 0u;
                 }
             }
+            if (leader) tc_commit_at(empty0 + 8u * s);
+            __syncwarp();
+            if (++s == kStages) {
+                s = 0;
+                sph ^= 1u;
+            }
+        }
+        if (leader) {
             if (seg >= 0) tc_commit(&sh.qempty[seg & 1]);
             // every MMA and copy issued above has completed before TMEM is freed
             tc_commit(&sh.done);
-            for (uint32_t k2 = 0; k2 < kSpinLimit; ++k2)
-                if (mbar_try_wait(&sh.done, 0)) break;
         }
         __syncwarp();
+        for (uint32_t k2 = 0; k2 < kSpinLimit; ++k2)
+            if (mbar_try_wait(&sh.done, 0)) break;
     } else {
-        // ---------------- epilogue: every item is shared by the 4 warpgroups, warpgroup
-        // eg taking query eg of the item's group; warp wq of it owns TMEM lanes 32wq..
-        // = positions 32wq.. of the tile
-        const int eg = warp >> 2, wq = warp & 3;
+        // ---------------- epilogue: warp (qp, wq) reads TMEM lanes 32 wq.. (positions
+        // 32 wq.. of the tile) for queries 2 qp and 2 qp + 1 of the item's group
+        const int wq = warp & 3, qp = warp >> 2;
         const uint32_t accf0 = smem_u32(&sh.accf[0]), acce0 = smem_u32(&sh.acce[0]);
-        const uint32_t tmem_lane = tmem + ((uint32_t)(32 * wq) << 16) + kColD + kHi * eg;
+        const uint32_t tmem_lane = tmem + ((uint32_t)(32 * wq) << 16) + kColD + kHi * kQPerWarp * qp;
+        const int ncomp32 = (int)max_ncomp, ldbm32 = (int)ld_bm;  // both below 2^31
         const bool blk_lead = (lane & (kBlk - 1)) == 0;
         int seg = -1, prev_k = -1;
         int a = 0;         // accumulator slot of the next item
@@ -299,19 +340,18 @@ k_index_shared_tc(int Q, Work wk, int64_t max_ncomp, int ratio, const uint8_t* _
             const int qs = seg & 1;
             const int nt = tiles_in(g, sh.ncmax[qs]);
             for (int gi = 0; gi < kGroups && ok; ++gi) {
-                const int qb = gi * kQPerGroup + eg;
-                const int32_t n_c = sh.nc[qs][qb];
+                const int qb = gi * kQPerGroup + kQPerWarp * qp;  // queries qb and qb + 1
+                const int32_t nc0 = sh.nc[qs][qb], nc1 = sh.nc[qs][qb + 1];
                 const int64_t qq = (int64_t)(k * kQPerBlock + qb);
-                float* srow = scores + qq * max_ncomp;
-                float* brow = block_max + qq * ld_bm;
-                float wr[kHi];
+                float* srow0 = scores + qq * max_ncomp;
+                float* brow0 = block_max + qq * ld_bm;
+                float w0[kHi], w1[kHi];
 #pragma unroll
                 for (int h4 = 0; h4 < kHi / 4; ++h4) {
-                    const float4 wv = reinterpret_cast<const float4*>(sh.w[qs][qb])[h4];
-                    wr[4 * h4] = wv.x;
-                    wr[4 * h4 + 1] = wv.y;
-                    wr[4 * h4 + 2] = wv.z;
-                    wr[4 * h4 + 3] = wv.w;
+                    const float4 v0 = reinterpret_cast<const float4*>(sh.w[qs][qb])[h4];
+                    const float4 v1 = reinterpret_cast<const float4*>(sh.w[qs][qb + 1])[h4];
+                    w0[4 * h4] = v0.x, w0[4 * h4 + 1] = v0.y, w0[4 * h4 + 2] = v0.z, w0[4 * h4 + 3] = v0.w;
+                    w1[4 * h4] = v1.x, w1[4 * h4 + 1] = v1.y, w1[4 * h4 + 2] = v1.z, w1[4 * h4 + 3] = v1.w;
                 }
                 int tl = g * kPosPerStage + 32 * wq + lane;  // this lane's position in tile j
                 for (int j = 0; j < nt; ++j, tl += kKeyTile) {
@@ -320,41 +360,25 @@ k_index_shared_tc(int Q, Work wk, int64_t max_ncomp, int ratio, const uint8_t* _
                         break;
                     }
                     tc_fence_after();
-                    uint32_t r[kHi];
-                    tmem_ld_32x32b_x32(tmem_lane + kN * a, r);
+                    uint32_t r[2 * kHi];
+                    tmem_ld_32x32b_x64_nowait(tmem_lane + kN * a, r);
+                    tmem_wait_ld();
                     tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_at(acce0 + 8u * a);  // the accumulator is read: release it
+                    mbar_arrive_at(acce0 + 8u * a);  // this thread's part of the accumulator is read
                     a = (a + 1 == kAcc) ? 0 : a + 1;
                     ph ^= (a == 0) ? 1u : 0u;
-                    // sum over heads of w ReLU(d): a max and an FMA for the first heads,
-                    // (w/2) d + (w/2) |d| (two FMAs) for the rest. Every partial sum is
-                    // exact when the products are (power-of-two scales), so the order of
-                    // the chains does not change the result there.
-                    float c0 = 0.0f, c1 = 0.0f, c2 = 0.0f, c3 = 0.0f;
+                    const float sc0 = head_sum(w0, r), sc1 = head_sum(w1, r + kHi);
+                    const bool v0 = tl < nc0, v1 = tl < nc1;
+                    float m0 = v0 ? sc0 : -INFINITY, m1 = v1 ? sc1 : -INFINITY;
 #pragma unroll
-                    for (int h = 0; h < kHRelu; h += 4) {
-                        c0 = __fmaf_rn(wr[h], fmaxf(__uint_as_float(r[h]), 0.0f), c0);
-                        c1 = __fmaf_rn(wr[h + 1], fmaxf(__uint_as_float(r[h + 1]), 0.0f), c1);
-                        c2 = __fmaf_rn(wr[h + 2], fmaxf(__uint_as_float(r[h + 2]), 0.0f), c2);
-                        c3 = __fmaf_rn(wr[h + 3], fmaxf(__uint_as_float(r[h + 3]), 0.0f), c3);
+                    for (int o = 1; o < kBlk; o <<= 1) {
+                        m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+                        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
                     }
-#pragma unroll
-                    for (int h = kHRelu; h < kHi; h += 2) {
-                        const float d0 = __uint_as_float(r[h]), d1 = __uint_as_float(r[h + 1]);
-                        c0 = __fmaf_rn(wr[h], d0, c0);
-                        c1 = __fmaf_rn(wr[h], fabsf(d0), c1);
-                        c2 = __fmaf_rn(wr[h + 1], d1, c2);
-                        c3 = __fmaf_rn(wr[h + 1], fabsf(d1), c3);
-                    }
-                    const float sc = (c0 + c1) + (c2 + c3);
-                    const bool valid = tl < n_c;
-                    float mx = valid ? sc : -INFINITY;
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-                    if (valid) srow[tl] = sc;
-                    if (valid && blk_lead) brow[tl >> 3] = mx;
+                    st_global_if(srow0 + tl, sc0, v0);
+                    st_global_if(srow0 + (ncomp32 + tl), sc1, v1);
+                    st_global_if(brow0 + (tl >> 3), m0, v0 && blk_lead);
+                    st_global_if(brow0 + (ldbm32 + (tl >> 3)), m1, v1 && blk_lead);
                 }
             }
         }

@@ -530,8 +530,9 @@ __device__ void softmax_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, i
 
 __global__ void __launch_bounds__(kAttnThreads, 1) k_sparse_attn_tc(UnitArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    AttnShared& sh = *reinterpret_cast<AttnShared*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // aligned by offsetting the shared array itself, so that accesses through sh
+    // stay shared-space loads and stores
+    AttnShared& sh = *reinterpret_cast<AttnShared*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int* abort = &sh.abort;
     if (tid == 0) {
