@@ -255,7 +255,7 @@ def main():
 
     K, Wm = args.steps, args.warmup
     e2e_steps = 0 if args.no_e2e else K
-    run = workloads.DecodeRun(cfg, n_steps=Wm + 2 + K + e2e_steps + 5)
+    run = workloads.DecodeRun(cfg, n_steps=Wm + 2 + K + e2e_steps + 5, out_slots=2)
     stream = torch.cuda.current_stream()
 
     # ---------------- warm-up, then one CUDA graph per prepared step
@@ -413,47 +413,80 @@ def prefill_main(args):
 
 
 def run_e2e(run, K, stream, barrier):
-    """Same steps through the public API with the step's inputs copied from pinned
-    host memory and the attention outputs copied back, inside the timed region."""
+    """Same steps through the public API with every step's inputs copied from pinned
+    host memory and its attention outputs copied back, inside the timed region.
+    The copies run on their own streams, overlapped with the neighbouring steps'
+    compute: step i+1's inputs travel (into their own prepared slot) while step i
+    computes, and step i's outputs (double-buffered by slot parity) travel back
+    while step i+1 computes. Every byte of every step still moves inside the timed
+    region: it ends when the last step's outputs have reached the host."""
     import torch
-    host_in, dev_in, host_out, dev_out = [], [], [], []
-    for grp in run.groups:
-        for name in ("kv", "gate", "kv_rd", "q", "iq", "iw"):
-            if name in grp:
-                t = grp[name]
-                h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
-                h.copy_(t)
-                host_in.append(h)
-                dev_in.append(t)
-        for o in grp["out"]:
-            host_out.append(torch.empty(o.shape, dtype=o.dtype, pin_memory=True))
-            dev_out.append(o)
-    torch.cuda.synchronize()
+    names = ("kv", "gate", "kv_rd", "q", "iq", "iw")
     n_prep = run.n_prep
-    h2d = 0
-    d2h = sum(o.numel() * o.element_size() for o in dev_out)
-    for h in host_in:
-        h2d += h[0].numel() * h.element_size()  # one step's slice
     advance = run.step_graph if getattr(run, "graphs", None) else run.step
     for _ in range(3):
         advance()
     torch.cuda.synchronize()
+    slot0 = run.step_done
+    slot = lambda i: (slot0 + i) % n_prep
+    host_in = {}   # slot -> list of (host, device) pairs of that slot's inputs
+    for k in sorted({slot(i) for i in range(K)}):
+        pairs = []
+        for grp in run.groups:
+            for name in names:
+                if name in grp:
+                    d = grp[name][k]
+                    h = torch.empty(d.shape, dtype=d.dtype, pin_memory=True)
+                    h.copy_(d)
+                    pairs.append((h, d))
+        host_in[k] = pairs
+    host_out = [torch.empty(run.out_of_slot(grp, 0).shape, dtype=run.out_of_slot(grp, 0).dtype,
+                            pin_memory=True) for grp in run.groups]
+    h2d = sum(h.numel() * h.element_size() for h, _ in host_in[slot(0)])
+    d2h = sum(h.numel() * h.element_size() for h in host_out)
+    torch.cuda.synchronize()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    in_done, comp_done, out_done = [ev() for _ in range(K)], [ev() for _ in range(K)], [ev() for _ in range(K)]
+
+    def send(i):
+        # the slot was last read by step i - n_prep (if it is in this loop)
+        if i - n_prep >= 0:
+            s_in.wait_event(comp_done[i - n_prep])
+        with torch.cuda.stream(s_in):
+            for h, d in host_in[slot(i)]:
+                d.copy_(h, non_blocking=True)
+        in_done[i].record(s_in)
+
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     start.record(stream)
-    for _ in range(K):
-        k = run.step_done % n_prep
-        for h, d in zip(host_in, dev_in):
-            d[k].copy_(h[k], non_blocking=True)
+    s_in.wait_stream(stream)
+    s_out.wait_stream(stream)
+    send(0)
+    for i in range(K):
+        stream.wait_event(in_done[i])
+        if i >= 2:  # the output buffer of this slot parity was read back
+            stream.wait_event(out_done[i - 2])
         advance()
-        for h, d in zip(host_out, dev_out):
-            h.copy_(d, non_blocking=True)
+        comp_done[i].record(stream)
+        if i + 1 < K:
+            send(i + 1)
+        s_out.wait_event(comp_done[i])
+        with torch.cuda.stream(s_out):
+            for h, grp in zip(host_out, run.groups):
+                h.copy_(run.out_of_slot(grp, slot(i)), non_blocking=True)
+        out_done[i].record(s_out)
+    stream.wait_stream(s_in)
+    stream.wait_stream(s_out)
     end.record(stream)
     torch.cuda.synchronize()
     barrier()
     el = start.elapsed_time(end) / 1000.0
     return {"value": run.cfg.B * K / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h}
+            "d2h_bytes_per_step": d2h,
+            "overlap": "inputs of step i+1 and outputs of step i copied on side streams "
+                       "while step i (resp. i+1) computes"}
 
 
 if __name__ == "__main__":

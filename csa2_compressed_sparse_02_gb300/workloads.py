@@ -26,6 +26,9 @@ class DecodeRun:
     max_prepared: int = 64
     cuda_core_indexer: bool = False
     fused_attention: bool = True
+    # attention outputs per input slot parity (2: a step's outputs can be read back
+    # while the next step writes its own; the prepared slot count is then even)
+    out_slots: int = 1
     step_done: int = 0
     groups: list = field(default_factory=list)
 
@@ -38,6 +41,9 @@ class DecodeRun:
         self.T0 = cfg.first_lengths()
         self.B = cfg.B
         self.n_prep = max(1, min(self.n_steps, self.max_prepared))
+        assert self.out_slots in (1, 2)
+        if self.out_slots == 2:
+            self.n_prep = max(2, self.n_prep - self.n_prep % 2)
         if cfg.quant:
             self.params = api.default_params(compress_ratio=cfg.ratio)
         else:
@@ -70,7 +76,9 @@ class DecodeRun:
             grp["bmax"] = torch.empty(self.B, self.n_b_max, dtype=torch.float32, device=dev)
             grp["idx"] = torch.empty(self.B, 512, dtype=torch.int32, device=dev)
             grp["n_sel"] = torch.empty(self.B, dtype=torch.int32, device=dev)
-            grp["out_all"] = torch.empty(cfg.readers, self.B, H, D, dtype=qdt, device=dev)
+            grp["out_buf"] = torch.empty(self.out_slots, cfg.readers, self.B, H, D, dtype=qdt,
+                                         device=dev)
+            grp["out_all"] = grp["out_buf"][0]
             grp["out"] = list(grp["out_all"].unbind(0))
             grp["sink_all"] = torch.empty(cfg.readers, H, dtype=torch.float32, device=dev)
             grp["sink"] = list(grp["sink_all"].unbind(0))
@@ -234,12 +242,17 @@ class DecodeRun:
         self.api.select_topk(self.params, self.max_ncomp, grp["scores"], grp["bmax"],
                              grp["src"].n_tokens, grp["idx"], grp["n_sel"], self.dev_status, s)
 
+    def out_of_slot(self, grp, k):
+        """Attention outputs [readers, B, H, D] written by the step of input slot k."""
+        return grp["out_buf"][k % self.out_slots]
+
     def _attn(self, s, grp, k, params):
         api, cfg, src = self.api, self.cfg, grp["src"]
+        out_all = self.out_of_slot(grp, k)
         if cfg.quant and self.fused_attention:
             api.sparse_attn_layers(params, grp["q"][k], grp["sink_all"], grp["win_all"],
                                    src.n_tokens, src.comp_ptrs, src.comp_scale_ptrs, grp["idx"],
-                                   grp["out_all"], self.dev_status, s)
+                                   out_all, self.dev_status, s)
             return
         for r in range(cfg.readers):
             if r == 0:
@@ -248,7 +261,7 @@ class DecodeRun:
                 sl = slice((r - 1) * self.B, r * self.B)
                 win_ptrs, n_tok = grp["rd"].win_ptrs[sl], grp["rd"].n_tokens[sl]
             api.sparse_attn(self.params, grp["q"][k, r], grp["sink"][r], win_ptrs, n_tok,
-                            src.comp_ptrs, src.comp_scale_ptrs, grp["idx"], grp["out"][r],
+                            src.comp_ptrs, src.comp_scale_ptrs, grp["idx"], out_all[r],
                             self.workspace, self.dev_status, s)
 
     def _enqueue(self, k, stream=None, timers=None):
