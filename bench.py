@@ -414,71 +414,24 @@ def prefill_main(args):
 
 def run_e2e(run, K, stream, barrier):
     """Same steps through the public API with every step's inputs copied from pinned
-    host memory and its attention outputs copied back, inside the timed region.
-    The copies run on their own streams, overlapped with the neighbouring steps'
-    compute: step i+1's inputs travel (into their own prepared slot) while step i
-    computes, and step i's outputs (double-buffered by slot parity) travel back
-    while step i+1 computes. Every byte of every step still moves inside the timed
-    region: it ends when the last step's outputs have reached the host."""
+    host memory and its attention outputs copied back, inside the timed region
+    (DecodeRun.pipelined_steps: the copies overlap the neighbouring steps' compute;
+    the region ends when the last step's outputs have reached the host)."""
     import torch
-    names = ("kv", "gate", "kv_rd", "q", "iq", "iw")
-    n_prep = run.n_prep
-    advance = run.step_graph if getattr(run, "graphs", None) else run.step
     for _ in range(3):
-        advance()
+        run.step_graph() if getattr(run, "graphs", None) else run.step(stream)
     torch.cuda.synchronize()
-    slot0 = run.step_done
-    slot = lambda i: (slot0 + i) % n_prep
-    host_in = {}   # slot -> list of (host, device) pairs of that slot's inputs
-    for k in sorted({slot(i) for i in range(K)}):
-        pairs = []
-        for grp in run.groups:
-            for name in names:
-                if name in grp:
-                    d = grp[name][k]
-                    h = torch.empty(d.shape, dtype=d.dtype, pin_memory=True)
-                    h.copy_(d)
-                    pairs.append((h, d))
-        host_in[k] = pairs
+    slots = sorted({(run.step_done + i) % run.n_prep for i in range(K)})
+    host_in = {k: run.host_input_pairs(k) for k in slots}
     host_out = [torch.empty(run.out_of_slot(grp, 0).shape, dtype=run.out_of_slot(grp, 0).dtype,
                             pin_memory=True) for grp in run.groups]
-    h2d = sum(h.numel() * h.element_size() for h, _ in host_in[slot(0)])
+    h2d = sum(h.numel() * h.element_size() for h, _ in host_in[slots[0]])
     d2h = sum(h.numel() * h.element_size() for h in host_out)
     torch.cuda.synchronize()
-    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    ev = lambda: torch.cuda.Event()
-    in_done, comp_done, out_done = [ev() for _ in range(K)], [ev() for _ in range(K)], [ev() for _ in range(K)]
-
-    def send(i):
-        # the slot was last read by step i - n_prep (if it is in this loop)
-        if i - n_prep >= 0:
-            s_in.wait_event(comp_done[i - n_prep])
-        with torch.cuda.stream(s_in):
-            for h, d in host_in[slot(i)]:
-                d.copy_(h, non_blocking=True)
-        in_done[i].record(s_in)
-
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     start.record(stream)
-    s_in.wait_stream(stream)
-    s_out.wait_stream(stream)
-    send(0)
-    for i in range(K):
-        stream.wait_event(in_done[i])
-        if i >= 2:  # the output buffer of this slot parity was read back
-            stream.wait_event(out_done[i - 2])
-        advance()
-        comp_done[i].record(stream)
-        if i + 1 < K:
-            send(i + 1)
-        s_out.wait_event(comp_done[i])
-        with torch.cuda.stream(s_out):
-            for h, grp in zip(host_out, run.groups):
-                h.copy_(run.out_of_slot(grp, slot(i)), non_blocking=True)
-        out_done[i].record(s_out)
-    stream.wait_stream(s_in)
-    stream.wait_stream(s_out)
+    run.pipelined_steps(K, host_in, lambda i: host_out, stream)
     end.record(stream)
     torch.cuda.synchronize()
     barrier()

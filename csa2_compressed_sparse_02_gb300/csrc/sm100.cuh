@@ -136,16 +136,23 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ---- tensor memory ----
+// The tcgen05 alloc / dealloc / ld / st / wait instructions are .sync.aligned: every
+// lane of the warp must execute the same instruction, converged. A bounded wait
+// lets lanes leave their polling loops at different iterations, so each wrapper
+// below reconverges the warp first. They must be called by all 32 lanes.
 __device__ __forceinline__ void tmem_alloc(uint32_t* smem_slot, uint32_t ncols) {
+    __syncwarp();  // .sync.aligned: the whole warp, converged
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
                      smem_u32(smem_slot)),
                  "r"(ncols)
                  : "memory");
 }
 __device__ __forceinline__ void tmem_relinquish() {
+    __syncwarp();  // .sync.aligned: the whole warp, converged
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
 }
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    __syncwarp();  // .sync.aligned: the whole warp, converged
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols)
                  : "memory");
 }
@@ -229,6 +236,7 @@ __device__ __forceinline__ void tc_commit_at(uint32_t bar) {
 // 32 lanes x 64 consecutive 32-bit columns, without the wait: the caller runs
 // tmem_wait_ld() before reading r (lane quarter of the calling warp).
 __device__ __forceinline__ void tmem_ld_32x32b_x64_nowait(uint32_t taddr, uint32_t* r) {
+    __syncwarp();  // .sync.aligned: the whole warp, converged
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
@@ -237,11 +245,13 @@ __device__ __forceinline__ void tmem_ld_32x32b_x64_nowait(uint32_t taddr, uint32
 // waits for every TMEM load of the thread (registers written by an earlier
 // *_nowait load are read only after this)
 __device__ __forceinline__ void tmem_wait_ld() {
+    __syncwarp();  // .sync.aligned: the whole warp, converged
     asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns (lane quarter of the calling warp).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t* r) {
+    __syncwarp();  // .sync.aligned: the whole warp, converged
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
         "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
@@ -256,6 +266,7 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t* r) 
 
 // 32 lanes x 8 consecutive 32-bit columns.
 __device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t* r) {
+    __syncwarp();  // .sync.aligned: the whole warp, converged
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
                    "=r"(r[6]), "=r"(r[7])
@@ -265,6 +276,7 @@ __device__ __forceinline__ void tmem_ld_32x32b_x8(uint32_t taddr, uint32_t* r) {
 
 // 32 lanes x 16 consecutive 32-bit columns.
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t* r) {
+    __syncwarp();  // .sync.aligned: the whole warp, converged
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
         "%15}, [%16];\n"
@@ -278,6 +290,7 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t* r) 
 // 32 lanes x 32 consecutive 32-bit columns from registers into TMEM (lane
 // quarter of the calling warp); tmem_wait_st() orders them before later use.
 __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t* r) {
+    __syncwarp();  // .sync.aligned: the whole warp, converged
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
         "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
@@ -289,6 +302,7 @@ __device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_
         : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() {
+    __syncwarp();  // .sync.aligned: the whole warp, converged
     asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
 }
 

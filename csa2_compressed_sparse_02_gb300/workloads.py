@@ -314,6 +314,72 @@ class DecodeRun:
         self.graphs[self.step_done % self.n_prep].replay()
         self.step_done += 1
 
+    def host_input_pairs(self, k):
+        """(pinned host copy, device slot view) of every per-step input of slot k, the
+        host copies filled from the device slot (the data a caller would send)."""
+        torch = self.torch
+        pairs = []
+        for grp in self.groups:
+            for name in ("kv", "gate", "kv_rd", "q", "iq", "iw"):
+                if name in grp:
+                    d = grp[name][k]
+                    h = torch.empty(d.shape, dtype=d.dtype, pin_memory=True)
+                    h.copy_(d)
+                    pairs.append((h, d))
+        return pairs
+
+    def pipelined_steps(self, K, host_in, host_out_of, stream):
+        """K steps with every step's inputs sent from pinned host memory and its
+        attention outputs read back, the copies overlapped with the neighbouring
+        steps' compute: step i+1's inputs travel on one side stream into their own
+        prepared slot while step i computes on `stream`, and step i's outputs
+        (double-buffered by slot parity; needs out_slots=2) travel back on another
+        while step i+1 computes (captured graphs when capture() ran, else eager). host_in: slot -> list of
+        (host, device) pairs (host_input_pairs); host_out_of(i): the pinned host
+        tensors, one per group, that receive step i's outputs. Everything is
+        enqueued; on return `stream` waits for every copy."""
+        torch = self.torch
+        assert self.out_slots == 2, "needs out_slots=2"
+        graphs = bool(getattr(self, "graphs", None))
+        n_prep, slot0 = self.n_prep, self.step_done
+        slot = lambda i: (slot0 + i) % n_prep
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        in_done = [torch.cuda.Event() for _ in range(K)]
+        comp_done = [torch.cuda.Event() for _ in range(K)]
+        out_done = [torch.cuda.Event() for _ in range(K)]
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+
+        def send(i):
+            if i - n_prep >= 0:  # the slot was last read by step i - n_prep
+                s_in.wait_event(comp_done[i - n_prep])
+            with torch.cuda.stream(s_in):
+                for h, d in host_in[slot(i)]:
+                    d.copy_(h, non_blocking=True)
+            in_done[i].record(s_in)
+
+        if K > 0:
+            send(0)
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                stream.wait_event(in_done[i])
+                if i >= 2:  # the output buffer of this slot parity was read back
+                    stream.wait_event(out_done[i - 2])
+                if graphs:
+                    self.step_graph()
+                else:
+                    self.step(stream)
+                comp_done[i].record(stream)
+                if i + 1 < K:
+                    send(i + 1)
+                s_out.wait_event(comp_done[i])
+                with torch.cuda.stream(s_out):
+                    for h, grp in zip(host_out_of(i), self.groups):
+                        h.copy_(self.out_of_slot(grp, slot(i)), non_blocking=True)
+                out_done[i].record(s_out)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+
     def tokens_after(self, s: int) -> int:
         return self.T0[s] - 1 + self.step_done
 

@@ -135,3 +135,33 @@ def test_config4_prefill_sampled_queries():
         rel = np.linalg.norm(o - e) / np.linalg.norm(e)
         assert err <= 1.5e-2 and rel <= 4e-3, (i, err, rel)
     assert int(run.n_sel.min().item()) == 512
+
+
+def test_pipelined_steps_overlapped_copies_config1():
+    """The end-to-end loop the bench times: per-step inputs sent from pinned host
+    memory and outputs read back on side streams, overlapped with the neighbouring
+    steps (double-buffered outputs). Each step's host outputs match the oracle."""
+    cfg = inputs.CONFIGS[1]
+    K = 5
+    run = workloads.DecodeRun(cfg, n_steps=K + 1, out_slots=2)
+    assert run.n_prep % 2 == 0
+    assert run.capture()
+    host_in = {k: run.host_input_pairs(k) for k in range(run.n_prep)}
+    # scramble the device slots: the step must use what was sent from the host
+    for grp in run.groups:
+        for name in ("kv", "gate", "kv_rd", "q", "iq", "iw"):
+            if name in grp:
+                grp[name].zero_()
+    outs = [[torch.empty(run.out_of_slot(grp, 0).shape, dtype=run.out_of_slot(grp, 0).dtype,
+                         pin_memory=True) for grp in run.groups] for _ in range(K)]
+    stream = torch.cuda.current_stream()
+    run.pipelined_steps(K, host_in, lambda i: outs[i], stream)
+    torch.cuda.synchronize()
+    assert run.dev_status.item() == 0
+    for k in (0, 1, K - 1):
+        ref = reference.decode_step(cfg, 0, 0, k)
+        for r, e in ref["out"].items():
+            o = outs[k][0][r][0].float().numpy().astype(np.float64)
+            err = np.abs(o - e).max()
+            rel = np.linalg.norm(o - e) / np.linalg.norm(e)
+            assert err <= 1.5e-2 and rel <= 4e-3, (k, r, err, rel)
