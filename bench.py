@@ -216,6 +216,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--nvtx", action="store_true", help="mark the timed steps with an NVTX range")
     ap.add_argument("--eager", action="store_true", help="launch kernels one by one (no CUDA graph)")
+    ap.add_argument("--whole-unit-attn", action="store_true",
+                    help="fused attention in whole (layer, sequence) units, round robin, instead "
+                         "of even (unit, tile) ranges per CTA")
     ap.add_argument("--chunk", type=int, default=0,
                     help="configuration 4 only: queries in the prefill chunk (default 8192)")
     args = ap.parse_args()
@@ -255,7 +258,8 @@ def main():
 
     K, Wm = args.steps, args.warmup
     e2e_steps = 0 if args.no_e2e else K
-    run = workloads.DecodeRun(cfg, n_steps=Wm + 2 + K + e2e_steps + 5, out_slots=2)
+    run = workloads.DecodeRun(cfg, n_steps=Wm + 2 + K + e2e_steps + 5, out_slots=2,
+                              split_attention=not args.whole_unit_attn)
     stream = torch.cuda.current_stream()
 
     # ---------------- warm-up, then one CUDA graph per prepared step
@@ -339,7 +343,9 @@ def main():
                    "l2": "inputs larger than L2: %.2f GB of index keys streamed per step, "
                          "%.1f GB compressed cache" % (scan_b / 76.5 * 72 * cfg.groups / 1e9,
                                                        scan_b / 76.5 * 288 * cfg.groups / 1e9),
-                   "parallelism": "replicas x%d (sequences sharded, no collective)" % world},
+                   "parallelism": "replicas x%d (sequences sharded, no collective)" % world,
+                   "attention_schedule": "whole units round robin" if args.whole_unit_attn
+                   else "even (unit, tile) ranges per CTA, cut units merged"},
         "roofline": {"kernel": "index_scores (Indexer scan, fused block max)", "bound": "hbm",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": index_traffic(scan_b / 76.5),

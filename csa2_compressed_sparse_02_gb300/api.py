@@ -130,12 +130,28 @@ def sparse_attn(params, q, sink, win_ptrs, n_tokens, comp_ptrs, comp_scale_ptrs,
         "sparse_attn")
 
 
+def sparse_attn_layers_split_workspace(params, L, B, device="cuda"):
+    """Zero-filled workspace for sparse_attn_layers(..., workspace=...) on the
+    current device (one partial-result slot per CTA boundary + the counts)."""
+    n = lib().csa2_sparse_attn_layers_split_workspace_size(ctypes.byref(params), L, B)
+    return torch.zeros(max(int(n), 256), dtype=torch.uint8, device=device)
+
+
 def sparse_attn_layers(params, q, sink, win_ptrs, n_tokens, comp_ptrs, comp_scale_ptrs, idx, out,
-                       dev_status=None, stream=None, mma_sync=False):
+                       dev_status=None, stream=None, mma_sync=False, workspace=None):
     """L layers sharing one compressed cache and selection: q/out [L, B, H, D] bf16,
     sink [L, H], win_ptrs [L*B] (layer-major), n_tokens [B]. mma_sync=True runs
-    the legacy warp-level tensor-core implementation of the same contract."""
+    the legacy warp-level tensor-core implementation of the same contract. With a
+    workspace (sparse_attn_layers_split_workspace) the tcgen05 path spreads the
+    (unit, tile) work evenly over the CTAs (csa2_sparse_attn_layers_split)."""
     L, B = q.shape[0], q.shape[1]
+    if workspace is not None and not mma_sync:
+        check(lib().csa2_sparse_attn_layers_split(
+            ctypes.byref(params), L, B, _ptr(q), _ptr(sink), _ptr(win_ptrs), _ptr(n_tokens),
+            _ptr(comp_ptrs), _ptr(comp_scale_ptrs), _ptr(idx), _ptr(out), _ptr(workspace),
+            workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)),
+            "sparse_attn_layers_split")
+        return
     fn = lib().csa2_sparse_attn_layers_mma if mma_sync else lib().csa2_sparse_attn_layers
     check(fn(
         ctypes.byref(params), L, B, _ptr(q), _ptr(sink), _ptr(win_ptrs), _ptr(n_tokens),

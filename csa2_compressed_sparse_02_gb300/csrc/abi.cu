@@ -1,5 +1,6 @@
 // Host-side pieces of the C ABI: defaults, version, per-thread error text.
 #include <cmath>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -18,6 +19,27 @@ int check_launch(const char* what) {
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return fail(CSA2_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+    return CSA2_OK;
+}
+
+int ensure_loaded() {
+    static std::mutex mu;
+    static uint64_t done = 0;  // bit d: device d loaded
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return check_launch("device");
+    if (dev < 0 || dev >= 64) return CSA2_OK;
+    std::lock_guard<std::mutex> g(mu);
+    if ((done >> dev) & 1u) return CSA2_OK;
+    cudaError_t (*lists[])() = {preload_compress, preload_index, preload_index_shared,
+                                preload_select, preload_attn, preload_attn_tc};
+    for (auto f : lists) {
+        const cudaError_t e = f();
+        if (e != cudaSuccess) {
+            cudaGetLastError();
+            return fail(CSA2_ERR_CUDA, std::string("loading the kernels: ") + cudaGetErrorString(e));
+        }
+    }
+    done |= 1ull << dev;
     return CSA2_OK;
 }
 

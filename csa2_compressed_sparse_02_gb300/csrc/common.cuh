@@ -30,6 +30,31 @@ int check_launch(const char* what);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Loads a kernel's code now (a CUDA runtime that loads modules lazily would
+// otherwise do it at the first launch or attribute call) and, when it asks
+// for more than 48 KB of shared memory, sets that limit.
+template <typename K>
+inline cudaError_t preload_kernel(K* k, int smem = 0) {
+    cudaFuncAttributes at;
+    cudaError_t e = cudaFuncGetAttributes(&at, reinterpret_cast<const void*>(k));
+    if (e == cudaSuccess && smem > 48 * 1024)
+        e = cudaFuncSetAttribute(reinterpret_cast<const void*>(k),
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    return e;
+}
+
+// Every kernel of the library loaded and its attributes set on the current
+// device, once per device, before the first launch of any of them. Returns
+// CSA2_OK or CSA2_ERR_CUDA (text in csa2_last_error). Each translation unit
+// contributes its own preload_* list.
+int ensure_loaded();
+cudaError_t preload_compress();
+cudaError_t preload_index();
+cudaError_t preload_index_shared();
+cudaError_t preload_select();
+cudaError_t preload_attn();
+cudaError_t preload_attn_tc();
+
 // Raise a status bit on the device (NULL status pointer = ignore).
 __device__ __forceinline__ void raise_status(int32_t* st, int bit) {
     if (st) atomicOr(st, bit);

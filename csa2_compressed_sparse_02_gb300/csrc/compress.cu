@@ -176,6 +176,25 @@ k_window_linear(int n_new, const float* __restrict__ kv_new, const void* const* 
 }
 
 }  // namespace
+
+cudaError_t preload_compress() {
+    cudaError_t (*l[])() = {
+        [] { return preload_kernel(k_compress_append<2, true, true>); },
+        [] { return preload_kernel(k_compress_append<2, true, false>); },
+        [] { return preload_kernel(k_compress_append<2, false, true>); },
+        [] { return preload_kernel(k_compress_append<2, false, false>); },
+        [] { return preload_kernel(k_compress_append<1, true, true>); },
+        [] { return preload_kernel(k_compress_append<1, true, false>); },
+        [] { return preload_kernel(k_compress_append<1, false, true>); },
+        [] { return preload_kernel(k_compress_append<1, false, false>); },
+        [] { return preload_kernel(k_advance); },
+        [] { return preload_kernel(k_nvfp4_quantize); },
+        [] { return preload_kernel(k_window_linear); }};
+    for (auto f : l)
+        if (const cudaError_t e = f()) return e;
+    return cudaSuccess;
+}
+
 }  // namespace csa2
 
 using namespace csa2;
@@ -194,6 +213,7 @@ extern "C" int csa2_window_linear(const csa2_params* p, int B, int n_new, const 
         return fail(CSA2_ERR_ALIGN, "window_linear: kv_new and out must be 16-byte aligned");
     const int rows = kW - 1 + n_new;
     const int gx = rows < 1024 ? rows : 1024;
+    if (const int rc = ensure_loaded()) return rc;
     k_window_linear<<<dim3(gx, B), kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         n_new, kv_new, win, n_tokens, out);
     return check_launch("window_linear");
@@ -233,6 +253,7 @@ extern "C" int csa2_compress_append(const csa2_params* p, int B, int n_new,
     const dim3 grid(gx, B);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool we = p->win_format == CSA2_E4M3;
+    if (const int rc = ensure_loaded()) return rc;
 #define CSA2_LAUNCH(R, NV, WE)                                                              \
     k_compress_append<R, NV, WE><<<grid, kThreads, 0, s>>>(n_new, kv_new, gate_new, pend_kv, \
                                                             pend_gate, comp, comp_scales,   \
@@ -265,6 +286,7 @@ extern "C" int csa2_nvfp4_quantize(const float* x, int64_t n_rows, int row_len, 
     const int64_t n = n_rows * (int64_t)row_len;
     const int64_t threads = n / 4;
     const int64_t blocks = (threads + 255) / 256;
+    if (const int rc = ensure_loaded()) return rc;
     k_nvfp4_quantize<<<(unsigned)blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(x, n, vals,
                                                                                       scales);
     return check_launch("nvfp4_quantize");

@@ -456,6 +456,14 @@ int check_index_args(const csa2_params* p, int B, int64_t max_ncomp, const void*
 }
 
 }  // namespace
+
+cudaError_t preload_index() {
+    cudaError_t e = preload_kernel(k_index_keys_write);
+    if (!e) e = preload_kernel(k_index_scores_cc);
+    if (!e) e = preload_kernel(k_index_scores_tc, kTcSmem);
+    return e;
+}
+
 }  // namespace csa2
 
 using namespace csa2;
@@ -473,6 +481,7 @@ extern "C" int csa2_index_keys_write(const csa2_params* p, int B, int64_t n, con
     if (!aligned16(vals) || (reinterpret_cast<uintptr_t>(scales) & 7))
         return fail(CSA2_ERR_ALIGN, "index_keys_write: vals 16-byte, scales 8-byte aligned");
     const int64_t total = (int64_t)B * n;
+    if (const int rc = ensure_loaded()) return rc;
     k_index_keys_write<<<(unsigned)((total + 255) / 256), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         B, n, vals, scales, pos0, dst, cap, dev_status);
     return check_launch("index_keys_write");
@@ -488,6 +497,7 @@ extern "C" int csa2_index_scores_cuda_cores(const csa2_params* p, int B, int64_t
     if (rc != CSA2_OK) return rc < 0 ? CSA2_OK : rc;
     const int64_t gx = (max_ncomp + kKeysPerCta - 1) / kKeysPerCta;
     if (gx > 0x7fffffff) return fail(CSA2_ERR_UNSUPPORTED, "index_scores: too many positions");
+    if (const int rc = ensure_loaded()) return rc;
     k_index_scores_cc<<<dim3((unsigned)gx, B), kKeysPerCta, 0, static_cast<cudaStream_t>(stream)>>>(
         max_ncomp, p->compress_ratio, q_vals, q_scales, w, key_cache, n_tokens, scores, block_max,
         dev_status);
@@ -503,6 +513,7 @@ extern "C" int csa2_index_scores(const csa2_params* p, int B, int64_t max_ncomp,
                                     scores, block_max);
     if (rc != CSA2_OK) return rc < 0 ? CSA2_OK : rc;
     if (B > kMaxSeq) return fail(CSA2_ERR_UNSUPPORTED, "index_scores: at most 1024 sequences per call");
+    if (const int rc = ensure_loaded()) return rc;
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(k_index_scores_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,

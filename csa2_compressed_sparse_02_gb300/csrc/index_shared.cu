@@ -410,6 +410,9 @@ int sm_count_sh() {
 }
 
 }  // namespace
+
+cudaError_t preload_index_shared() { return preload_kernel(k_index_shared_tc, kShSmem); }
+
 }  // namespace csa2
 
 using namespace csa2;
@@ -434,6 +437,7 @@ extern "C" int csa2_index_scores_shared(const csa2_params* p, int Q, int64_t max
         (reinterpret_cast<uintptr_t>(w) & 3))
         return fail(CSA2_ERR_ALIGN, "index_scores_shared: q_vals, key_cache 16-byte, q_scales 8-byte aligned");
     {
+        if (const int rc = ensure_loaded()) return rc;
         static std::mutex mu;
         static uint64_t attr_set = 0;
         int dev = 0;

@@ -461,6 +461,9 @@ k_select_topk(int64_t max_ncomp, int ratio, const float* __restrict__ scores,
 }
 
 }  // namespace
+
+cudaError_t preload_select() { return preload_kernel(k_select_topk, (int)sizeof(SelShared)); }
+
 }  // namespace csa2
 
 using namespace csa2;
@@ -479,6 +482,7 @@ extern "C" int csa2_select_topk(const csa2_params* p, int B, int64_t max_ncomp,
         return fail(CSA2_ERR_UNSUPPORTED, "select_topk: more than 2^31 positions");
     if (!scores || !block_max || !n_tokens || !idx)
         return fail(CSA2_ERR_INVALID_ARG, "select_topk: NULL buffer");
+    if (const int rc = ensure_loaded()) return rc;
     static bool attr_set = false;
     const int smem = (int)sizeof(SelShared);
     if (!attr_set) {

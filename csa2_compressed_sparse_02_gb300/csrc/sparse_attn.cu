@@ -721,6 +721,16 @@ size_t ws_o_bytes(int B) { return (size_t)B * kSplits * kH * kD * sizeof(float);
 size_t ws_ml_bytes(int B) { return (size_t)B * kSplits * kH * sizeof(float2); }
 
 }  // namespace
+
+cudaError_t preload_attn() {
+    cudaError_t e = preload_kernel(k_sparse_attn_bf16, kSmemBf16);
+    if (!e) e = preload_kernel(k_sparse_attn_f32, kSmemF32);
+    if (!e) e = preload_kernel(k_sparse_attn_merge<true>);
+    if (!e) e = preload_kernel(k_sparse_attn_merge<false>);
+    if (!e) e = preload_kernel(k_sparse_attn_fd, kSmemFd);
+    return e;
+}
+
 }  // namespace csa2
 
 using namespace csa2;
@@ -749,6 +759,7 @@ extern "C" int csa2_sparse_attn_layers_mma(const csa2_params* p, int L, int B, c
     if (!aligned16(q) || !aligned16(out))
         return fail(CSA2_ERR_ALIGN, "sparse_attn_layers_mma: q, out must be 16-byte aligned");
     if (L > 65535 || B > 65535) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn_layers_mma: grid too large");
+    if (const int rc = ensure_loaded()) return rc;
     static bool attr = false;
     if (!attr) {
         if (cudaFuncSetAttribute(k_sparse_attn_fd, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -793,6 +804,7 @@ extern "C" int csa2_sparse_attn(const csa2_params* p, int B, const void* q, cons
     float2* ws_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + ws_o_bytes(B));
     const float scale_log2 = p->softmax_scale * kLog2e;
     const dim3 grid(kSplits, B);
+    if (const int rc = ensure_loaded()) return rc;
     static bool attr_bf16 = false, attr_f32 = false;
     if (quant) {
         if (!attr_bf16) {
@@ -852,6 +864,7 @@ extern "C" int csa2_sparse_attn_noalloc(const csa2_params* p, int B, const void*
         return fail(CSA2_ERR_UNSUPPORTED,
                     "sparse_attn_noalloc: at most 32 sequences per call (the built-in scratch "
                     "holds 32); split the batch or use csa2_sparse_attn with a workspace");
+    if (const int rc = ensure_loaded()) return rc;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
         return check_launch("sparse_attn_noalloc: current device");

@@ -7,8 +7,10 @@
 // layer's compressed cache and selection).
 //
 // Work unit: one (layer, sequence); a persistent CTA per SM walks its units.
-// The 640 positions are 5 tiles of 128 (tile 0 = the window ring, tiles 1..4 =
-// idx[0..512) in 128s). Per tile, with the positions as the MMA's M:
+// The 640 positions are 5 tiles of 128 (tiles 0..3 = idx[0..512) in 128s, tile
+// 4 = the window ring: a unit opens on gathered rows, one round trip away, and
+// the window's two rounds of loads overlap tile 3). Per tile, with the
+// positions as the MMA's M:
 //   S^T[128 x 64]  = K_tile[128 x 512] . Q^T            (TMEM, 64 columns)
 //   O^T[512 x 64] += V_tile^T[512 x 128] . P^T[128 x 64] (TMEM, 4 x 64 columns)
 // The tile is decoded exactly into f16 in shared memory once and is the A
@@ -62,8 +64,10 @@ struct AttnShared {
     float red_sum[4][64];     // per lane quarter: the sum over its 32 rows of each head
     uint64_t q_full, q_empty, s_full, p_full, o_full, drain;
     uint64_t chunk_full[4], chunk_empty[4], red_max_bar[2], red_sum_bar[2];
+    uint64_t soft_bar;  // the 8 softmax warps (merge of a cut unit)
     uint32_t tmem_base;
     int abort;
+    int merge;          // merge decision of a cut unit, broadcast to the softmax warps
 };
 constexpr int kAttnSmem = (int)sizeof(AttnShared) + 1024;
 
@@ -139,6 +143,9 @@ __device__ __forceinline__ float warp_max(float v) {
 struct UnitArgs {
     int L, B, ratio, win_linear;
     int b0, nb;  // the sequences [b0, b0 + nb) of the batch of B are processed; units = L * nb
+    int split;   // 0: whole units round robin; 1: even ranges of (unit, tile) items
+    float* ws_part;   // split: per boundary two partial results (kPartFloats each)
+    int32_t* ws_cnt;  // split: per boundary the count of its finished pieces
     float scale_log2;
     const __nv_bfloat16* q;
     const float* sink;
@@ -164,6 +171,55 @@ __device__ __forceinline__ UnitIdx unit_idx(const UnitArgs& a, int u) {
     return x;
 }
 
+// ---------------------------------------------------------------- schedule
+// A piece is the tiles [j0, j1) of unit u. Without a workspace a CTA takes whole
+// units round robin (blockIdx.x, + gridDim.x, ...). With one, the L * nb * 5
+// (unit, tile) items are cut into gridDim.x contiguous ranges of equal length,
+// so every CTA streams the same number of tiles (10 or 11 of them for 320 units
+// on 152 CTAs, against 3 or 2 whole units of 5). A unit cut by the start of
+// CTA c's range is finished by two pieces — its head, the last piece of CTA
+// c - 1, and its tail, the first piece of CTA c — which share boundary slot c.
+// A range is at least 5 items long (grid <= units), so no unit is cut twice.
+struct Piece {
+    int u, j0, j1;
+    // boundary slot of a cut unit (0: the unit is whole) and the piece's role
+    // in it (0: head, tiles from 0; 1: tail, tiles up to 5)
+    __device__ __forceinline__ int slot(const UnitArgs& a) const {
+        if (!a.split) return 0;
+        return j0 > 0 ? (int)blockIdx.x : (j1 < kTiles ? (int)blockIdx.x + 1 : 0);
+    }
+    __device__ __forceinline__ int role() const { return j0 > 0 ? 1 : 0; }
+};
+
+struct PieceIter {
+    int item, end, step;  // step: items between round-robin units; 0 in range mode
+    __device__ __forceinline__ void init(const UnitArgs& a) {
+        const int64_t n = (int64_t)a.L * a.nb * kTiles;  // < 2^31 (units <= 2^28)
+        if (a.split) {
+            item = (int)(n * blockIdx.x / gridDim.x);
+            end = (int)(n * (blockIdx.x + 1) / gridDim.x);
+            step = 0;
+        } else {
+            item = (int)blockIdx.x * kTiles;
+            end = (int)n;
+            step = (int)gridDim.x * kTiles;
+        }
+    }
+    __device__ __forceinline__ bool next(Piece& p) {
+        if (item >= end) return false;
+        p.u = item / kTiles;
+        p.j0 = item - p.u * kTiles;
+        p.j1 = min(kTiles, p.j0 + (end - item));
+        item = step ? item + step : item + (p.j1 - p.j0);
+        return true;
+    }
+};
+
+// Partial result of a piece in its boundary slot: O [64 heads][512 dims] fp32
+// (unnormalised, relative to the piece's running maximum), then the maximum m
+// (log2 domain) and the sum l of each head.
+constexpr int kPartFloats = kH * kD + 2 * kH;
+
 __device__ __forceinline__ bool unit_aligned(const UnitArgs& a, int f, int b) {
     const uintptr_t w = reinterpret_cast<uintptr_t>(a.win[f]);
     const uintptr_t c = reinterpret_cast<uintptr_t>(a.comp[b]);
@@ -177,22 +233,20 @@ __device__ __forceinline__ bool unit_aligned(const UnitArgs& a, int f, int b) {
 __device__ void producer_role(AttnShared& sh, const UnitArgs& a, int pt, int lane,
                               volatile int* abort) {
     const int pw = pt >> 5, r = pt >> 1, hf = pt & 1;
-    const int n_units = a.L * a.nb;
-    int it = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
-        const UnitIdx ui = unit_idx(a, u);
+    PieceIter pi;
+    pi.init(a);
+    Piece pc;
+    int it = 0, gt = 0;  // pieces and tiles done
+    int64_t T = 0;
+    bool aligned = false;
+    int32_t xs[kTiles - 1];
+    for (; pi.next(pc); ++it) {
+        const UnitIdx ui = unit_idx(a, pc.u);
         const int b = ui.b;
-        const int64_t T = a.n_tokens[b];
-        const int64_t n_c = T > 0 ? T / a.ratio : 0;
-        const bool aligned = unit_aligned(a, ui.f, b);
-        if (!aligned && pt == 0) raise_status(a.dev_status, CSA2_DEV_BAD_ALIGN);
-
-        // selected positions of this thread's row in tiles 1..4
-        int32_t xs[kTiles - 1];
-#pragma unroll
-        for (int j = 0; j < kTiles - 1; ++j) xs[j] = a.idx[(int64_t)b * kKp + 128 * j + r];
-
-        // ---- query: warp pw stages heads 8pw..8pw+7, lane = dims 16*lane..+15
+        // ---- query: warp pw stages heads 8pw..8pw+7, lane = dims 16*lane..+15. The
+        // loads go first: nothing below waits on them until the conversion, so their
+        // latency overlaps the scalar loads and the wait for the last S of the
+        // previous piece (no branch on a loaded value comes before that wait).
         {
             const uint4* qu = reinterpret_cast<const uint4*>(a.q + (int64_t)ui.f * kH * kD);
             uint4 qa[4], qb[4];
@@ -202,7 +256,13 @@ __device__ void producer_role(AttnShared& sh, const UnitArgs& a, int pt, int lan
                 qa[hi] = __ldg(src);
                 qb[hi] = __ldg(src + 1);
             }
+            T = a.n_tokens[b];
+            aligned = unit_aligned(a, ui.f, b);
+            // selected positions of this thread's row in tiles 0..3
+#pragma unroll
+            for (int j = 0; j < kTiles - 1; ++j) xs[j] = a.idx[(int64_t)b * kKp + 128 * j + r];
             if (it > 0 && !mbar_wait(&sh.q_empty, (uint32_t)((it - 1) & 1), abort)) return;
+            if (!aligned && pt == 0) raise_status(a.dev_status, CSA2_DEV_BAD_ALIGN);
 #pragma unroll
             for (int hi = 0; hi < 8; ++hi) {
                 const int h = 8 * pw + hi;
@@ -242,25 +302,25 @@ __device__ void producer_role(AttnShared& sh, const UnitArgs& a, int pt, int lan
         __syncwarp();
         if (lane == 0) mbar_arrive(&sh.q_full);
 
-        // ---- the 5 tiles
+        // ---- the 5 tiles: the 4 tiles of selected rows, then the window
+        const int64_t n_c = T > 0 ? T / a.ratio : 0;
         const uint8_t* winb = static_cast<const uint8_t*>(a.win[ui.f]);
         const uint8_t* compb = static_cast<const uint8_t*>(a.comp[b]);
         const uint8_t* compsb = a.comp_scales[b];
-        for (int j = 0; j < kTiles; ++j) {
-            const int gt = it * kTiles + j;
+        for (int j = pc.j0; j < pc.j1; ++j, ++gt) {
             // window: two pairs in flight (4 x 16 B each); compressed: all four (2 x 16 B + scales)
             uint4 raw[8];
             uint32_t scw[4];
             bool valid;
             const uint4* wsrc = nullptr;
-            if (j == 0) {
+            if (j == kTiles - 1) {
                 valid = aligned && win_row_valid(r, T, a.win_linear);
                 wsrc = reinterpret_cast<const uint4*>(winb + (int64_t)r * kD + 64 * hf);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     raw[k] = valid ? __ldg(wsrc + 8 * (k >> 2) + (k & 3)) : make_uint4(0u, 0u, 0u, 0u);
             } else {
-                const int64_t x0 = xs[j - 1];
+                const int64_t x0 = xs[j];
                 if (x0 >= n_c && hf == 0) raise_status(a.dev_status, CSA2_DEV_BAD_INDEX);
                 valid = aligned && x0 >= 0 && x0 < n_c;
                 const int64_t x = valid ? x0 : 0;
@@ -281,7 +341,7 @@ __device__ void producer_role(AttnShared& sh, const UnitArgs& a, int pt, int lan
 #pragma unroll
                     for (int un = 0; un < 8; ++un)
                         *reinterpret_cast<uint4*>(dst + sw128(r, un)) = make_uint4(0u, 0u, 0u, 0u);
-                } else if (j == 0) {  // 64 E4M3 bytes -> 64 f16, unit un = bytes 8un..8un+7
+                } else if (j == kTiles - 1) {  // 64 E4M3 bytes -> 64 f16, unit un = bytes 8un..8un+7
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const uint4 v = raw[4 * (pr & 1) + k];
@@ -329,13 +389,14 @@ __device__ void mma_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, volat
     const uint64_t dQ = smem_desc(smem_u32(sh.q[0]), 16, 1024, kLayoutSw128);
     const uint64_t dV = smem_desc(smem_u32(sh.kv[0]), kKVChunk, 1024, kLayoutSw128);
     const uint64_t dP = smem_desc(smem_u32(sh.p), 1024, 1024, kLayoutSw128);
-    const int n_units = a.L * a.nb;
-    int it = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
+    PieceIter pi;
+    pi.init(a);
+    Piece pc;
+    int it = 0, gt = 0;
+    for (; pi.next(pc); ++it) {
         if (!mbar_wait(&sh.q_full, (uint32_t)(it & 1), abort)) return;
         tc_fence_after();
-        for (int j = 0; j < kTiles; ++j) {
-            const int gt = it * kTiles + j;
+        for (int j = pc.j0; j < pc.j1; ++j, ++gt) {
             // S^T = K . Q^T over the 512 dims, chunk pair by chunk pair as they land
 #pragma unroll
             for (int pr = 0; pr < 4; ++pr) {
@@ -351,7 +412,7 @@ __device__ void mma_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, volat
                     }
             }
             tc_commit(&sh.s_full);
-            if (j == kTiles - 1) tc_commit(&sh.q_empty);
+            if (j == pc.j1 - 1) tc_commit(&sh.q_empty);
             // O^T += V^T . P^T, one block of 128 dims (= one chunk pair) at a time
             if (!mbar_wait(&sh.p_full, (uint32_t)(gt & 1), abort)) return;
             tc_fence_after();
@@ -360,7 +421,7 @@ __device__ void mma_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, volat
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     mma_f16(tmem + kColO + 64 * mb, dV + ((2 * mb * kKVChunk + k * 2048) >> 4),
-                            dP + ((k * 2048) >> 4), kIdescPV, (j | k) != 0);
+                            dP + ((k * 2048) >> 4), kIdescPV, j != pc.j0 || k != 0);
                 tc_commit(&sh.chunk_empty[mb]);
             }
         }
@@ -374,7 +435,7 @@ struct SoftUnit {
     int32_t T, n_c;  // raw tokens, compressed positions
     bool aligned;
     float sink2;     // sink logit of head 32hh + lane, log2 domain
-    int32_t xs[4];   // this row's selected positions in tiles 1..4
+    int32_t xs[4];   // this row's selected positions in tiles 0..3
     __device__ __forceinline__ void load(const UnitArgs& a, int u, int r, int hh, int lane) {
         const UnitIdx ui = unit_idx(a, u);
         const int l = ui.l, b = ui.b;
@@ -387,27 +448,44 @@ struct SoftUnit {
     }
 };
 
+// Barrier of the 8 softmax warps on an mbarrier (bounded wait: an aborted warp
+// cannot strand the others). n counts the phases used so far.
+__device__ __forceinline__ bool soft_sync(AttnShared& sh, uint32_t& n, int lane, volatile int* abort) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sh.soft_bar);
+    return mbar_wait(&sh.soft_bar, (n++) & 1u, abort);
+}
+
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ void softmax_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, int warp, int lane,
                              volatile int* abort) {
     const int qd = warp & 3, hh = warp >> 2;
     const int r = 32 * qd + lane;                   // position row of the tile
     const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);  // this warp's TMEM lane quarter
-    const int n_units = a.L * a.nb;
+    PieceIter pi;
+    pi.init(a);
+    Piece cur, nxt;
+    bool has = pi.next(cur);
+    bool has_nx = has && pi.next(nxt);
     SoftUnit cu, nx;
-    if ((int)blockIdx.x < n_units) cu.load(a, blockIdx.x, r, hh, lane);
-    int it = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++it) {
+    if (has) cu.load(a, cur.u, r, hh, lane);
+    int it = 0, gt = 0;
+    uint32_t sync_n = 0;  // soft_sync phases used
+    for (; has; ++it) {
         if (!mbar_wait(&sh.q_full, (uint32_t)(it & 1), abort)) return;
         float m_run = -INFINITY;  // running maximum of head 32hh + lane
         float lpart[32];          // this row's share of the sum of P, head 32hh + i
 #pragma unroll
         for (int i = 0; i < 32; ++i) lpart[i] = 0.f;
-        for (int j = 0; j < kTiles; ++j) {
-            const int gt = it * kTiles + j;
-            const bool valid = j == 0 ? cu.aligned && win_row_valid(r, cu.T, a.win_linear)
-                                      : cu.aligned && cu.xs[j - 1] >= 0 && cu.xs[j - 1] < cu.n_c;
-            if (j == kTiles - 1 && u + (int)gridDim.x < n_units)  // next unit's scalars, early
-                nx.load(a, u + gridDim.x, r, hh, lane);
+        for (int j = cur.j0; j < cur.j1; ++j, ++gt) {
+            const bool valid = j == kTiles - 1 ? cu.aligned && win_row_valid(r, cu.T, a.win_linear)
+                                               : cu.aligned && cu.xs[j] >= 0 && cu.xs[j] < cu.n_c;
+            if (j == cur.j1 - 1 && has_nx) nx.load(a, nxt.u, r, hh, lane);  // next piece's scalars, early
             if (!mbar_wait(&sh.s_full, (uint32_t)(gt & 1), abort)) return;
             tc_fence_after();
             const float bias = valid ? 0.f : -INFINITY;
@@ -498,32 +576,106 @@ __device__ void softmax_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, i
         const float lsum = (sh.red_sum[0][32 * hh + lane] + sh.red_sum[1][32 * hh + lane]) +
                            (sh.red_sum[2][32 * hh + lane] + sh.red_sum[3][32 * hh + lane]);
         const float sink2 = cu.sink2;
-        const float M = fmaxf(m_run, sink2);
-        const float sc = m_run == -INFINITY ? 0.f : exp2f(m_run - M);
-        const float fin = sc / (lsum * sc + exp2f(sink2 - M));
-        // Lane = dim d of 32 heads. The warp stages its 32 heads x 32 dims as bf16
-        // (head i -> row 32qd + i, its 64 bytes -> the units 4hh..4hh+3 of that
-        // row): exactly the bytes of the P buffer this warp writes itself, so no
-        // other warp touches them. Then 16-byte stores of 64-byte row pieces.
-        uint8_t* ob = reinterpret_cast<uint8_t*>(a.out + (int64_t)unit_idx(a, u).f * kH * kD + 32 * hh * kD);
+        // o = O fo (+ O' fx): fo scales this piece's O; fx the other piece's O' when a
+        // unit cut at a CTA boundary is merged here (lane = head 32hh + lane).
+        float fo = 0.f, fx = 0.f;
+        const float* oth = nullptr;
+        bool emit = true;
+        const int slot = cur.slot(a);
+        if (slot == 0) {
+            const float M = fmaxf(m_run, sink2);
+            const float sc = m_run == -INFINITY ? 0.f : exp2f(m_run - M);
+            fo = sc / (lsum * sc + exp2f(sink2 - M));
+        } else {
+            // Cut unit: the piece that finishes second merges (log-sum-exp). A piece
+            // that finds the other one counted already merges at once; otherwise it
+            // publishes its partial (stores, fence, barrier, count) and the count
+            // decides. The merging piece puts the count back to 0.
+            float* slotp = a.ws_part + (int64_t)(slot - 1) * 2 * kPartFloats;
+            float* own = slotp + cur.role() * kPartFloats;
+            oth = slotp + (cur.role() ^ 1) * kPartFloats;
+            int32_t* cnt = a.ws_cnt + (slot - 1);
+            const bool t0 = warp == 0 && lane == 0;
+            if (!soft_sync(sh, sync_n, lane, abort)) return;
+            if (t0) sh.merge = ld_acquire_gpu(cnt) == 1 ? 1 : 0;
+            if (!soft_sync(sh, sync_n, lane, abort)) return;
+            int mode = sh.merge;
+            if (mode == 0) {
+                if (qd == 0) {
+                    own[kH * kD + 32 * hh + lane] = m_run;
+                    own[kH * kD + kH + 32 * hh + lane] = lsum;
+                }
 #pragma unroll 1
-        for (int mb = 0; mb < 4; ++mb) {
-            uint32_t ov[32];
-            tmem_ld_32x32b_x32(tl + kColO + 64 * mb + 32 * hh, ov);
+                for (int mb = 0; mb < 4; ++mb) {
+                    uint32_t ov[32];
+                    tmem_ld_32x32b_x32(tl + kColO + 64 * mb + 32 * hh, ov);
+                    float* dst = own + (int64_t)(32 * hh) * kD + 128 * mb + 32 * qd + lane;
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                *reinterpret_cast<__nv_bfloat16*>(sh.p + sw128(32 * qd + i, 4 * hh + (lane >> 3)) + 2 * (lane & 7)) =
-                    __float2bfloat16_rn(__uint_as_float(ov[i]) * __shfl_sync(0xffffffffu, fin, i));
-            __syncwarp();
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int q = lane + 32 * c, row = q >> 2, piece = q & 3;
-                const uint4 v = *reinterpret_cast<const uint4*>(sh.p + sw128(32 * qd + row, 4 * hh + piece));
-                *reinterpret_cast<uint4*>(ob + (int64_t)row * kD * 2 + (128 * mb + 32 * qd) * 2 + 16 * piece) = v;
+                    for (int i = 0; i < 32; ++i) dst[(int64_t)i * kD] = __uint_as_float(ov[i]);
+                }
+                __threadfence();
+                if (!soft_sync(sh, sync_n, lane, abort)) return;
+                if (t0) {
+                    __threadfence();
+                    sh.merge = atomicAdd(cnt, 1) == 1 ? 1 : 2;
+                }
+                if (!soft_sync(sh, sync_n, lane, abort)) return;
+                mode = sh.merge;
             }
-            __syncwarp();
+            emit = mode == 1;
+            if (emit) {
+                __threadfence();
+                if (t0) *cnt = 0;
+                const float mx = __ldcg(oth + kH * kD + 32 * hh + lane);
+                const float lx = __ldcg(oth + kH * kD + kH + 32 * hh + lane);
+                // combined head piece first whichever piece merges: the result does
+                // not depend on which one finished second
+                const bool own_head = cur.role() == 0;
+                const float mh = own_head ? m_run : mx, lh = own_head ? lsum : lx;
+                const float mt = own_head ? mx : m_run, lt = own_head ? lx : lsum;
+                const float M = fmaxf(fmaxf(mh, mt), sink2);
+                const float sh_ = mh == -INFINITY ? 0.f : exp2f(mh - M);
+                const float st_ = mt == -INFINITY ? 0.f : exp2f(mt - M);
+                const float den = __fadd_rn(__fadd_rn(__fmul_rn(lh, sh_), __fmul_rn(lt, st_)), exp2f(sink2 - M));
+                fo = (own_head ? sh_ : st_) / den;
+                fx = (own_head ? st_ : sh_) / den;
+            }
+        }
+        // Lane = dim d = 128 mb + 32 qd + lane of 32 heads: for each head the warp
+        // stores 32 consecutive bf16 (64 contiguous bytes) straight from registers.
+        if (emit) {
+            __nv_bfloat16* ob = a.out + (int64_t)unit_idx(a, cur.u).f * kH * kD + (int64_t)(32 * hh) * kD +
+                                32 * qd + lane;
+#pragma unroll 1
+            for (int mb = 0; mb < 4; ++mb) {
+                uint32_t ov[32];
+                tmem_ld_32x32b_x32(tl + kColO + 64 * mb + 32 * hh, ov);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    ov[i] = __float_as_uint(__fmul_rn(__uint_as_float(ov[i]), __shfl_sync(0xffffffffu, fo, i)));
+                if (oth) {  // o = O_head f_head + O_tail f_tail, rounded products (no
+                            // contraction), so the sum is the same whichever piece merges
+                    const float* src = oth + (int64_t)(32 * hh) * kD + 128 * mb + 32 * qd + lane;
+#pragma unroll
+                    for (int h16 = 0; h16 < 2; ++h16) {
+                        float x[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) x[i] = __ldcg(src + (int64_t)(16 * h16 + i) * kD);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            ov[16 * h16 + i] = __float_as_uint(__fadd_rn(
+                                __uint_as_float(ov[16 * h16 + i]),
+                                __fmul_rn(x[i], __shfl_sync(0xffffffffu, fx, 16 * h16 + i))));
+                    }
+                }
+#pragma unroll
+                for (int i = 0; i < 32; ++i) ob[(int64_t)i * kD + 128 * mb] = __float2bfloat16_rn(__uint_as_float(ov[i]));
+            }
         }
         cu = nx;
+        cur = nxt;
+        has = has_nx;
+        has_nx = has && pi.next(nxt);
         tc_fence_before();
     }
 }
@@ -550,6 +702,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_sparse_attn_tc(UnitArgs a) 
             mbar_init(&sh.red_max_bar[i], 4);
             mbar_init(&sh.red_sum_bar[i], 4);
         }
+        mbar_init(&sh.soft_bar, kSoftWarps);
         sh.abort = 0;
         fence_mbar_init();
     }
@@ -593,34 +746,54 @@ int sm_count(int dev) {
     return n[dev];
 }
 
-}  // namespace
-}  // namespace csa2
+// Boundary slots a split launch of L x nb units uses on this device: one per CTA
+// boundary of the grid the launch takes.
+int64_t split_slots(const csa2_params* p, int64_t units, int dev) {
+    int64_t sms = sm_count(dev);
+    if (p->max_ctas > 0 && p->max_ctas < sms) sms = p->max_ctas;
+    const int64_t grid = units < sms ? units : sms;
+    return grid > 1 ? grid - 1 : 0;
+}
 
-using namespace csa2;
+size_t split_ws_bytes(int64_t slots) {
+    const size_t cnt = ((size_t)slots * sizeof(int32_t) + 255) & ~(size_t)255;
+    return cnt + (size_t)slots * 2 * kPartFloats * sizeof(float);
+}
 
-extern "C" int csa2_sparse_attn_layers_part(const csa2_params* p, int L, int B, int b0, int nb,
-                                            const void* q,
-                                       const float* sink, const void* const* win,
-                                       const int32_t* n_tokens, const void* const* comp,
-                                       const uint8_t* const* comp_scales, const int32_t* idx,
-                                       void* out, int32_t* dev_status, void* stream) {
+int launch_layers(const char* name, const csa2_params* p, int L, int B, int b0, int nb,
+                  const void* q, const float* sink, const void* const* win,
+                  const int32_t* n_tokens, const void* const* comp,
+                  const uint8_t* const* comp_scales, const int32_t* idx, void* out,
+                  void* workspace, size_t ws_bytes, bool split, int32_t* dev_status,
+                  void* stream) {
+    const std::string n(name);
     CSA2_CHECK_PARAMS(p);
     if (L < 0 || B < 0 || b0 < 0 || nb < 0 || b0 + nb > B)
-        return fail(CSA2_ERR_INVALID_ARG, "sparse_attn_layers: bad size or sequence range");
+        return fail(CSA2_ERR_INVALID_ARG, n + ": bad size or sequence range");
     if (L == 0 || nb == 0) return CSA2_OK;
     if (p->heads != kH || p->head_dim != kD || p->window != kW || p->topk_pos != kKp ||
         p->compress_ratio < 1)
-        return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn_layers: built for 64 heads x 512, W=128, k=512");
+        return fail(CSA2_ERR_UNSUPPORTED, n + ": built for 64 heads x 512, W=128, k=512");
     if (p->kv_format != CSA2_NVFP4 || p->win_format != CSA2_E4M3 || p->q_format != CSA2_BF16)
-        return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn_layers: formats must be NVFP4, E4M3, BF16");
+        return fail(CSA2_ERR_UNSUPPORTED, n + ": formats must be NVFP4, E4M3, BF16");
     if (!q || !sink || !win || !n_tokens || !comp || !comp_scales || !idx || !out)
-        return fail(CSA2_ERR_INVALID_ARG, "sparse_attn_layers: NULL buffer");
+        return fail(CSA2_ERR_INVALID_ARG, n + ": NULL buffer");
     if (!aligned16(q) || !aligned16(out))
-        return fail(CSA2_ERR_ALIGN, "sparse_attn_layers: q, out must be 16-byte aligned");
-    if ((int64_t)L * B > (int64_t)1 << 30)
-        return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn_layers: too many (layer, sequence) units");
+        return fail(CSA2_ERR_ALIGN, n + ": q, out must be 16-byte aligned");
+    if ((int64_t)L * B > (int64_t)1 << 28)
+        return fail(CSA2_ERR_UNSUPPORTED, n + ": too many (layer, sequence) units");
+    if (const int rc = ensure_loaded()) return rc;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return check_launch("sparse_attn_layers: device");
+    if (cudaGetDevice(&dev) != cudaSuccess) return check_launch((n + ": device").c_str());
+    const int64_t units = (int64_t)L * nb;
+    if (split) {
+        const int64_t slots = split_slots(p, units, dev);
+        if (slots > 0 && !workspace) return fail(CSA2_ERR_INVALID_ARG, n + ": NULL workspace");
+        if (ws_bytes < split_ws_bytes(slots))
+            return fail(CSA2_ERR_INVALID_ARG, n + ": workspace smaller than its size function asks");
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+            return fail(CSA2_ERR_ALIGN, n + ": workspace must be 256-byte aligned");
+    }
     {
         static std::mutex mu;
         static uint64_t attr_set = 0;
@@ -628,7 +801,7 @@ extern "C" int csa2_sparse_attn_layers_part(const csa2_params* p, int L, int B, 
         if (dev >= 0 && dev < 64 && !((attr_set >> dev) & 1u)) {
             if (cudaFuncSetAttribute(k_sparse_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      kAttnSmem) != cudaSuccess)
-                return check_launch("sparse_attn_layers: smem attribute");
+                return check_launch((n + ": smem attribute").c_str());
             attr_set |= 1ull << dev;
         }
     }
@@ -649,12 +822,36 @@ extern "C" int csa2_sparse_attn_layers_part(const csa2_params* p, int L, int B, 
     a.idx = idx;
     a.out = static_cast<__nv_bfloat16*>(out);
     a.dev_status = dev_status;
-    const int64_t units = (int64_t)L * nb;
+    a.split = split ? 1 : 0;
+    a.ws_cnt = static_cast<int32_t*>(workspace);
+    a.ws_part = nullptr;
+    if (split && workspace) {
+        const int64_t slots = split_slots(p, units, dev);
+        a.ws_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                             (split_ws_bytes(slots) - (size_t)slots * 2 * kPartFloats * sizeof(float)));
+    }
     int64_t sms = sm_count(dev);
     if (p->max_ctas > 0 && p->max_ctas < sms) sms = p->max_ctas;
     const int grid = (int)(units < sms ? units : sms);
     k_sparse_attn_tc<<<grid, kAttnThreads, kAttnSmem, static_cast<cudaStream_t>(stream)>>>(a);
-    return check_launch("sparse_attn_layers");
+    return check_launch(name);
+}
+
+}  // namespace
+
+cudaError_t preload_attn_tc() { return preload_kernel(k_sparse_attn_tc, kAttnSmem); }
+
+}  // namespace csa2
+
+using namespace csa2;
+
+extern "C" int csa2_sparse_attn_layers_part(const csa2_params* p, int L, int B, int b0, int nb,
+                                            const void* q, const float* sink, const void* const* win,
+                                            const int32_t* n_tokens, const void* const* comp,
+                                            const uint8_t* const* comp_scales, const int32_t* idx,
+                                            void* out, int32_t* dev_status, void* stream) {
+    return launch_layers("sparse_attn_layers", p, L, B, b0, nb, q, sink, win, n_tokens, comp,
+                         comp_scales, idx, out, nullptr, 0, false, dev_status, stream);
 }
 
 extern "C" int csa2_sparse_attn_layers(const csa2_params* p, int L, int B, const void* q,
@@ -662,6 +859,23 @@ extern "C" int csa2_sparse_attn_layers(const csa2_params* p, int L, int B, const
                                        const int32_t* n_tokens, const void* const* comp,
                                        const uint8_t* const* comp_scales, const int32_t* idx,
                                        void* out, int32_t* dev_status, void* stream) {
-    return csa2_sparse_attn_layers_part(p, L, B, 0, B, q, sink, win, n_tokens, comp, comp_scales,
-                                        idx, out, dev_status, stream);
+    return launch_layers("sparse_attn_layers", p, L, B, 0, B, q, sink, win, n_tokens, comp,
+                         comp_scales, idx, out, nullptr, 0, false, dev_status, stream);
+}
+
+extern "C" size_t csa2_sparse_attn_layers_split_workspace_size(const csa2_params* p, int L, int B) {
+    if (!p || L <= 0 || B <= 0) return 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    return split_ws_bytes(split_slots(p, (int64_t)L * B, dev));
+}
+
+extern "C" int csa2_sparse_attn_layers_split(const csa2_params* p, int L, int B, const void* q,
+                                             const float* sink, const void* const* win,
+                                             const int32_t* n_tokens, const void* const* comp,
+                                             const uint8_t* const* comp_scales, const int32_t* idx,
+                                             void* out, void* workspace, size_t ws_bytes,
+                                             int32_t* dev_status, void* stream) {
+    return launch_layers("sparse_attn_layers_split", p, L, B, 0, B, q, sink, win, n_tokens, comp,
+                         comp_scales, idx, out, workspace, ws_bytes, true, dev_status, stream);
 }

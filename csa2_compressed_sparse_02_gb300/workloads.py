@@ -26,6 +26,8 @@ class DecodeRun:
     max_prepared: int = 64
     cuda_core_indexer: bool = False
     fused_attention: bool = True
+    # fused attention with the (unit, tile) work cut evenly over the CTAs
+    split_attention: bool = True
     # attention outputs per input slot parity (2: a step's outputs can be read back
     # while the next step writes its own; the prepared slot count is then even)
     out_slots: int = 1
@@ -60,6 +62,11 @@ class DecodeRun:
         self.dev_status = torch.zeros(1, dtype=torch.int32, device=dev)
         ws = api.sparse_attn_workspace_size(self.params, self.B)
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=dev)
+        self.attn_ws = None
+        if cfg.quant and self.fused_attention and self.split_attention:
+            # sized for the full grid (max_ctas 0), so it also serves capped grids
+            self.attn_ws = api.sparse_attn_layers_split_workspace(self.params, cfg.readers, self.B,
+                                                                  device=dev)
         qdt = torch.bfloat16 if cfg.quant else torch.float32
         for g in range(cfg.groups):
             grp = {}
@@ -252,7 +259,7 @@ class DecodeRun:
         if cfg.quant and self.fused_attention:
             api.sparse_attn_layers(params, grp["q"][k], grp["sink_all"], grp["win_all"],
                                    src.n_tokens, src.comp_ptrs, src.comp_scale_ptrs, grp["idx"],
-                                   out_all, self.dev_status, s)
+                                   out_all, self.dev_status, s, workspace=self.attn_ws)
             return
         for r in range(cfg.readers):
             if r == 0:

@@ -353,6 +353,43 @@ int csa2_sparse_attn_layers_part(const csa2_params* p, int L, int B, int b0, int
                                  int32_t* dev_status, void* stream);
 
 /*
+ * csa2_sparse_attn_layers_split — csa2_sparse_attn_layers with the work spread
+ * evenly over the CTAs. ("DeepSeek-V4.1-Flash-NVFP4" §3.4: the pages' kernel
+ * splits the positions of a query across CTAs and merges the parts by their
+ * log-sum-exp; here only units cut by a CTA boundary are split.)
+ * The L*B units x 5 tiles of 128 positions (idx in 128s, then the window) are cut
+ * into one contiguous range of equal length per CTA (one CTA per SM, or
+ * p->max_ctas), so no SM idles while others finish a third unit. A unit cut by
+ * a range boundary is computed in two pieces; each piece leaves its partial
+ * (unnormalised O, running maximum and sum per head) in its boundary's slot of
+ * the workspace and the piece that finishes second merges both and writes out.
+ * Arguments and results as csa2_sparse_attn_layers, plus:
+ *   workspace: device memory of at least
+ *     csa2_sparse_attn_layers_split_workspace_size(p, L, B) bytes, 256-byte
+ *     aligned, ZERO-FILLED before its first use (it holds one completion count
+ *     per boundary, which every launch that completes leaves at zero again).
+ *     Launches that share a workspace must be ordered (one stream or events).
+ *     After a launch that raised CSA2_DEV_TIMEOUT, zero it again.
+ *   A smaller or NULL workspace returns CSA2_ERR_INVALID_ARG (nothing enqueued);
+ *   a misaligned one CSA2_ERR_ALIGN.
+ */
+int csa2_sparse_attn_layers_split(const csa2_params* p, int L, int B,
+                                  const void* q, const float* sink,
+                                  const void* const* win, const int32_t* n_tokens,
+                                  const void* const* comp, const uint8_t* const* comp_scales,
+                                  const int32_t* idx, void* out,
+                                  void* workspace, size_t ws_bytes,
+                                  int32_t* dev_status, void* stream);
+
+/*
+ * Workspace bytes of csa2_sparse_attn_layers_split for L layers x B sequences
+ * on the CURRENT device (its SM count and p->max_ctas fix the grid): one
+ * 263,168-byte slot per CTA boundary (about 40 MB at 152 SMs) plus the counts.
+ * 0 for empty sizes or a NULL p.
+ */
+size_t csa2_sparse_attn_layers_split_workspace_size(const csa2_params* p, int L, int B);
+
+/*
  * csa2_sparse_attn_layers_mma — the same contract as csa2_sparse_attn_layers on
  * the legacy warp-level tensor-core path (mma.sync bf16, P rounded to bf16),
  * one CTA per (layer, sequence) with the output accumulator in registers.

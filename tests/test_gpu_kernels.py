@@ -428,8 +428,29 @@ def test_sparse_attn_out_of_range_index_is_skipped_and_flagged():
     assert ok, e
 
 
-@pytest.mark.parametrize("mma_sync", [False, True], ids=["tcgen05", "mma_sync"])
-def test_sparse_attn_layers_matches_oracle_per_layer(mma_sync):
+# How the fused reader attention is launched: (mma_sync, split, max_ctas). The
+# split modes cut the (unit, tile) work into equal ranges per CTA; max_ctas caps
+# the grid so that ranges cut units at many different tiles.
+LAYER_MODES = {
+    "tcgen05": (False, False, 0),
+    "tcgen05_split": (False, True, 0),
+    "tcgen05_split_4ctas": (False, True, 4),
+    "tcgen05_split_7ctas": (False, True, 7),
+    "mma_sync": (True, False, 0),
+}
+
+
+def _run_layers(mode, p, L, B, *args, repeat=1):
+    mma_sync, split, max_ctas = LAYER_MODES[mode]
+    p.max_ctas = max_ctas
+    ws = api.sparse_attn_layers_split_workspace(p, L, B) if split else None
+    for _ in range(repeat):
+        api.sparse_attn_layers(p, *args, mma_sync=mma_sync, workspace=ws)
+    return ws
+
+
+@pytest.mark.parametrize("mode", list(LAYER_MODES))
+def test_sparse_attn_layers_matches_oracle_per_layer(mode):
     """L layers share one compressed cache and one selection; each has its own
     window ring, query and sink (the KV-sharing readers of a source layer)."""
     rng = np.random.default_rng(31)
@@ -469,10 +490,13 @@ def test_sparse_attn_layers_matches_oracle_per_layer(mma_sync):
     win_all = torch.cat([src.win_ptrs] + [w.win_ptrs for w in wins])
     out = torch.empty(L, B, 64, 512, dtype=torch.bfloat16, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    api.sparse_attn_layers(p, q_dev, t(sink), win_all, src.n_tokens, src.comp_ptrs,
-                           src.comp_scale_ptrs, t(idx), out, status, mma_sync=mma_sync)
+    ws = _run_layers(mode, p, L, B, q_dev, t(sink), win_all, src.n_tokens, src.comp_ptrs,
+                     src.comp_scale_ptrs, t(idx), out, status)
     torch.cuda.synchronize()
     assert status.item() == 1
+    if ws is not None:  # every boundary count is back at zero for the next launch
+        n_slots = max(0, min(L * B, p.max_ctas or 10 ** 9, torch.cuda.get_device_properties(0).multi_processor_count) - 1)
+        assert int(ws[: 4 * n_slots].view(torch.int32).abs().sum().item()) == 0
     got = out.float().cpu().numpy().astype(np.float64)
     q64 = synth.bf16_to_f64(qb)
     for l in range(L):
@@ -496,8 +520,8 @@ def _e4m3_small_bytes(rng, shape):
     return ((sgn << 7) | (e << 3) | m).astype(np.uint8)
 
 
-@pytest.mark.parametrize("mma_sync", [False, True], ids=["tcgen05", "mma_sync"])
-def test_sparse_attn_layers_rescale_and_many_units(mma_sync):
+@pytest.mark.parametrize("mode", list(LAYER_MODES))
+def test_sparse_attn_layers_rescale_and_many_units(mode):
     """192 (layer, sequence) units (more than one per SM), partial windows, empty
     and out-of-range selections, NaN bytes in window slots that are not yet
     valid, and planted compressed rows aligned with a query head whose logits
@@ -547,10 +571,16 @@ def test_sparse_attn_layers_rescale_and_many_units(mma_sync):
     win_all = torch.cat([src.win_ptrs] + [w.win_ptrs for w in wins])
     out = torch.empty(L, B, 64, 512, dtype=torch.bfloat16, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    api.sparse_attn_layers(p, q_dev, t(sink), win_all, src.n_tokens, src.comp_ptrs,
-                           src.comp_scale_ptrs, t(idx), out, status, mma_sync=mma_sync)
+    _run_layers(mode, p, L, B, q_dev, t(sink), win_all, src.n_tokens, src.comp_ptrs,
+                src.comp_scale_ptrs, t(idx), out, status)
     torch.cuda.synchronize()
     assert status.item() == 1  # the planted out-of-range index only
+    if LAYER_MODES[mode][1]:  # a second launch on the same workspace gives the same bytes
+        out2 = torch.empty_like(out)
+        _run_layers(mode, p, L, B, q_dev, t(sink), win_all, src.n_tokens, src.comp_ptrs,
+                    src.comp_scale_ptrs, t(idx), out2, status, repeat=2)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
     got = out.float().cpu().numpy().astype(np.float64)
     assert np.isfinite(got).all()
     for l in range(L):
