@@ -68,6 +68,25 @@ class DecodeRun:
             self.attn_ws = api.sparse_attn_layers_split_workspace(self.params, cfg.readers, self.B,
                                                                   device=dev)
         qdt = torch.bfloat16 if cfg.quant else torch.float32
+        # Per-step inputs of every group live in one contiguous slot per prepared
+        # step (in_buf[k]) and the attention outputs of every group in one buffer per
+        # output slot (out_buf_all[k % out_slots]): a caller sends a step's inputs
+        # with one copy and reads its outputs back with one.
+        R, G, Bn = cfg.readers, cfg.groups, self.B
+        shapes = [("kv", (Bn, 1, D), torch.float32), ("gate", (Bn, 1, D), torch.float32)]
+        if R > 1:
+            shapes.append(("kv_rd", (Bn * (R - 1), 1, D), torch.float32))
+        shapes += [("q", (R, Bn, H, D), qdt), ("iq", (Bn, HI, DI // 2), torch.uint8),
+                   ("iw", (Bn, HI), torch.float32)]
+        layout, off = [], 0
+        for g in range(G):
+            for name, shp, dt in shapes:
+                nbytes = math.prod(shp) * torch.empty((), dtype=dt).element_size()
+                layout.append((g, name, shp, dt, off))
+                off += -(-nbytes // 256) * 256
+        self.slot_bytes = off
+        self.in_buf = torch.empty(self.n_prep, off, dtype=torch.uint8, device=dev)
+        self.out_buf_all = torch.empty(self.out_slots, G, R, Bn, H, D, dtype=qdt, device=dev)
         for g in range(cfg.groups):
             grp = {}
             grp["src"] = api.LayerCache(self.B, self.comp_caps, self.params, device=dev)
@@ -83,23 +102,23 @@ class DecodeRun:
             grp["bmax"] = torch.empty(self.B, self.n_b_max, dtype=torch.float32, device=dev)
             grp["idx"] = torch.empty(self.B, 512, dtype=torch.int32, device=dev)
             grp["n_sel"] = torch.empty(self.B, dtype=torch.int32, device=dev)
-            grp["out_buf"] = torch.empty(self.out_slots, cfg.readers, self.B, H, D, dtype=qdt,
-                                         device=dev)
+            grp["out_buf"] = self.out_buf_all[:, g]
             grp["out_all"] = grp["out_buf"][0]
             grp["out"] = list(grp["out_all"].unbind(0))
             grp["sink_all"] = torch.empty(cfg.readers, H, dtype=torch.float32, device=dev)
             grp["sink"] = list(grp["sink_all"].unbind(0))
-            # per-step inputs, resident before timing
-            grp["kv"] = torch.empty(self.n_prep, self.B, 1, D, dtype=torch.float32, device=dev)
-            grp["gate"] = torch.empty(self.n_prep, self.B, 1, D, dtype=torch.float32, device=dev)
-            if cfg.readers > 1:
-                grp["kv_rd"] = torch.empty(self.n_prep, self.B * (cfg.readers - 1), 1, D,
-                                           dtype=torch.float32, device=dev)
-            grp["q"] = torch.empty(self.n_prep, cfg.readers, self.B, H, D, dtype=qdt, device=dev)
-            grp["iq"] = torch.empty(self.n_prep, self.B, HI, DI // 2, dtype=torch.uint8, device=dev)
+            # per-step inputs, resident before timing: [n_prep, ...] views into in_buf
+            for gg, name, shp, dt, o in layout:
+                if gg != g:
+                    continue
+                es = torch.empty((), dtype=dt).element_size()
+                inner = [1]
+                for n in reversed(shp[1:]):
+                    inner.insert(0, inner[0] * n)
+                grp[name] = self.in_buf.view(dt).as_strided(
+                    (self.n_prep,) + shp, (off // es,) + tuple(inner), o // es)
             grp["iqs"] = torch.full((self.n_prep, self.B, HI, DI // 16), synth.E4M3_ONE,
                                     dtype=torch.uint8, device=dev)
-            grp["iw"] = torch.empty(self.n_prep, self.B, HI, dtype=torch.float32, device=dev)
             self.groups.append(grp)
         self._fill()
 
@@ -253,6 +272,11 @@ class DecodeRun:
         """Attention outputs [readers, B, H, D] written by the step of input slot k."""
         return grp["out_buf"][k % self.out_slots]
 
+    def outputs_of_slot(self, k):
+        """Attention outputs of every group [groups, readers, B, H, D] (contiguous)
+        written by the step of input slot k."""
+        return self.out_buf_all[k % self.out_slots]
+
     def _attn(self, s, grp, k, params):
         api, cfg, src = self.api, self.cfg, grp["src"]
         out_all = self.out_of_slot(grp, k)
@@ -322,18 +346,14 @@ class DecodeRun:
         self.step_done += 1
 
     def host_input_pairs(self, k):
-        """(pinned host copy, device slot view) of every per-step input of slot k, the
-        host copies filled from the device slot (the data a caller would send)."""
+        """(pinned host copy, device slot) pairs of the per-step inputs of slot k: one
+        pair, the whole contiguous slot in_buf[k] of every group's inputs, the host
+        copy filled from the device slot (the data a caller would send)."""
         torch = self.torch
-        pairs = []
-        for grp in self.groups:
-            for name in ("kv", "gate", "kv_rd", "q", "iq", "iw"):
-                if name in grp:
-                    d = grp[name][k]
-                    h = torch.empty(d.shape, dtype=d.dtype, pin_memory=True)
-                    h.copy_(d)
-                    pairs.append((h, d))
-        return pairs
+        d = self.in_buf[k]
+        h = torch.empty(d.shape, dtype=d.dtype, pin_memory=True)
+        h.copy_(d)
+        return [(h, d)]
 
     def pipelined_steps(self, K, host_in, host_out_of, stream):
         """K steps with every step's inputs sent from pinned host memory and its
@@ -341,10 +361,11 @@ class DecodeRun:
         steps' compute: step i+1's inputs travel on one side stream into their own
         prepared slot while step i computes on `stream`, and step i's outputs
         (double-buffered by slot parity; needs out_slots=2) travel back on another
-        while step i+1 computes (captured graphs when capture() ran, else eager). host_in: slot -> list of
-        (host, device) pairs (host_input_pairs); host_out_of(i): the pinned host
-        tensors, one per group, that receive step i's outputs. Everything is
-        enqueued; on return `stream` waits for every copy."""
+        while step i+1 computes (captured graphs when capture() ran, else eager).
+        host_in: slot -> list of (host, device) pairs (host_input_pairs);
+        host_out_of(i): the pinned host tensor shaped like outputs_of_slot(k) that
+        receives step i's outputs (one copy). Everything is enqueued; on return
+        `stream` waits for every copy."""
         torch = self.torch
         assert self.out_slots == 2, "needs out_slots=2"
         graphs = bool(getattr(self, "graphs", None))
@@ -381,8 +402,7 @@ class DecodeRun:
                     send(i + 1)
                 s_out.wait_event(comp_done[i])
                 with torch.cuda.stream(s_out):
-                    for h, grp in zip(host_out_of(i), self.groups):
-                        h.copy_(self.out_of_slot(grp, slot(i)), non_blocking=True)
+                    host_out_of(i).copy_(self.outputs_of_slot(slot(i)), non_blocking=True)
                 out_done[i].record(s_out)
         stream.wait_stream(s_in)
         stream.wait_stream(s_out)

@@ -152,8 +152,8 @@ def test_pipelined_steps_overlapped_copies_config1():
         for name in ("kv", "gate", "kv_rd", "q", "iq", "iw"):
             if name in grp:
                 grp[name].zero_()
-    outs = [[torch.empty(run.out_of_slot(grp, 0).shape, dtype=run.out_of_slot(grp, 0).dtype,
-                         pin_memory=True) for grp in run.groups] for _ in range(K)]
+    outs = [torch.empty(run.outputs_of_slot(0).shape, dtype=run.outputs_of_slot(0).dtype,
+                        pin_memory=True) for _ in range(K)]
     stream = torch.cuda.current_stream()
     run.pipelined_steps(K, host_in, lambda i: outs[i], stream)
     torch.cuda.synchronize()
