@@ -45,11 +45,12 @@ def peaks():
 
 
 # DRAM bytes per scanned position of k_index_scores_tc, from one ncu capture of
-# the decode workload B=32, T=131072 (151.44 MB read + 5.32 MB written over
-# 2,097,152 positions per launch). The figure belongs to that build of the
-# kernel: it is reported only while the kernel source hashes to the same value.
-INDEX_TRAFFIC_PER_POS = (151445248 + 6415872) / 2097152
-INDEX_TRAFFIC_SRC_SHA256 = "06c95577a96eae43f6d266a599e3c617f70e4360733bb4414bd15b00a2c3c1fc"
+# the decode workload B=32, T=131072 (151.45 MB read + 5.92 MB written over
+# 2,097,152 positions, the first timed launch). The figure belongs to that build
+# of the kernel: it is reported only while the kernel source hashes to the same
+# value.
+INDEX_TRAFFIC_PER_POS = (151449344 + 5915136) / 2097152
+INDEX_TRAFFIC_SRC_SHA256 = "191cae837b0ff48c6419cffea023057ffefe0cb3449b1a97e72ef66111c32d7d"
 
 
 def index_traffic(positions: float):
