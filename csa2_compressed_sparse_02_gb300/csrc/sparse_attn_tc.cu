@@ -62,7 +62,12 @@ struct AttnShared {
     float col_scale[2][64];   // per-head logit factor (softmax scale x log2 e / query scale), by unit parity
     float red_max[4][64];     // per lane quarter: the tile's maximum of each head
     float red_sum[4][64];     // per lane quarter: the sum over its 32 rows of each head
-    uint64_t q_full, q_empty, s_full, p_full, o_full, drain;
+    // q_full[it & 1] publishes the query (and col_scale) of piece it. Two barriers:
+    // a one-tile piece needs no softmax progress before its S completes, so the
+    // producers can publish the next piece's query before the softmax warps have
+    // waited on this one; on a single barrier two completed phases would read as
+    // none. (Only a CTA's first piece can be that short and have a successor.)
+    uint64_t q_full[2], q_empty, s_full, p_full, o_full, drain;
     uint64_t chunk_full[4], chunk_empty[4], red_max_bar[2], red_sum_bar[2];
     uint64_t soft_bar;  // the 8 softmax warps (merge of a cut unit)
     uint32_t tmem_base;
@@ -300,7 +305,7 @@ __device__ void producer_role(AttnShared& sh, const UnitArgs& a, int pt, int lan
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sh.q_full);
+        if (lane == 0) mbar_arrive(&sh.q_full[it & 1]);
 
         // ---- the 5 tiles: the 4 tiles of selected rows, then the window
         const int64_t n_c = T > 0 ? T / a.ratio : 0;
@@ -394,7 +399,7 @@ __device__ void mma_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, volat
     Piece pc;
     int it = 0, gt = 0;
     for (; pi.next(pc); ++it) {
-        if (!mbar_wait(&sh.q_full, (uint32_t)(it & 1), abort)) return;
+        if (!mbar_wait(&sh.q_full[it & 1], (uint32_t)((it >> 1) & 1), abort)) return;
         tc_fence_after();
         for (int j = pc.j0; j < pc.j1; ++j, ++gt) {
             // S^T = K . Q^T over the 512 dims, chunk pair by chunk pair as they land
@@ -477,7 +482,7 @@ __device__ void softmax_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, i
     int it = 0, gt = 0;
     uint32_t sync_n = 0;  // soft_sync phases used
     for (; has; ++it) {
-        if (!mbar_wait(&sh.q_full, (uint32_t)(it & 1), abort)) return;
+        if (!mbar_wait(&sh.q_full[it & 1], (uint32_t)((it >> 1) & 1), abort)) return;
         float m_run = -INFINITY;  // running maximum of head 32hh + lane
         float lpart[32];          // this row's share of the sum of P, head 32hh + i
 #pragma unroll
@@ -489,26 +494,29 @@ __device__ void softmax_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, i
             if (!mbar_wait(&sh.s_full, (uint32_t)(gt & 1), abort)) return;
             tc_fence_after();
             const float bias = valid ? 0.f : -INFINITY;
-            // warp maximum of every head (uniform in the warp), 8 heads at a time;
-            // lane 0 publishes this quarter's
+            // this row's 32 logits (log2 domain), read from TMEM once per tile and kept
+            // in registers for both passes
+            float x[32];
+            {
+                uint32_t sv[32];
+                tmem_ld_32x32b_x32(tl + kColS + 32 * hh, sv);
+                const float4* cs = reinterpret_cast<const float4*>(&sh.col_scale[it & 1][32 * hh]);
 #pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-                uint32_t sv[8];
-                tmem_ld_32x32b_x8(tl + kColS + 32 * hh + 8 * c8, sv);
-                const float4* cs = reinterpret_cast<const float4*>(&sh.col_scale[it & 1][32 * hh + 8 * c8]);
-                const float4 ca = cs[0], cb = cs[1];
-                const float4 ra = make_float4(warp_max(fmaf(__uint_as_float(sv[0]), ca.x, bias)),
-                                              warp_max(fmaf(__uint_as_float(sv[1]), ca.y, bias)),
-                                              warp_max(fmaf(__uint_as_float(sv[2]), ca.z, bias)),
-                                              warp_max(fmaf(__uint_as_float(sv[3]), ca.w, bias)));
-                const float4 rb = make_float4(warp_max(fmaf(__uint_as_float(sv[4]), cb.x, bias)),
-                                              warp_max(fmaf(__uint_as_float(sv[5]), cb.y, bias)),
-                                              warp_max(fmaf(__uint_as_float(sv[6]), cb.z, bias)),
-                                              warp_max(fmaf(__uint_as_float(sv[7]), cb.w, bias)));
-                if (lane == 0) {
-                    *reinterpret_cast<float4*>(&sh.red_max[qd][32 * hh + 8 * c8]) = ra;
-                    *reinterpret_cast<float4*>(&sh.red_max[qd][32 * hh + 8 * c8 + 4]) = rb;
+                for (int q4 = 0; q4 < 8; ++q4) {
+                    const float4 c = cs[q4];
+                    x[4 * q4] = fmaf(__uint_as_float(sv[4 * q4]), c.x, bias);
+                    x[4 * q4 + 1] = fmaf(__uint_as_float(sv[4 * q4 + 1]), c.y, bias);
+                    x[4 * q4 + 2] = fmaf(__uint_as_float(sv[4 * q4 + 2]), c.z, bias);
+                    x[4 * q4 + 3] = fmaf(__uint_as_float(sv[4 * q4 + 3]), c.w, bias);
                 }
+            }
+            // warp maximum of every head (uniform in the warp); lane 0 publishes this
+            // quarter's
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+                const float4 m4 = make_float4(warp_max(x[4 * q4]), warp_max(x[4 * q4 + 1]),
+                                              warp_max(x[4 * q4 + 2]), warp_max(x[4 * q4 + 3]));
+                if (lane == 0) *reinterpret_cast<float4*>(&sh.red_max[qd][32 * hh + 4 * q4]) = m4;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.red_max_bar[hh]);
@@ -525,20 +533,13 @@ __device__ void softmax_role(AttnShared& sh, const UnitArgs& a, uint32_t tmem, i
 #pragma unroll
                 for (int i = 0; i < 32; ++i) lpart[i] *= __shfl_sync(0xffffffffu, alpha, i);
             }
-            // P = 2^(x - m) in four chunks of 8 heads (one 16-byte unit of the P row
-            // each), read again from TMEM: keeps the working set small
+            // P = 2^(x - m), one 16-byte unit of the P row per 8 heads
 #pragma unroll
             for (int c8 = 0; c8 < 4; ++c8) {
-                uint32_t sv[8];
-                tmem_ld_32x32b_x8(tl + kColS + 32 * hh + 8 * c8, sv);
-                const float4* cs = reinterpret_cast<const float4*>(&sh.col_scale[it & 1][32 * hh + 8 * c8]);
-                const float4 ca = cs[0], cb = cs[1];
-                const float cc[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
                 float pv[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    pv[e] = ex2(fmaf(__uint_as_float(sv[e]), cc[e], bias) -
-                                __shfl_sync(0xffffffffu, mfix, 8 * c8 + e));
+                    pv[e] = ex2(x[8 * c8 + e] - __shfl_sync(0xffffffffu, mfix, 8 * c8 + e));
                     lpart[8 * c8 + e] += pv[e];
                 }
                 *reinterpret_cast<uint4*>(sh.p + sw128(r, 4 * hh + c8)) =
@@ -688,7 +689,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_sparse_attn_tc(UnitArgs a) 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int* abort = &sh.abort;
     if (tid == 0) {
-        mbar_init(&sh.q_full, kProdWarps);
+        mbar_init(&sh.q_full[0], kProdWarps);
+        mbar_init(&sh.q_full[1], kProdWarps);
         mbar_init(&sh.q_empty, 1);
         mbar_init(&sh.s_full, 1);
         mbar_init(&sh.p_full, kSoftWarps);

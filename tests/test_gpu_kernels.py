@@ -430,12 +430,14 @@ def test_sparse_attn_out_of_range_index_is_skipped_and_flagged():
 
 # How the fused reader attention is launched: (mma_sync, split, max_ctas). The
 # split modes cut the (unit, tile) work into equal ranges per CTA; max_ctas caps
-# the grid so that ranges cut units at many different tiles.
+# the grid so that ranges cut units at many different tiles. With 13 CTAs both
+# tests below have ranges that open on a one-tile piece (the window tile alone)
+# followed by more pieces (boundaries at 24 and 64 of 105 items, 369 of 960).
 LAYER_MODES = {
     "tcgen05": (False, False, 0),
     "tcgen05_split": (False, True, 0),
     "tcgen05_split_4ctas": (False, True, 4),
-    "tcgen05_split_7ctas": (False, True, 7),
+    "tcgen05_split_13ctas": (False, True, 13),
     "mma_sync": (True, False, 0),
 }
 
