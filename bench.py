@@ -18,6 +18,7 @@ on a bounded sample of the same workload on the host cores.
 from __future__ import annotations
 
 import argparse
+import faulthandler
 import json
 import math
 import os
@@ -34,6 +35,14 @@ sys.path.insert(0, ROOT)
 METRIC = "CSA2 decode query-tok/s at 1M ctx, batch 32; indexer+attn HBM GB/s vs roofline"
 UNIT = "query-tok/s"
 
+
+
+_T0 = time.time()
+
+
+def phase(msg):
+    """Progress marker on stderr (the JSON line stays the only stdout output)."""
+    print("[bench %7.1fs] %s" % (time.time() - _T0, msg), file=sys.stderr, flush=True)
 
 def peaks():
     try:
@@ -223,6 +232,7 @@ def main():
     ap.add_argument("--chunk", type=int, default=0,
                     help="configuration 4 only: queries in the prefill chunk (default 8192)")
     args = ap.parse_args()
+    faulthandler.enable()  # a crash prints every thread's Python stack to stderr
     args.warmup = max(3, args.warmup)
 
     rank = int(os.environ.get("RANK", "0"))
@@ -259,6 +269,7 @@ def main():
 
     K, Wm = args.steps, args.warmup
     e2e_steps = 0 if args.no_e2e else K
+    phase("filling configuration %d" % args.config)
     run = workloads.DecodeRun(cfg, n_steps=Wm + 2 + K + e2e_steps + 5, out_slots=2,
                               split_attention=not args.whole_unit_attn)
     stream = torch.cuda.current_stream()
@@ -269,12 +280,14 @@ def main():
     torch.cuda.synchronize()
     mode = "eager"
     if not args.eager:
+        phase("warm-up done; capturing graphs")
         if run.capture(with_timers=True):
             mode = "cuda-graph"
             for _ in range(2):
                 run.step_graph()
             torch.cuda.synchronize()
     advance = run.step_graph if mode == "cuda-graph" else None
+    phase("%s ready; timed steps" % mode)
     uuid = None
     try:
         uuid = str(torch.cuda.get_device_properties(dev).uuid)
@@ -331,6 +344,7 @@ def main():
     # ---------------- end to end through the public API with host buffers
     e2e = None
     if e2e_steps:
+        phase("timed steps done; end-to-end steps")
         e2e = run_e2e(run, e2e_steps, stream, barrier)
 
     line = {
@@ -364,6 +378,7 @@ def main():
     if e2e:
         line["e2e"] = e2e
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        phase("oracle baseline on the host cores")
         line["cpu_baseline"] = cpu_baseline(cfg)
     if rank == 0:
         print(json.dumps(line), flush=True)
