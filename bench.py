@@ -38,6 +38,7 @@ UNIT = "query-tok/s"
 
 
 _T0 = time.time()
+_TRACE = None  # pinned launch-trace record (csa2_trace_attach), read after an error
 
 
 def phase(msg):
@@ -269,6 +270,9 @@ def main():
 
     K, Wm = args.steps, args.warmup
     e2e_steps = 0 if args.no_e2e else K
+    global _TRACE
+    from csa2_compressed_sparse_02_gb300 import api as _api
+    _TRACE = _api.trace_attach()
     phase("filling configuration %d" % args.config)
     run = workloads.DecodeRun(cfg, n_steps=Wm + 2 + K + e2e_steps + 5, out_slots=2,
                               split_attention=not args.whole_unit_attn)
@@ -450,19 +454,42 @@ def run_e2e(run, K, stream, barrier):
     h2d = sum(h.numel() * h.element_size() for h, _ in host_in[slots[0]])
     d2h = host_out.numel() * host_out.element_size()
     torch.cuda.synchronize()
+    # the link as this process sees it: one slot's copies alone, each way
+    link = {}
+    for name, fn in (("h2d_gbs", lambda: [d.copy_(h, non_blocking=True) for h, d in host_in[slots[0]]]),
+                     ("d2h_gbs", lambda: host_out.copy_(run.outputs_of_slot(0), non_blocking=True))):
+        fn()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(3):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        link[name] = 3 * (h2d if name == "h2d_gbs" else d2h) / (a.elapsed_time(b) / 1e3) / 1e9
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     start.record(stream)
+    t_host = time.perf_counter()
     run.pipelined_steps(K, host_in, lambda i: host_out, stream)
+    t_host = time.perf_counter() - t_host
     end.record(stream)
     torch.cuda.synchronize()
     barrier()
     el = start.elapsed_time(end) / 1000.0
+    phase("end-to-end: %.3f ms per step (host enqueue %.3f ms per step); copies alone "
+          "%.0f GB/s in, %.0f GB/s out" % (1e3 * el / K, 1e3 * t_host / K, link["h2d_gbs"],
+                                           link["d2h_gbs"]))
     return {"value": run.cfg.B * K / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h,
+            "d2h_bytes_per_step": d2h, "link_gbs": link,
             "overlap": "inputs of step i+1 and outputs of step i copied on side streams "
                        "while step i (resp. i+1) computes; one contiguous copy each way per step"}
 
 
 if __name__ == "__main__":
-    main()
+    try:
+        main()
+    except Exception:
+        if _TRACE is not None:  # which kernel launch was running when the error came
+            from csa2_compressed_sparse_02_gb300 import api as _api
+            print("[bench] " + _api.trace_read(_TRACE), file=sys.stderr, flush=True)
+        raise

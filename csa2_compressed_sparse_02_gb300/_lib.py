@@ -35,6 +35,7 @@ PP = ctypes.POINTER(Params)
 SIGNATURES = {
     "csa2_default_params": (None, [PP]),
     "csa2_version": (I32, []),
+    "csa2_trace_attach": (I32, [P]),
     "csa2_last_error": (ctypes.c_char_p, []),
     "csa2_compress_append": (I32, [PP, I32, I32, P, P, P, P, P, P, P, P, P, P, P]),
     "csa2_nvfp4_quantize": (I32, [P, I64, I32, P, P, P]),

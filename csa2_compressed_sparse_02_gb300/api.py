@@ -37,6 +37,26 @@ def version() -> int:
     return lib().csa2_version()
 
 
+TRACE_KERNELS = {0: "none", 1: "compress_append", 2: "index_scores", 3: "select_topk",
+                 4: "sparse_attn_layers"}
+
+
+def trace_attach():
+    """Attach a zeroed pinned record to the library's launch trace (csa2_trace_attach)
+    and return it; read it with trace_read() after an error."""
+    rec = torch.zeros(4, dtype=torch.int32, pin_memory=True)
+    check(lib().csa2_trace_attach(ctypes.c_void_p(rec.data_ptr())), "trace_attach")
+    return rec
+
+
+def trace_read(rec) -> str:
+    """The trace record as text: the last launch that started and the last whose
+    first CTA finished."""
+    v = [int(x) for x in rec.tolist()]
+    return "last launch started: %s #%d; last first-CTA finish: %s #%d" % (
+        TRACE_KERNELS.get(v[0], str(v[0])), v[1], TRACE_KERNELS.get(v[2], str(v[2])), v[3])
+
+
 def _ptr(t):
     if t is None:
         return None

@@ -64,6 +64,15 @@ extern "C" void csa2_default_params(csa2_params* p) {
     p->max_ctas = 0;
 }
 
+extern "C" int csa2_trace_attach(int32_t* record) {
+    cudaError_t (*setters[])(int32_t*) = {csa2::trace_set_compress, csa2::trace_set_index,
+                                          csa2::trace_set_select, csa2::trace_set_attn_tc};
+    if (const int rc = csa2::ensure_loaded()) return rc;
+    for (auto f : setters)
+        if (f(record) != cudaSuccess) return csa2::check_launch("trace_attach");
+    return CSA2_OK;
+}
+
 extern "C" int csa2_version(void) { return 200; }
 
 extern "C" const char* csa2_last_error(void) { return csa2::g_last_error.c_str(); }

@@ -55,6 +55,43 @@ cudaError_t preload_select();
 cudaError_t preload_attn();
 cudaError_t preload_attn_tc();
 
+// ---- launch trace (diagnostics; off unless csa2_trace_attach set a record).
+// Every translation unit has its own copy of the record pointer. When set, CTA 0
+// thread 0 of the traced kernels writes {kernel id, launch number} into record
+// words 0-1 at its start and into words 2-3 when it finishes: plain posted stores
+// to host-mapped memory (no fence: nothing waits for them), which the host can
+// read after an error has ended the context.
+enum TraceKernel { kTraceCompress = 1, kTraceIndex = 2, kTraceSelect = 3, kTraceAttn = 4 };
+namespace {
+__device__ int32_t* g_trace = nullptr;
+__device__ int32_t g_trace_seq = 0;
+}  // namespace
+__device__ __forceinline__ bool trace_lead() {
+    return blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0;
+}
+__device__ __forceinline__ void trace_start(int id) {
+    volatile int32_t* t = g_trace;
+    if (t && trace_lead()) {
+        const int32_t n = ++g_trace_seq;
+        t[1] = n;
+        t[0] = id;
+    }
+}
+__device__ __forceinline__ void trace_end(int id) {
+    volatile int32_t* t = g_trace;
+    if (t && trace_lead()) {
+        t[3] = g_trace_seq;
+        t[2] = id;
+    }
+}
+// Sets this translation unit's record pointer (NULL detaches).
+#define CSA2_TRACE_SETTER(fn) \
+    cudaError_t fn(int32_t* rec) { return cudaMemcpyToSymbol(g_trace, &rec, sizeof(rec)); }
+cudaError_t trace_set_compress(int32_t* rec);
+cudaError_t trace_set_index(int32_t* rec);
+cudaError_t trace_set_select(int32_t* rec);
+cudaError_t trace_set_attn_tc(int32_t* rec);
+
 // Raise a status bit on the device (NULL status pointer = ignore).
 __device__ __forceinline__ void raise_status(int32_t* st, int bit) {
     if (st) atomicOr(st, bit);

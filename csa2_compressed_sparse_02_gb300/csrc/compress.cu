@@ -56,6 +56,7 @@ k_compress_append(int n_new, const float* __restrict__ kv_new, const float* __re
                   uint8_t* const* comp_scales, const int64_t* comp_cap, void* const* win,
                   int32_t* n_tokens, int advance_here, int32_t* dev_status) {
     const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
+    trace_start(kTraceCompress);
     const int ch = 4 * tid;
     const int64_t T = n_tokens[b];
     if (T < 0) {
@@ -133,6 +134,7 @@ k_compress_append(int n_new, const float* __restrict__ kv_new, const float* __re
         __syncthreads();
         if (tid == 0) n_tokens[b] = (int32_t)(T + n_new);
     }
+    trace_end(kTraceCompress);
 }
 
 __global__ void k_advance(int32_t* n_tokens, int B, int n_new) {
@@ -176,6 +178,8 @@ k_window_linear(int n_new, const float* __restrict__ kv_new, const void* const* 
 }
 
 }  // namespace
+
+CSA2_TRACE_SETTER(trace_set_compress)
 
 cudaError_t preload_compress() {
     cudaError_t (*l[])() = {

@@ -217,6 +217,7 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
     TcShared& sh = *reinterpret_cast<TcShared*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int* abort = &sh.abort;
+    trace_start(kTraceIndex);
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -424,6 +425,7 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    trace_end(kTraceIndex);
 }
 
 constexpr int kTcSmem = (int)sizeof(TcShared) + 1024;
@@ -456,6 +458,8 @@ int check_index_args(const csa2_params* p, int B, int64_t max_ncomp, const void*
 }
 
 }  // namespace
+
+CSA2_TRACE_SETTER(trace_set_index)
 
 cudaError_t preload_index() {
     cudaError_t e = preload_kernel(k_index_keys_write);

@@ -329,6 +329,7 @@ k_select_topk(int64_t max_ncomp, int ratio, const float* __restrict__ scores,
     extern __shared__ __align__(16) unsigned char smem_raw[];
     SelShared& sh = *reinterpret_cast<SelShared*>(smem_raw);
     const int b = blockIdx.x, tid = threadIdx.x;
+    trace_start(kTraceSelect);
     int64_t n_c64 = n_tokens[b] / ratio;
     if (n_c64 > max_ncomp || n_c64 < 0) {
         if (tid == 0) raise_status(dev_status, CSA2_DEV_BAD_LENGTH);
@@ -458,9 +459,12 @@ k_select_topk(int64_t max_ncomp, int ratio, const float* __restrict__ scores,
         }
     }
     if (tid == 0 && n_sel_out) n_sel_out[b] = min(n_cand, kKp);
+    trace_end(kTraceSelect);
 }
 
 }  // namespace
+
+CSA2_TRACE_SETTER(trace_set_select)
 
 cudaError_t preload_select() { return preload_kernel(k_select_topk, (int)sizeof(SelShared)); }
 

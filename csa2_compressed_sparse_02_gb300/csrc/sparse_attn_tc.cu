@@ -688,6 +688,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_sparse_attn_tc(UnitArgs a) 
     AttnShared& sh = *reinterpret_cast<AttnShared*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int* abort = &sh.abort;
+    trace_start(kTraceAttn);
     if (tid == 0) {
         mbar_init(&sh.q_full[0], kProdWarps);
         mbar_init(&sh.q_full[1], kProdWarps);
@@ -735,6 +736,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_sparse_attn_tc(UnitArgs a) 
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+    trace_end(kTraceAttn);
 }
 
 int sm_count(int dev) {
@@ -840,6 +842,8 @@ int launch_layers(const char* name, const csa2_params* p, int L, int B, int b0, 
 }
 
 }  // namespace
+
+CSA2_TRACE_SETTER(trace_set_attn_tc)
 
 cudaError_t preload_attn_tc() { return preload_kernel(k_sparse_attn_tc, kAttnSmem); }
 

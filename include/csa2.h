@@ -97,6 +97,21 @@ typedef struct csa2_params {
  * NVFP4 cache, E4M3 window, bf16 query, 1/sqrt(512), ring window). */
 void csa2_default_params(csa2_params* p);
 
+/*
+ * csa2_trace_attach — launch trace for diagnosing device errors. (No counterpart
+ * in the pages.) record: NULL (off, the default) or a device-accessible pointer
+ * to 4 int32, normally pinned host memory (with unified addressing the host
+ * pointer is the device pointer), zero-filled by the caller. While attached,
+ * one thread of each compress_append, index_scores (tcgen05), select_topk and
+ * sparse_attn_layers* launch stores {kernel id, launch number} into words 0-1 when
+ * the launch starts and into words 2-3 when its first CTA finishes (ids: 1
+ * compress, 2 index, 3 select, 4 attention; launch numbers count per kernel).
+ * After an error has ended the CUDA context the host can still read the record:
+ * words 0-1 name the last launch that started. Applies to the current device;
+ * returns CSA2_OK or CSA2_ERR_CUDA.
+ */
+int csa2_trace_attach(int32_t* record);
+
 /* Library ABI version (major*10000 + minor*100 + patch). */
 int csa2_version(void);
 

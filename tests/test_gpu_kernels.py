@@ -594,3 +594,30 @@ def test_sparse_attn_layers_rescale_and_many_units(mode):
                                      comp_scales=comp_s[b], idx=keep)
             ok, e = close_bf16(got[l, b], ref)
             assert ok, (l, b, T, e)
+
+
+def test_launch_trace_names_the_last_launch():
+    """csa2_trace_attach: after a selection launch the host-mapped record names it
+    (started and first-CTA-finished), without a synchronising read of device
+    memory; detaching stops the stores."""
+    p = api.default_params()
+    B, n_c = 2, 300
+    rng = np.random.default_rng(5)
+    scores = t(rng.standard_normal((B, 320)).astype(np.float32))
+    bmax = torch.full((B, 40), -1.0, device=DEV)
+    bmax[:, :38] = t(rng.standard_normal((B, 38)).astype(np.float32))
+    n_tok = t(np.full(B, 2 * n_c, np.int32))
+    idx = torch.empty(B, 512, dtype=torch.int32, device=DEV)
+    rec = api.trace_attach()
+    try:
+        api.select_topk(p, 320, scores, bmax, n_tok, idx)
+        torch.cuda.synchronize()
+        v = [int(x) for x in rec.tolist()]
+        assert v[0] == 3 and v[2] == 3 and v[1] >= 1 and v[3] == v[1], v
+        assert "select_topk" in api.trace_read(rec)
+    finally:
+        api.check(api.lib().csa2_trace_attach(None), "trace detach")
+    before = [int(x) for x in rec.tolist()]
+    api.select_topk(p, 320, scores, bmax, n_tok, idx)
+    torch.cuda.synchronize()
+    assert [int(x) for x in rec.tolist()] == before
