@@ -295,18 +295,26 @@ class DecodeRun:
                             src.comp_ptrs, src.comp_scale_ptrs, grp["idx"], out_all[r],
                             self.workspace, self.dev_status, s)
 
-    def _enqueue(self, k, stream=None, timers=None):
+    def _enqueue(self, k, stream=None, timers=None, timer_cats=None, timer_groups=None):
         """Enqueue one decode step (every group, every layer) using input slot k.
         timers: optional dict receiving (start, end) CUDA events per call category
-        ("compress", "index", "select", "attn"), recorded on the launching stream.
-        Groups run in layer order: group g+1's index query comes from the hidden
-        state after group g's layers, so its scan cannot start earlier."""
+        ("compress", "index", "select", "attn"), recorded on the launching stream;
+        timer_cats / timer_groups restrict the events to those categories / group
+        indices (None: all). Groups run in layer order: group g+1's index query
+        comes from the hidden state after group g's layers, so its scan cannot
+        start earlier."""
         st = self.torch.cuda.current_stream() if stream is None else stream
-        for grp in self.groups:
-            self._timed(timers, "compress", st, self._compress, grp, k)
-            self._timed(timers, "index", st, self._index, grp, k, self.params)
-            self._timed(timers, "select", st, self._select, grp, k)
-            self._timed(timers, "attn", st, self._attn, grp, k, self.params)
+
+        def tm(cat, g):
+            keep = timers is not None and (timer_cats is None or cat in timer_cats) and (
+                timer_groups is None or g in timer_groups)
+            return timers if keep else None
+
+        for g, grp in enumerate(self.groups):
+            self._timed(tm("compress", g), "compress", st, self._compress, grp, k)
+            self._timed(tm("index", g), "index", st, self._index, grp, k, self.params)
+            self._timed(tm("select", g), "select", st, self._select, grp, k)
+            self._timed(tm("attn", g), "attn", st, self._attn, grp, k, self.params)
 
     def step(self, stream=None, timers=None):
         """Enqueue the next decode step eagerly (one launch per kernel)."""
@@ -314,10 +322,22 @@ class DecodeRun:
         self._enqueue(self.step_done % self.n_prep, stream, timers)
         self.step_done += 1
 
-    def capture(self, with_timers=False):
-        """Capture one CUDA graph per prepared input slot (a whole step each).
+    def capture(self, with_timers=False, timer_cats=None, timer_groups=None):
+        """Capture one CUDA graph per prepared input slot (a whole step each) as the
+        graphs step_graph() replays. Timing events (with_timers; restricted by
+        timer_cats / timer_groups as in _enqueue) are recorded inside the graphs:
+        each one orders the kernels around it fully, so they cost step time.
         Returns False if the timers were requested but this torch cannot record
         events inside a graph."""
+        got = self.capture_set(with_timers, timer_cats, timer_groups)
+        if got is None:
+            return False
+        self.graphs, self.graph_timers = got
+        return True
+
+    def capture_set(self, with_timers=False, timer_cats=None, timer_groups=None):
+        """Capture a set of per-slot step graphs without installing it: returns
+        (graphs, timers per graph), or None if events cannot be recorded in a graph."""
         torch = self.torch
         self._external_events = False
         if with_timers:
@@ -325,19 +345,19 @@ class DecodeRun:
                 torch.cuda.Event(enable_timing=True, external=True)
                 self._external_events = True
             except TypeError:
-                return False
-        self.graphs, self.graph_timers = [], []
+                return None
+        graphs, graph_timers = [], []
         cs = torch.cuda.Stream()
         cs.wait_stream(torch.cuda.current_stream())
         for k in range(self.n_prep):
             g = torch.cuda.CUDAGraph()
             tm = {} if with_timers else None
             with torch.cuda.graph(g, stream=cs):
-                self._enqueue(k, None, tm)
-            self.graphs.append(g)
-            self.graph_timers.append(tm)
+                self._enqueue(k, None, tm, timer_cats, timer_groups)
+            graphs.append(g)
+            graph_timers.append(tm)
         torch.cuda.current_stream().wait_stream(cs)
-        return True
+        return graphs, graph_timers
 
     def step_graph(self):
         """Replay the captured step of the next input slot on the current stream."""
