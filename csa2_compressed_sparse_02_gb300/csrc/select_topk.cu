@@ -19,9 +19,11 @@
 // count falls outside [2,047, kMaxFiltered] the threshold moves, and after a
 // few tries the exact select runs over all blocks in global memory.
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace csa2 {
 namespace {
+using namespace sm100;
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
@@ -330,6 +332,8 @@ k_select_topk(int64_t max_ncomp, int ratio, const float* __restrict__ scores,
     SelShared& sh = *reinterpret_cast<SelShared*>(smem_raw);
     const int b = blockIdx.x, tid = threadIdx.x;
     trace_start(kTraceSelect);
+    // the attention after it may be scheduled now (it waits for this grid first)
+    grid_dep_launch_dependents();
     int64_t n_c64 = n_tokens[b] / ratio;
     if (n_c64 > max_ncomp || n_c64 < 0) {
         if (tid == 0) raise_status(dev_status, CSA2_DEV_BAD_LENGTH);

@@ -135,6 +135,17 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
 
+// ---- programmatic dependent launch ----
+// A kernel launched with programmatic stream serialization may start while the
+// kernel before it on the stream still runs; grid_dep_wait() returns once that
+// kernel has completed and its memory operations are visible (immediately when
+// the launch had no such attribute). grid_dep_launch_dependents() lets the next
+// kernel of the stream, if launched that way, start before this one completes.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 // ---- tensor memory ----
 // The tcgen05 alloc / dealloc / ld / st / wait instructions are .sync.aligned: every
 // lane of the warp must execute the same instruction, converged. A bounded wait

@@ -713,6 +713,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) k_sparse_attn_tc(UnitArgs a) 
         tmem_alloc(&sh.tmem_base, kTmemCols);
         tmem_relinquish();
     }
+    // Launched programmatically, the kernel before this one on the stream may still
+    // be running: only the setup above (barriers, TMEM) overlaps it; every global
+    // read comes after this wait.
+    grid_dep_wait();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -837,7 +841,20 @@ int launch_layers(const char* name, const csa2_params* p, int L, int B, int b0, 
     int64_t sms = sm_count(dev);
     if (p->max_ctas > 0 && p->max_ctas < sms) sms = p->max_ctas;
     const int grid = (int)(units < sms ? units : sms);
-    k_sparse_attn_tc<<<grid, kAttnThreads, kAttnSmem, static_cast<cudaStream_t>(stream)>>>(a);
+    // Programmatic launch: the CTAs may start while the kernel before it on the
+    // stream still runs and do their setup (barriers, TMEM) on free SMs; the kernel
+    // waits for that grid (grid_dep_wait) before any global read or write.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = kAttnSmem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, k_sparse_attn_tc, a) != cudaSuccess) return check_launch(name);
     return check_launch(name);
 }
 
