@@ -275,6 +275,10 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
         // ---------------- loader: query slots per sequence, super-tiles per stage
         int seg = -1, b = 0, prev_b = -1;
         int64_t issued = 0;
+        // the key stream (72 B per position, far larger than L2) is read once: its
+        // lines go first, so the scores and block maxima written here are still in
+        // L2 when the selection reads them
+        const uint64_t key_policy = l2_policy_evict_first();
         for (int64_t f = f0; f < f1; ++f) {
             b = advance_seq(sh, b, f);
             const int64_t g = f - sh.prefix[b];
@@ -304,7 +308,8 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
             if (lane == 0) {
                 const uint32_t bytes = (uint32_t)tiles_in(g, sh.ncomp[b]) * kKeyTileBytes;
                 mbar_arrive_expect_tx(&sh.full[s], bytes);
-                bulk_g2s(sh.stage[s], key_cache[b] + g * kStageBytes, bytes, &sh.full[s]);
+                bulk_g2s_hint(sh.stage[s], key_cache[b] + g * kStageBytes, bytes, &sh.full[s],
+                              key_policy);
             }
             __syncwarp();
             issued = i + 1;
