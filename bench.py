@@ -55,12 +55,12 @@ def peaks():
 
 
 # DRAM bytes per scanned position of k_index_scores_tc, from one ncu capture of
-# the decode workload B=32, T=131072 (151.45 MB read + 5.92 MB written over
+# the decode workload B=32, T=131072 (151.41 MB read + 4.11 MB written over
 # 2,097,152 positions, the first timed launch). The figure belongs to that build
 # of the kernel: it is reported only while the kernel source hashes to the same
 # value.
-INDEX_TRAFFIC_PER_POS = (151449344 + 5915136) / 2097152
-INDEX_TRAFFIC_SRC_SHA256 = "191cae837b0ff48c6419cffea023057ffefe0cb3449b1a97e72ef66111c32d7d"
+INDEX_TRAFFIC_PER_POS = (151413504 + 4113664) / 2097152
+INDEX_TRAFFIC_SRC_SHA256 = "26bc7cbf6e093d36dcf88583f4f70985bbe400d91743146887e009ffa777b3c7"
 
 
 def index_traffic(positions: float):
