@@ -6,8 +6,10 @@
 // 512-d KV head so K = V = the latent, §四 reader layers share the source
 // layer's compressed cache and selection).
 //
-// Work unit: one (layer, sequence); a persistent CTA per SM walks its units.
-// The 640 positions are 5 tiles of 128 (tiles 0..3 = idx[0..512) in 128s, tile
+// Work unit: one (layer, sequence); a persistent CTA per SM walks its units
+// round robin, or (with a workspace) an equal contiguous range of (unit, tile)
+// items, a unit cut by a range boundary being merged by log-sum-exp (see the
+// schedule below). The 640 positions are 5 tiles of 128 (tiles 0..3 = idx[0..512) in 128s, tile
 // 4 = the window ring: a unit opens on gathered rows, one round trip away, and
 // the window's two rounds of loads overlap tile 3). Per tile, with the
 // positions as the MMA's M:
