@@ -41,6 +41,18 @@ _T0 = time.time()
 _TRACE = None  # pinned launch-trace record (csa2_trace_attach), read after an error
 
 
+def max_over_ranks(x, dist=None, device="cpu"):
+    """The largest value of x over the ranks of the process group (x itself
+    without one): the whole-job time of weakly scaled replicas is the slowest
+    rank's."""
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def phase(msg):
     """Progress marker on stderr (the JSON line stays the only stdout output)."""
     print("[bench %7.1fs] %s" % (time.time() - _T0, msg), file=sys.stderr, flush=True)
@@ -325,11 +337,7 @@ def main():
         torch.cuda.synchronize()
         barrier()
     clocks = clk.summary()
-    elapsed = start.elapsed_time(end) / 1000.0
-    if dist is not None:
-        t = torch.tensor([elapsed], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed = float(t.item())
+    elapsed = max_over_ranks(start.elapsed_time(end) / 1000.0, dist, dev)
     assert int(run.dev_status.item()) == 0, "device status %d" % int(run.dev_status.item())
     step_s = elapsed / K
     value = world * cfg.B * K / elapsed
@@ -376,7 +384,7 @@ def main():
     e2e = None
     if e2e_steps:
         phase("timed steps done; end-to-end steps")
-        e2e = run_e2e(run, e2e_steps, stream, barrier)
+        e2e = run_e2e(run, e2e_steps, stream, barrier, lambda x: max_over_ranks(x, dist, dev), world)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
@@ -468,7 +476,7 @@ def prefill_main(args):
         "clocks": clk.summary(), "gpu_launches": None}), flush=True)
 
 
-def run_e2e(run, K, stream, barrier):
+def run_e2e(run, K, stream, barrier, over_ranks=lambda x: x, world=1):
     """Same steps through the public API with every step's inputs copied from pinned
     host memory and its attention outputs copied back, inside the timed region
     (DecodeRun.pipelined_steps: the copies overlap the neighbouring steps' compute;
@@ -505,11 +513,11 @@ def run_e2e(run, K, stream, barrier):
     end.record(stream)
     torch.cuda.synchronize()
     barrier()
-    el = start.elapsed_time(end) / 1000.0
+    el = over_ranks(start.elapsed_time(end) / 1000.0)
     phase("end-to-end: %.3f ms per step (host enqueue %.3f ms per step); copies alone "
           "%.0f GB/s in, %.0f GB/s out" % (1e3 * el / K, 1e3 * t_host / K, link["h2d_gbs"],
                                            link["d2h_gbs"]))
-    return {"value": run.cfg.B * K / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
+    return {"value": world * run.cfg.B * K / el, "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "link_gbs": link,
             "overlap": "inputs of step i+1 and outputs of step i copied on side streams "
                        "while step i (resp. i+1) computes; one contiguous copy each way per step"}
