@@ -14,7 +14,7 @@
 // per lane (32 heads), apply ReLU and the head weights, and reduce the block
 // maximum over 8 adjacent lanes. One persistent CTA per SM; warps 0-7 epilogue
 // (two warpgroups taking alternate super-tiles), warp 8 loads (one bulk copy
-// per super-tile of 4 tiles into a 5-stage ring), warps 9 and 10 issue the
+// per super-tile of 5 tiles into a 4-stage ring), warps 9 and 10 issue the
 // MMAs of alternate super-tiles (a single issuing thread serialises each scale
 // copy with its MMA; two overlap them), each into its own TMEM accumulators.
 //
@@ -159,14 +159,27 @@ k_index_scores_cc(int64_t max_ncomp, int ratio, const uint8_t* __restrict__ q_va
 
 // ------------------------------------------------------------------ tensor-core build
 // Unit of work: a super-tile of up to kTilesPerStage consecutive tiles of one sequence
-// (contiguous in the cache, so one bulk copy of up to 36 KB). Per super-tile the
+// (contiguous in the cache, so one bulk copy of up to 45 KB). Per super-tile the
 // MMA thread issues 2 scale copies + 2 MMAs per tile into the tile's own TMEM
 // accumulator, then one commit for the stage and one for the epilogue: the
-// fixed per-commit and per-copy costs are paid once per 36 KB, not per 9 KB.
-constexpr int kTilesPerStage = 4;
-constexpr int kStageBytes = kTilesPerStage * kKeyTileBytes;  // 36,864 = 36 x 1024
-constexpr int kStages = 5;
+// fixed per-commit, per-copy and per-handoff costs are paid once per 45 KB, not
+// per 9 KB. Those costs, not the bytes in flight, set the rate: at 1 M context
+// (1.28 GB per launch) super-tiles of 2 / 3 / 4 / 5 tiles in 10 / 7 / 5 / 4
+// stages took 0.256 / 0.227 / 0.205 / 0.203 ms (6 tiles in 3 stages: 0.201 ms,
+// but an odd ring breaks the issuers' barrier protocol, below).
+constexpr int kTilesPerStage = 5;
+constexpr int kStageBytes = kTilesPerStage * kKeyTileBytes;  // 46,080 = 45 x 1024
+constexpr int kStages = 4;
 constexpr int kIssuers = 2;      // MMA-issuing warps, alternating super-tiles
+// Each issuer waits only for the stage fills of its own super-tiles. A parity
+// wait is exact only if the phase before the awaited one has completed, i.e.
+// the waiter saw the stage's previous fill itself: so every use of a stage must
+// belong to the same issuer, which needs kStages to be a multiple of kIssuers.
+// With an odd ring a stage alternates between the issuers, and an issuer whose
+// previous fill of that stage (the other issuer's copy) was still in flight
+// read the preceding phase as the awaited one and went ahead on a stage being
+// filled; its commit then freed the stage once too often.
+static_assert(kStages % kIssuers == 0, "every use of a stage must belong to one issuer");
 constexpr int kAcc = kIssuers;   // one super-tile accumulator set per issuer
 constexpr int kEpiGroups = 2;    // epilogue warpgroups, alternating super-tiles
 constexpr int kLoadWarp = 4 * kEpiGroups, kMmaWarp = kLoadWarp + 1;
@@ -197,6 +210,46 @@ __device__ __forceinline__ int advance_seq(const TcShared& sh, int b, int64_t f)
     while (f >= sh.prefix[b + 1]) ++b;
     return b;
 }
+
+// The super-tiles of one CTA, in increasing order: chunks of kChunk super-tiles
+// (369 KB) dealt round robin over the grid, then the remainder cut into equal
+// contiguous ranges. At any moment the CTAs stream neighbouring chunks of the
+// cache, which spreads the load over the memory system more evenly than one
+// long contiguous range per CTA (whose end times spread by tens of microseconds
+// in a read of the same size); a chunk is long enough that sequence changes
+// (each a new query slot, two slots deep) stay rare against the stage ring.
+constexpr int kChunk = 8;
+struct TileIter {
+    int64_t f, end, total, body;
+    int k, rounds;
+    __device__ __forceinline__ void init(int64_t total_) {
+        total = total_;
+        rounds = (int)(total / kChunk / gridDim.x);
+        body = (int64_t)rounds * gridDim.x * kChunk;
+        k = 0;
+        set();
+    }
+    __device__ __forceinline__ void set() {
+        if (k < rounds) {
+            f = ((int64_t)k * gridDim.x + blockIdx.x) * kChunk;
+            end = f + kChunk;
+        } else {
+            const int64_t rest = total - body;
+            f = body + rest * blockIdx.x / gridDim.x;
+            end = body + rest * (blockIdx.x + 1) / gridDim.x;
+        }
+    }
+    // the next super-tile (flat index over all sequences); false when done
+    __device__ __forceinline__ bool next(int64_t& out) {
+        while (f >= end) {
+            if (k >= rounds) return false;
+            ++k;
+            set();
+        }
+        out = f++;
+        return true;
+    }
+};
 
 // tiles in super-tile g of a sequence with n_c positions
 __device__ __forceinline__ int tiles_in(int64_t g, int32_t n_c) {
@@ -268,8 +321,8 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
     const int64_t total = sh.prefix[B];
-    const int64_t f0 = total * blockIdx.x / gridDim.x;
-    const int64_t f1 = total * (blockIdx.x + 1) / gridDim.x;
+    TileIter ti;
+    ti.init(total);
 
     if (warp == kLoadWarp) {
         // ---------------- loader: query slots per sequence, super-tiles per stage
@@ -279,7 +332,8 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
         // lines go first, so the scores and block maxima written here are still in
         // L2 when the selection reads them
         const uint64_t key_policy = l2_policy_evict_first();
-        for (int64_t f = f0; f < f1; ++f) {
+        int64_t f, i = 0;
+        for (; ti.next(f); ++i) {
             b = advance_seq(sh, b, f);
             const int64_t g = f - sh.prefix[b];
             if (b != prev_b) {
@@ -302,7 +356,6 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
                 if (lane == 0) mbar_arrive(&sh.qfull[qs]);
                 prev_b = b;
             }
-            const int64_t i = f - f0;
             const int s = (int)(i % kStages);
             if (!mbar_wait(&sh.empty[s], (uint32_t)((i / kStages) & 1) ^ 1, abort)) break;
             if (lane == 0) {
@@ -326,9 +379,9 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
         const int e = warp - kMmaWarp;
         if (lane == 0) {
             int seg = -1, b = 0, prev_b = -1;
-            for (int64_t f = f0; f < f1; ++f) {
+            int64_t f, i = 0;
+            for (; ti.next(f); ++i) {
                 b = advance_seq(sh, b, f);
-                const int64_t i = f - f0;
                 if (b != prev_b) {
                     if (seg >= 0) tc_commit(&sh.qempty[seg & 1]);
                     ++seg;
@@ -377,9 +430,9 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
         const int64_t ld_bm = (max_ncomp + kBlk - 1) / kBlk;
         int b = 0, prev_b = -1;
         float wv[kHi];
-        for (int64_t f = f0; f < f1; ++f) {
+        int64_t f, i = 0;
+        for (; ti.next(f); ++i) {
             b = advance_seq(sh, b, f);
-            const int64_t i = f - f0;
             const int a = (int)(i % kAcc);
             if (b != prev_b) {
                 const float4* w4 = reinterpret_cast<const float4*>(w + (int64_t)b * kHi);
