@@ -190,13 +190,22 @@ def test_index_keys_write_produces_the_documented_tile_image():
             assert img[off] == ks[t_, g]
 
 
-@pytest.mark.parametrize("cuda_cores", [False, True])
-def test_index_scores_bit_exact_ragged(cuda_cores):
+# (cuda_cores, max_ctas). With the full grid this batch gives every CTA less than
+# one chunk of super-tiles (the tensor-core build's contiguous tail ranges only);
+# 3 CTAs take several round-robin chunks each, cross sequence boundaries inside a
+# chunk and wrap the stage ring many times.
+INDEX_MODES = {"tcgen05": (False, 0), "tcgen05_3ctas": (False, 3), "cuda_cores": (True, 0)}
+
+
+@pytest.mark.parametrize("mode", list(INDEX_MODES))
+def test_index_scores_bit_exact_ragged(mode):
+    cuda_cores, max_ctas = INDEX_MODES[mode]
     n_cs = [1, 7, 8, 9, 127, 128, 129, 255, 256, 257, 1000, 5003, 0, 70000]
     qv, qs, w, kvs, kss, _ = _index_case(3, n_cs)
     B = len(n_cs)
     max_nc = max(n_cs)
     p = api.default_params()
+    p.max_ctas = max_ctas
     cache = _tiled_caches(p, kvs, kss)
     n_tok = t(np.array([2 * n for n in n_cs], np.int32))
     scores = torch.full((B, max_nc), -7.0, device=DEV)
