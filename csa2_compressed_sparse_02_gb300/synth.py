@@ -9,7 +9,7 @@ twin in ``csrc/synth/synth.cu`` implements the same definitions, so the host
 copying hundreds of GB through the host.
 
 This module holds input distributions only — none of the method's arithmetic.
-Distributions (the workloads' shapes):
+Distributions (the shapes of the workloads' latents, codes, scales and weights):
 
 * ``normal``: unit-variance, zero-mean Irwin-Hall sum of eight 16-bit uniforms
   (two 64-bit draws per value), scaled by one fp32 constant, so both sides

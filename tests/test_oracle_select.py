@@ -1,8 +1,9 @@
 """Pins of the oracle's two-level selection ("DeepSeek-V4.1-Flash-NVFP4" §3.3:
 blocks of 8 positions scored by their best position, top-2048 blocks with the
 block holding the newest position always kept, then top-512 positions; config
-walkthrough §2.1 for the sizes). Ties go to the lower index (reading stated in
-the design doc). Checked by brute force on tiny inputs with many ties."""
+walkthrough §2.1 for the sizes). Ties go to the lower index (the pages are silent
+on ties; the lower index is the reading taken). Checked by brute force on tiny
+inputs with many ties."""
 import itertools
 
 import numpy as np
