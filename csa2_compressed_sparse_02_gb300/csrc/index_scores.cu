@@ -14,7 +14,7 @@
 // per lane (32 heads), apply ReLU and the head weights, and reduce the block
 // maximum over 8 adjacent lanes. One persistent CTA per SM; warps 0-7 epilogue
 // (two warpgroups taking alternate super-tiles), warp 8 loads (one bulk copy
-// per super-tile of 5 tiles into a 4-stage ring), warps 9 and 10 issue the
+// per super-tile of 6 tiles into a 4-stage ring), warps 9 and 10 issue the
 // MMAs of alternate super-tiles (a single issuing thread serialises each scale
 // copy with its MMA; two overlap them), each into its own TMEM accumulators.
 //
@@ -159,16 +159,17 @@ k_index_scores_cc(int64_t max_ncomp, int ratio, const uint8_t* __restrict__ q_va
 
 // ------------------------------------------------------------------ tensor-core build
 // Unit of work: a super-tile of up to kTilesPerStage consecutive tiles of one sequence
-// (contiguous in the cache, so one bulk copy of up to 45 KB). Per super-tile the
+// (contiguous in the cache, so one bulk copy of up to 54 KB). Per super-tile the
 // MMA thread issues 2 scale copies + 2 MMAs per tile into the tile's own TMEM
 // accumulator, then one commit for the stage and one for the epilogue: the
-// fixed per-commit, per-copy and per-handoff costs are paid once per 45 KB, not
+// fixed per-commit, per-copy and per-handoff costs are paid once per 54 KB, not
 // per 9 KB. Those costs, not the bytes in flight, set the rate: at 1 M context
 // (1.28 GB per launch) super-tiles of 2 / 3 / 4 / 5 tiles in 10 / 7 / 5 / 4
-// stages took 0.256 / 0.227 / 0.205 / 0.203 ms (6 tiles in 3 stages: 0.201 ms,
-// but an odd ring breaks the issuers' barrier protocol, below).
-constexpr int kTilesPerStage = 5;
-constexpr int kStageBytes = kTilesPerStage * kKeyTileBytes;  // 46,080 = 45 x 1024
+// stages took 0.256 / 0.227 / 0.205 / 0.203 ms. Six tiles fill the TMEM (2 x 6 x 32
+// accumulator columns, 2 x 6 x 8 scale columns, 32 query scale columns), and four
+// of them fit in shared memory because no per-sequence table is kept there.
+constexpr int kTilesPerStage = 6;
+constexpr int kStageBytes = kTilesPerStage * kKeyTileBytes;  // 55,296 = 54 x 1024
 constexpr int kStages = 4;
 constexpr int kIssuers = 2;      // MMA-issuing warps, alternating super-tiles
 // Each issuer waits only for the stage fills of its own super-tiles. A parity
@@ -184,7 +185,6 @@ constexpr int kAcc = kIssuers;   // one super-tile accumulator set per issuer
 constexpr int kEpiGroups = 2;    // epilogue warpgroups, alternating super-tiles
 constexpr int kLoadWarp = 4 * kEpiGroups, kMmaWarp = kLoadWarp + 1;
 constexpr int kTcThreads = 32 * (kMmaWarp + kIssuers);  // 0-7 epilogue, 8 loader, 9-10 MMA
-constexpr int kMaxSeq = 1024;
 constexpr uint32_t kTmemCols = 512;
 // TMEM columns: D[kAcc][kTilesPerStage] x 32, SFA[kAcc][kTilesPerStage] x 8, SFB[kIssuers][2] x 8
 constexpr uint32_t kColD = 0, kColSFA = 32 * kAcc * kTilesPerStage, kColSFB = kColSFA + 8 * kAcc * kTilesPerStage;
@@ -199,20 +199,37 @@ struct TcShared {
     uint8_t sfb[2][1024];                  // B scale factors, two 512-byte atoms per slot
     uint64_t full[kStages], empty[kStages];
     uint64_t qfull[2], qempty[2], accf[kAcc], acce[kAcc], done;
+    int64_t total;  // super-tiles of all sequences
     uint32_t tmem_base;
     int abort;
-    int32_t prefix[kMaxSeq + 1];  // super-tiles of sequences < b
-    int32_t ncomp[kMaxSeq];
 };
 
-// sequence of flat super-tile f: advance b while f is past sequence b's super-tiles
-__device__ __forceinline__ int advance_seq(const TcShared& sh, int b, int64_t f) {
-    while (f >= sh.prefix[b + 1]) ++b;
-    return b;
+// super-tiles of a sequence with n_c positions
+__device__ __forceinline__ int64_t supers_of(int64_t n_c) {
+    return (n_c + kTilesPerStage * kKeyTile - 1) / (kTilesPerStage * kKeyTile);
 }
 
+// The sequence of each flat super-tile (super-tiles numbered sequence after
+// sequence) for a role that visits increasing f: it reads each sequence's length
+// as it passes it, so no per-sequence table sits in shared memory and the batch
+// size is not bounded by it. f must be below the total.
+struct SeqCursor {
+    int b = -1;
+    int64_t start = 0, end = 0;  // flat super-tiles [start, end) belong to sequence b
+    int64_t n_c = 0;
+    __device__ __forceinline__ void advance(int64_t f, const int32_t* n_tokens, int ratio,
+                                            int64_t max_ncomp) {
+        while (f >= end) {
+            ++b;
+            start = end;
+            n_c = seq_ncomp(n_tokens, b, ratio, max_ncomp, nullptr, false);
+            end = start + supers_of(n_c);
+        }
+    }
+};
+
 // The super-tiles of one CTA, in increasing order: chunks of kChunk super-tiles
-// (369 KB) dealt round robin over the grid, then the remainder cut into equal
+// (442 KB) dealt round robin over the grid, then the remainder cut into equal
 // contiguous ranges. At any moment the CTAs stream neighbouring chunks of the
 // cache, which spreads the load over the memory system more evenly than one
 // long contiguous range per CTA (whose end times spread by tens of microseconds
@@ -252,7 +269,7 @@ struct TileIter {
 };
 
 // tiles in super-tile g of a sequence with n_c positions
-__device__ __forceinline__ int tiles_in(int64_t g, int32_t n_c) {
+__device__ __forceinline__ int tiles_in(int64_t g, int64_t n_c) {
     const int64_t nt = (n_c + kKeyTile - 1) / kKeyTile;
     const int64_t left = nt - g * kTilesPerStage;
     return left < kTilesPerStage ? (int)left : kTilesPerStage;
@@ -289,28 +306,13 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
         sh.abort = 0;
         fence_mbar_init();
     }
-    if (warp == 0) {  // per-sequence compressed lengths and super-tile prefix
-        const int per = (B + 31) / 32;
-        const int b0 = min(B, lane * per), b1 = min(B, b0 + per);
-        int32_t local = 0;
-        for (int b = b0; b < b1; ++b) {
-            const int64_t n_c = seq_ncomp(n_tokens, b, ratio, max_ncomp, dev_status,
-                                          blockIdx.x == 0);
-            sh.ncomp[b] = (int32_t)n_c;
-            local += (int32_t)((n_c + kTilesPerStage * kKeyTile - 1) / (kTilesPerStage * kKeyTile));
-        }
-        int32_t incl = local;
+    if (warp == 0) {  // super-tiles of all sequences (CTA 0 flags bad lengths)
+        int64_t local = 0;
+        for (int b = lane; b < B; b += 32)
+            local += supers_of(seq_ncomp(n_tokens, b, ratio, max_ncomp, dev_status, blockIdx.x == 0));
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int32_t u = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += u;
-        }
-        int32_t run = incl - local;
-        for (int b = b0; b < b1; ++b) {
-            sh.prefix[b] = run;
-            run += (sh.ncomp[b] + kTilesPerStage * kKeyTile - 1) / (kTilesPerStage * kKeyTile);
-        }
-        if (lane == 31) sh.prefix[B] = incl;
+        for (int o = 16; o >= 1; o >>= 1) local += __shfl_xor_sync(0xffffffffu, local, o);
+        if (lane == 0) sh.total = local;
     }
     if (warp == kMmaWarp) {  // the first MMA warp owns the TMEM allocation
         tmem_alloc(&sh.tmem_base, kTmemCols);
@@ -320,13 +322,14 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
-    const int64_t total = sh.prefix[B];
+    const int64_t total = sh.total;
     TileIter ti;
     ti.init(total);
 
     if (warp == kLoadWarp) {
         // ---------------- loader: query slots per sequence, super-tiles per stage
         int seg = -1, b = 0, prev_b = -1;
+        SeqCursor cur;
         int64_t issued = 0;
         // the key stream (72 B per position, far larger than L2) is read once: its
         // lines go first, so the scores and block maxima written here are still in
@@ -334,8 +337,9 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
         const uint64_t key_policy = l2_policy_evict_first();
         int64_t f, i = 0;
         for (; ti.next(f); ++i) {
-            b = advance_seq(sh, b, f);
-            const int64_t g = f - sh.prefix[b];
+            cur.advance(f, n_tokens, ratio, max_ncomp);
+            b = cur.b;
+            const int64_t g = f - cur.start;
             if (b != prev_b) {
                 ++seg;
                 const int qs = seg & 1;
@@ -359,7 +363,7 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
             const int s = (int)(i % kStages);
             if (!mbar_wait(&sh.empty[s], (uint32_t)((i / kStages) & 1) ^ 1, abort)) break;
             if (lane == 0) {
-                const uint32_t bytes = (uint32_t)tiles_in(g, sh.ncomp[b]) * kKeyTileBytes;
+                const uint32_t bytes = (uint32_t)tiles_in(g, cur.n_c) * kKeyTileBytes;
                 mbar_arrive_expect_tx(&sh.full[s], bytes);
                 bulk_g2s_hint(sh.stage[s], key_cache[b] + g * kStageBytes, bytes, &sh.full[s],
                               key_policy);
@@ -379,9 +383,11 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
         const int e = warp - kMmaWarp;
         if (lane == 0) {
             int seg = -1, b = 0, prev_b = -1;
+            SeqCursor cur;
             int64_t f, i = 0;
             for (; ti.next(f); ++i) {
-                b = advance_seq(sh, b, f);
+                cur.advance(f, n_tokens, ratio, max_ncomp);
+                b = cur.b;
                 if (b != prev_b) {
                     if (seg >= 0) tc_commit(&sh.qempty[seg & 1]);
                     ++seg;
@@ -402,7 +408,7 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
                 const int qs = seg & 1;
                 const uint32_t qa = smem_u32(sh.q[qs]);
                 const uint32_t sfb = tmem + kColSFB + 16 * e + 8 * qs;
-                const int nt = tiles_in(f - sh.prefix[b], sh.ncomp[b]);
+                const int nt = tiles_in(f - cur.start, cur.n_c);
                 for (int j = 0; j < nt; ++j) {
                     const uint32_t st = smem_u32(sh.stage[s]) + j * kKeyTileBytes;
                     const uint32_t sfa = tmem + kColSFA + 8 * (a * kTilesPerStage + j);
@@ -429,10 +435,12 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
         const int eg = warp >> 2, wq = warp & 3;
         const int64_t ld_bm = (max_ncomp + kBlk - 1) / kBlk;
         int b = 0, prev_b = -1;
+        SeqCursor cur;
         float wv[kHi];
         int64_t f, i = 0;
         for (; ti.next(f); ++i) {
-            b = advance_seq(sh, b, f);
+            cur.advance(f, n_tokens, ratio, max_ncomp);
+            b = cur.b;
             const int a = (int)(i % kAcc);
             if (b != prev_b) {
                 const float4* w4 = reinterpret_cast<const float4*>(w + (int64_t)b * kHi);
@@ -449,9 +457,9 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
             if ((int)(i % kEpiGroups) != eg) continue;
             if (!mbar_wait(&sh.accf[a], (uint32_t)((i / kAcc) & 1), abort)) break;
             tc_fence_after();
-            const int64_t g = f - sh.prefix[b];
-            const int nt = tiles_in(g, sh.ncomp[b]);
-            const int32_t n_c = sh.ncomp[b];
+            const int64_t g = f - cur.start;
+            const int nt = tiles_in(g, cur.n_c);
+            const int64_t n_c = cur.n_c;
             for (int j = 0; j < nt; ++j) {
                 uint32_t r[kHi];
                 tmem_ld_32x32b_x32(
@@ -559,6 +567,7 @@ extern "C" int csa2_index_scores_cuda_cores(const csa2_params* p, int B, int64_t
     if (rc != CSA2_OK) return rc < 0 ? CSA2_OK : rc;
     const int64_t gx = (max_ncomp + kKeysPerCta - 1) / kKeysPerCta;
     if (gx > 0x7fffffff) return fail(CSA2_ERR_UNSUPPORTED, "index_scores: too many positions");
+    if (B > 65535) return fail(CSA2_ERR_UNSUPPORTED, "index_scores: at most 65535 sequences per call");
     if (const int rc = ensure_loaded()) return rc;
     k_index_scores_cc<<<dim3((unsigned)gx, B), kKeysPerCta, 0, static_cast<cudaStream_t>(stream)>>>(
         max_ncomp, p->compress_ratio, q_vals, q_scales, w, key_cache, n_tokens, scores, block_max,
@@ -574,7 +583,7 @@ extern "C" int csa2_index_scores(const csa2_params* p, int B, int64_t max_ncomp,
     const int rc = check_index_args(p, B, max_ncomp, q_vals, q_scales, w, key_cache, n_tokens,
                                     scores, block_max);
     if (rc != CSA2_OK) return rc < 0 ? CSA2_OK : rc;
-    if (B > kMaxSeq) return fail(CSA2_ERR_UNSUPPORTED, "index_scores: at most 1024 sequences per call");
+    if (B > 65535) return fail(CSA2_ERR_UNSUPPORTED, "index_scores: at most 65535 sequences per call");
     if (const int rc = ensure_loaded()) return rc;
     static bool attr = false;
     if (!attr) {

@@ -239,7 +239,7 @@ int csa2_index_keys_write(const csa2_params* p, int B, int64_t n,
  *   max_ncomp >= every n_c (else CSA2_DEV_BAD_LENGTH, and the sequence is clipped).
  *   A pipeline wait that does not complete within about a second sets
  *   CSA2_DEV_TIMEOUT and the kernel returns.
- * Constraints: Hi == 32, Di == 128, block_size == 8, B <= 1024.
+ * Constraints: Hi == 32, Di == 128, block_size == 8, B <= 65535.
  * The fp32 result is exact (independent of summation order) when every
  * partial sum is a multiple of a common power of two below 2^24 of it — true
  * for E2M1 codes with power-of-two scales and weights.
