@@ -72,7 +72,7 @@ def peaks():
 # of the kernel: it is reported only while the kernel source hashes to the same
 # value.
 INDEX_TRAFFIC_PER_POS = (151422208 + 4354304) / 2097152
-INDEX_TRAFFIC_SRC_SHA256 = "f372548dfa1abe26cf69eb13d3b69e2f1e04c6bd1d36ee3e04c9b8b5ad153941"
+INDEX_TRAFFIC_SRC_SHA256 = "d1a875cf2670bd7d5fef3fa38919702ec87a35ddeda4b03c5cfef473396887a5"
 
 
 def index_traffic(positions: float):

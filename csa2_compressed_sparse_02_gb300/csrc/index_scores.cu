@@ -165,9 +165,10 @@ k_index_scores_cc(int64_t max_ncomp, int ratio, const uint8_t* __restrict__ q_va
 // fixed per-commit, per-copy and per-handoff costs are paid once per 54 KB, not
 // per 9 KB. Those costs, not the bytes in flight, set the rate: at 1 M context
 // (1.28 GB per launch) super-tiles of 2 / 3 / 4 / 5 tiles in 10 / 7 / 5 / 4
-// stages took 0.256 / 0.227 / 0.205 / 0.203 ms. Six tiles fill the TMEM (2 x 6 x 32
-// accumulator columns, 2 x 6 x 8 scale columns, 32 query scale columns), and four
-// of them fit in shared memory because no per-sequence table is kept there.
+// stages took 0.256 / 0.227 / 0.205 / 0.203 ms, and 6 tiles in 4 stages the same
+// as 5. Six tiles fill the TMEM (2 x 6 x 32 accumulator columns, 2 x 6 x 8 scale
+// columns, 32 query scale columns), and a ring of four such stages fits in shared
+// memory because no per-sequence table is kept there.
 constexpr int kTilesPerStage = 6;
 constexpr int kStageBytes = kTilesPerStage * kKeyTileBytes;  // 55,296 = 54 x 1024
 constexpr int kStages = 4;
@@ -495,6 +496,7 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
 }
 
 constexpr int kTcSmem = (int)sizeof(TcShared) + 1024;
+static_assert(kTcSmem <= 227 * 1024, "shared memory of the tensor-core Indexer");
 
 int num_sms() {
     static int n = 0;
