@@ -55,6 +55,14 @@ def test_host_side_rejections_without_launching(L):
     assert L.csa2_index_scores_cuda_cores(pp, 1, 10, *([None] * 9)) == 1
     bad = api.default_params(index_heads=16)
     assert L.csa2_index_scores(ctypes.byref(bad), 1, 10, *([None] * 9)) == 4
+    # more sequences than one launch takes (grid.y of the CUDA-core build): rejected
+    # before anything is enqueued; the buffers are host memory, never dereferenced
+    buf = (ctypes.c_uint8 * 64)()
+    base = ctypes.addressof(buf)
+    al = ctypes.c_void_p((base + 15) & ~15)
+    for fn in (L.csa2_index_scores, L.csa2_index_scores_cuda_cores):
+        assert fn(pp, 65536, 10, al, al, al, al, al, al, al, None, None) == 4
+        assert "65535" in L.csa2_last_error().decode()
     bad_dim = api.default_params(index_dim=64)
     assert L.csa2_index_keys_write(ctypes.byref(bad_dim), 1, 4, *([None] * 7)) == 4
     assert L.csa2_index_keys_write(pp, 1, 4, *([None] * 7)) == 1
