@@ -123,8 +123,66 @@ int64_t orc_compress_append_ratio(int64_t T, int n_new, int D, int W, int ratio,
                                   float* pend_kv, float* pend_g,
                                   uint8_t* comp_vals, uint8_t* comp_scales, float* comp_f32,
                                   uint8_t* win_u8, float* win_f32) {
-    int has_comp = (comp_vals != NULL) || (comp_f32 != NULL);
+    return orc_compress_append_rope(T, n_new, D, W, ratio, NULL, kv_new, g_new, pend_kv, pend_g,
+                                    comp_vals, comp_scales, comp_f32, win_u8, win_f32);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Rotary position embedding of the compressed KV (RoFormer rotation, YaRN    */
+/* NTK-by-parts frequencies)                                                  */
+/* ------------------------------------------------------------------------- */
+
+void orc_rope_freqs(const orc_rope* r, double* theta) {
+    const double two_pi = 2.0 * acos(-1.0);
+    for (int i = 0; i < r->dim / 2; ++i) {
+        double th = pow(r->base, -2.0 * i / r->dim); /* RoFormer frequency of pair i */
+        double wavelength = two_pi / th;
+        double rotations = r->orig_len / wavelength; /* turns over the original context */
+        double gamma;
+        if (rotations < r->beta_slow)
+            gamma = 0.0; /* long wavelength: interpolate */
+        else if (rotations > r->beta_fast)
+            gamma = 1.0; /* short wavelength: keep */
+        else
+            gamma = (rotations - r->beta_slow) / (r->beta_fast - r->beta_slow);
+        theta[i] = (1.0 - gamma) * th / r->factor + gamma * th;
+    }
+}
+
+void orc_rope_rotate(float* x, int D, int64_t pos, const orc_rope* r) {
+    if (!r || r->dim <= 0) return;
+    double* theta = (double*)malloc(sizeof(double) * (size_t)(r->dim / 2));
+    orc_rope_freqs(r, theta);
+    float* part = x + (D - r->dim);
+    for (int i = 0; i < r->dim / 2; ++i) {
+        double angle = (double)pos * theta[i];
+        double c = cos(angle), s = sin(angle);
+        double a = part[2 * i], b = part[2 * i + 1];
+        part[2 * i] = (float)(a * c - b * s);
+        part[2 * i + 1] = (float)(a * s + b * c);
+    }
+    free(theta);
+}
+
+void orc_compress_row(int D, int ratio, int64_t j, const float* kv0, const float* kv1,
+                      const float* g0, const float* g1, const orc_rope* rope,
+                      uint8_t* vals, uint8_t* scales, float* f32) {
     float* row = (float*)malloc(sizeof(float) * (size_t)D);
+    for (int d = 0; d < D; ++d) row[d] = ratio == 1 ? kv0[d] : orc_pool(kv0[d], kv1[d], g0[d], g1[d]);
+    orc_rope_rotate(row, D, (int64_t)ratio * j, rope); /* raw position of the pair's first token */
+    if (f32)
+        memcpy(f32, row, sizeof(float) * (size_t)D);
+    else
+        orc_nvfp4_quantize(row, D / 16, vals, scales);
+    free(row);
+}
+
+int64_t orc_compress_append_rope(int64_t T, int n_new, int D, int W, int ratio,
+                                 const orc_rope* rope, const float* kv_new, const float* g_new,
+                                 float* pend_kv, float* pend_g,
+                                 uint8_t* comp_vals, uint8_t* comp_scales, float* comp_f32,
+                                 uint8_t* win_u8, float* win_f32) {
+    int has_comp = (comp_vals != NULL) || (comp_f32 != NULL);
     for (int i = 0; i < n_new; ++i) {
         int64_t p = T + i; /* raw position of this token */
         const float* kv = kv_new + (int64_t)i * D;
@@ -135,26 +193,17 @@ int64_t orc_compress_append_ratio(int64_t T, int n_new, int D, int W, int ratio,
         if (win_f32)
             for (int d = 0; d < D; ++d) win_f32[slot * D + d] = kv[d];
         if (!has_comp) continue;
-        if (ratio == 1) { /* 1:1 layer: pooling skipped, raw token p is compressed row p */
-            if (comp_f32)
-                memcpy(comp_f32 + p * D, kv, sizeof(float) * (size_t)D);
-            else
-                orc_nvfp4_quantize(kv, D / 16, comp_vals + p * (D / 2), comp_scales + p * (D / 16));
-            continue;
-        }
-        if ((p & 1) == 0) { /* first token of a pair: wait for its partner */
+        int64_t j = p / ratio; /* ratio 1 (1:1 layer): raw token p is compressed row p */
+        if (ratio == 2 && (p & 1) == 0) { /* first token of a pair: wait for its partner */
             memcpy(pend_kv, kv, sizeof(float) * (size_t)D);
             memcpy(pend_g, g, sizeof(float) * (size_t)D);
             continue;
         }
-        int64_t j = p / 2; /* pair (2j, 2j+1) is complete: emit compressed row j */
-        for (int d = 0; d < D; ++d) row[d] = orc_pool(pend_kv[d], kv[d], pend_g[d], g[d]);
-        if (comp_f32)
-            memcpy(comp_f32 + j * D, row, sizeof(float) * (size_t)D);
-        else
-            orc_nvfp4_quantize(row, D / 16, comp_vals + j * (D / 2), comp_scales + j * (D / 16));
+        orc_compress_row(D, ratio, j, ratio == 1 ? kv : pend_kv, kv, pend_g, g, rope,
+                         comp_f32 ? NULL : comp_vals + j * (D / 2),
+                         comp_f32 ? NULL : comp_scales + j * (D / 16),
+                         comp_f32 ? comp_f32 + j * D : NULL);
     }
-    free(row);
     return T + n_new;
 }
 

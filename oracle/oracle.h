@@ -84,6 +84,57 @@ int64_t orc_compress_append_ratio(int64_t T, int n_new, int D, int W, int ratio,
                                   uint8_t* comp_vals, uint8_t* comp_scales, float* comp_f32,
                                   uint8_t* win_u8, float* win_f32);
 
+/* ---- Rotary position embedding of the compressed KV ---- */
+/*
+ * [CFG] §2.2 (compress_rope_theta 160000: the compressed KV gets its own RoPE
+ * base), §四 (rope_scaling: rope_type yarn, factor 16,
+ * original_max_position_embeddings 65536, beta_fast 32, beta_slow 1);
+ * [NVFP4] §3.2 (one latent stands for 2 tokens, so it uses compress_rope_theta
+ * 160000 with YaRN factor 16 to reach 1M).
+ * Method: RoPE as in Su et al., "RoFormer" (2021) — dims (2i, 2i+1) of the
+ * rotated part turn by the angle pos * theta_i, theta_i = base^(-2i/dim) —
+ * with YaRN's "NTK-by-parts" frequencies (Peng et al., "YaRN", 2023): with
+ * wavelength lambda_i = 2 pi / theta_i and r_i = orig_len / lambda_i, a pair
+ * with r_i > beta_fast keeps theta_i, one with r_i < beta_slow takes
+ * theta_i / factor, and between them gamma = (r_i - beta_slow) /
+ * (beta_fast - beta_slow) blends (1 - gamma) theta_i / factor + gamma theta_i.
+ * Readings (the pages name only the base and the YaRN keys): the rotated part
+ * is the last `dim` dims of the latent; compressed row j sits at raw position
+ * ratio * j (the first raw token of its pair); YaRN's attention temperature is
+ * a logit scale, not part of the rotation.
+ */
+typedef struct orc_rope {
+    int dim;           /* rotated dims (even): the last `dim` of the row; 0 = none */
+    double base;       /* rotary base (compress_rope_theta) */
+    double factor;     /* YaRN scale s; 1 gives plain RoPE */
+    double orig_len;   /* original context length L */
+    double beta_fast;  /* above this many rotations over L a pair keeps its frequency */
+    double beta_slow;  /* below this many it is interpolated by 1/factor */
+} orc_rope;
+
+/* theta'_i of pairs i = 0 .. dim/2-1 (fp64).                                */
+void orc_rope_freqs(const orc_rope* r, double* theta);
+/* Rotates x[D-dim .. D) of one fp32 row in place at raw position pos: pair i =
+ * (x[D-dim+2i], x[D-dim+2i+1]) -> (a cos - b sin, a sin + b cos), angle
+ * pos * theta'_i, fp64 arithmetic, rounded to fp32. NULL or dim 0: no-op.   */
+void orc_rope_rotate(float* x, int D, int64_t pos, const orc_rope* r);
+
+/* One compressed row j of a layer of compression ratio 1 or 2 ([NVFP4] §3.2):
+ * kv0 (and kv1, g0, g1 at ratio 2) are the raw tokens ratio*j (.. ratio*j+1);
+ * the row is the gated pool (ratio 2) or the token itself (ratio 1), rotated at
+ * raw position ratio*j when rope is set, then written as NVFP4 (vals [D/2],
+ * scales [D/16]) or, when f32 is non-NULL, as fp32 [D].                     */
+void orc_compress_row(int D, int ratio, int64_t j, const float* kv0, const float* kv1,
+                      const float* g0, const float* g1, const orc_rope* rope,
+                      uint8_t* vals, uint8_t* scales, float* f32);
+
+/* orc_compress_append_ratio with the compressed rows rotated (rope may be NULL). */
+int64_t orc_compress_append_rope(int64_t T, int n_new, int D, int W, int ratio,
+                                 const orc_rope* rope, const float* kv_new, const float* g_new,
+                                 float* pend_kv, float* pend_g,
+                                 uint8_t* comp_vals, uint8_t* comp_scales, float* comp_f32,
+                                 uint8_t* win_u8, float* win_f32);
+
 /* ---- Indexer ([NVFP4] §3.3, [CFG] §2.1) ---- */
 /*
  * s_t = sum_h w[h] * ReLU( sum_d q[h,d] * k[t,d] ),  t < n_c, fp64.

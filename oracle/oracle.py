@@ -71,6 +71,19 @@ def lib():
             L.orc_compress_append_ratio.argtypes = [
                 ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, _f32p,
                 _f32p, _f32p, _f32p, _u8p, _u8p, _f32p, _u8p, _f32p]
+            L.orc_rope_freqs.restype = None
+            L.orc_rope_freqs.argtypes = [ctypes.POINTER(Rope), _f64p]
+            L.orc_rope_rotate.restype = None
+            L.orc_rope_rotate.argtypes = [_f32p, ctypes.c_int, ctypes.c_int64,
+                                          ctypes.POINTER(Rope)]
+            L.orc_compress_row.restype = None
+            L.orc_compress_row.argtypes = [
+                ctypes.c_int, ctypes.c_int, ctypes.c_int64, _f32p, _f32p, _f32p, _f32p,
+                ctypes.POINTER(Rope), _u8p, _u8p, _f32p]
+            L.orc_compress_append_rope.restype = ctypes.c_int64
+            L.orc_compress_append_rope.argtypes = [
+                ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.POINTER(Rope), _f32p, _f32p, _f32p, _f32p, _u8p, _u8p, _f32p, _u8p, _f32p]
             L.orc_index_scores.restype = ctypes.c_int64
             L.orc_index_scores.argtypes = [
                 ctypes.c_int, ctypes.c_int, _u8p, _u8p, _f32p, ctypes.c_int64, _u8p, _u8p, _f32p]
@@ -89,6 +102,25 @@ def lib():
             L.orc_nvfp4_scale_bytes.argtypes = [ctypes.c_int64, ctypes.c_int]
             _lib = L
     return _lib
+
+
+class Rope(ctypes.Structure):
+    """orc_rope: the compressed KV's rotary embedding (oracle.h)."""
+    _fields_ = [("dim", ctypes.c_int), ("base", ctypes.c_double), ("factor", ctypes.c_double),
+                ("orig_len", ctypes.c_double), ("beta_fast", ctypes.c_double),
+                ("beta_slow", ctypes.c_double)]
+
+
+def rope_config(dim=64, base=160000.0, factor=16.0, orig_len=65536.0, beta_fast=32.0,
+                beta_slow=1.0) -> Rope:
+    """The pages' compressed-KV rotary setting ("CSA2稀疏注意力、384专家MoE与1M上下文" §2.2
+    compress_rope_theta, §四 rope_scaling; "DeepSeek-V4.1-Flash-NVFP4" §3.2), with the
+    rotated width as a reading (default: the last 64 dims)."""
+    return Rope(dim, base, factor, orig_len, beta_fast, beta_slow)
+
+
+def _rp(rope):
+    return ctypes.byref(rope) if rope is not None else ctypes.cast(None, ctypes.POINTER(Rope))
 
 
 def _p(a, typ):
@@ -147,16 +179,53 @@ def pool(kv0: float, kv1: float, g0: float, g1: float) -> float:
     return lib().orc_pool(float(kv0), float(kv1), float(g0), float(g1))
 
 
+# --------------------------------------------------------------------------- rotary
+def rope_freqs(rope: Rope) -> np.ndarray:
+    th = np.zeros(rope.dim // 2, np.float64)
+    lib().orc_rope_freqs(ctypes.byref(rope), _p(th, _f64p))
+    return th
+
+
+def rope_rotate(x: np.ndarray, pos: int, rope: Rope) -> np.ndarray:
+    """Rotated copy of the fp32 row(s) x [..., D] at raw position pos."""
+    x = np.array(x, dtype=np.float32, copy=True).reshape(-1, np.shape(x)[-1])
+    for r in range(x.shape[0]):
+        row = np.ascontiguousarray(x[r])
+        lib().orc_rope_rotate(_p(row, _f32p), row.size, int(pos), ctypes.byref(rope))
+        x[r] = row
+    return x.reshape(np.shape(x)) if x.shape[0] > 1 else x[0]
+
+
+def compress_row(j: int, kv, g=None, ratio: int = 2, rope: Rope | None = None, f32=False):
+    """Compressed row j from its raw tokens kv [ratio, D] (and gates g [2, D] at
+    ratio 2): -> fp32 [D] when f32, else (vals [D/2], scales [D/16])."""
+    kv = np.ascontiguousarray(kv, np.float32).reshape(ratio, -1)
+    D = kv.shape[1]
+    if ratio == 2:
+        g = np.ascontiguousarray(g, np.float32).reshape(2, D)
+        k0, k1, g0, g1 = (np.ascontiguousarray(a) for a in (kv[0], kv[1], g[0], g[1]))
+    else:
+        k0, k1, g0, g1 = np.ascontiguousarray(kv[0]), None, None, None
+    vals = None if f32 else np.zeros(D // 2, np.uint8)
+    scales = None if f32 else np.zeros(D // 16, np.uint8)
+    out = np.zeros(D, np.float32) if f32 else None
+    lib().orc_compress_row(D, ratio, int(j), _p(k0, _f32p), _p(k1, _f32p), _p(g0, _f32p),
+                           _p(g1, _f32p), _rp(rope), _p(vals, _u8p), _p(scales, _u8p),
+                           _p(out, _f32p))
+    return out if f32 else (vals, scales)
+
+
 # --------------------------------------------------------------------------- compressor
 class SeqState:
     """One sequence's cache for one layer, as the oracle keeps it (host arrays)."""
 
     def __init__(self, cap_comp: int, D: int = 512, W: int = 128,
                  comp_f32: bool = False, win_f32: bool = False, has_comp: bool = True,
-                 ratio: int = 2):
-        """ratio 2: the 2:1 pooled layers; ratio 1: the 1:1 layers (pooling skipped)."""
+                 ratio: int = 2, rope: Rope | None = None):
+        """ratio 2: the 2:1 pooled layers; ratio 1: the 1:1 layers (pooling skipped);
+        rope: rotate each compressed row at its raw position (None: rows unrotated)."""
         assert ratio in (1, 2)
-        self.D, self.W, self.T, self.ratio = D, W, 0, ratio
+        self.D, self.W, self.T, self.ratio, self.rope = D, W, 0, ratio, rope
         self.pend_kv = np.zeros(D, np.float32)
         self.pend_g = np.zeros(D, np.float32)
         self.comp_f32 = np.zeros((cap_comp, D), np.float32) if (has_comp and comp_f32) else None
@@ -171,8 +240,9 @@ class SeqState:
         kv = np.ascontiguousarray(kv, dtype=np.float32).reshape(-1, self.D)
         if g is not None:
             g = np.ascontiguousarray(g, dtype=np.float32).reshape(-1, self.D)
-        self.T = lib().orc_compress_append_ratio(
-            self.T, kv.shape[0], self.D, self.W, self.ratio, _p(kv, _f32p), _p(g, _f32p),
+        self.T = lib().orc_compress_append_rope(
+            self.T, kv.shape[0], self.D, self.W, self.ratio, _rp(self.rope), _p(kv, _f32p),
+            _p(g, _f32p),
             _p(self.pend_kv, _f32p), _p(self.pend_g, _f32p), _p(self.comp_vals, _u8p),
             _p(self.comp_scales, _u8p), _p(self.comp_f32, _f32p), _p(self.win_u8, _u8p),
             _p(self.win_f32, _f32p))
