@@ -27,7 +27,10 @@ class Params(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in (
         "heads", "head_dim", "index_heads", "index_dim", "window", "block_size", "topk_blocks",
         "topk_pos", "compress_ratio", "kv_format", "win_format", "q_format")] + [
-        ("softmax_scale", ctypes.c_float), ("win_layout", ctypes.c_int), ("max_ctas", ctypes.c_int)]
+        ("softmax_scale", ctypes.c_float), ("win_layout", ctypes.c_int), ("max_ctas", ctypes.c_int),
+        ("rope_dim", ctypes.c_int), ("rope_theta", ctypes.c_float), ("rope_factor", ctypes.c_float),
+        ("rope_orig_len", ctypes.c_float), ("rope_beta_fast", ctypes.c_float),
+        ("rope_beta_slow", ctypes.c_float)]
 
 
 PP = ctypes.POINTER(Params)

@@ -62,6 +62,12 @@ extern "C" void csa2_default_params(csa2_params* p) {
     p->softmax_scale = 1.0f / std::sqrt((float)csa2::kD);
     p->win_layout = CSA2_WIN_RING;
     p->max_ctas = 0;
+    p->rope_dim = 0;
+    p->rope_theta = 160000.0f;
+    p->rope_factor = 16.0f;
+    p->rope_orig_len = 65536.0f;
+    p->rope_beta_fast = 32.0f;
+    p->rope_beta_slow = 1.0f;
 }
 
 extern "C" int csa2_trace_attach(int32_t* record) {
@@ -73,6 +79,6 @@ extern "C" int csa2_trace_attach(int32_t* record) {
     return CSA2_OK;
 }
 
-extern "C" int csa2_version(void) { return 200; }
+extern "C" int csa2_version(void) { return 300; }
 
 extern "C" const char* csa2_last_error(void) { return csa2::g_last_error.c_str(); }

@@ -41,6 +41,41 @@ __device__ __forceinline__ uint32_t nvfp4_4(float4 c, uint8_t& scale_byte) {
            (e2m1_code_rne(__fdiv_rn(c.z, S)) << 8) | (e2m1_code_rne(__fdiv_rn(c.w, S)) << 12);
 }
 
+// Rotary embedding of a compressed row ("CSA2稀疏注意力、384专家MoE与1M上下文" §2.2
+// compress_rope_theta, §四 rope_scaling yarn; "DeepSeek-V4.1-Flash-NVFP4" §3.2).
+// The last `dim` channels turn in adjacent pairs by pos * theta_i, theta_i the
+// YaRN frequency (Peng et al. 2023, NTK-by-parts) of the RoFormer frequency
+// base^(-2i/dim). fp64 throughout; the caller rounds the result to fp32.
+struct RopeArgs {
+    int dim;  // 0: no rotation
+    double base, factor, orig_len, beta_fast, beta_slow;
+};
+
+__device__ __forceinline__ double yarn_freq(int i, const RopeArgs& r) {
+    const double f = pow(r.base, -(double)(2 * i) / (double)r.dim);
+    // turns of this pair over the original context: orig_len / (2 pi / f)
+    const double turns = r.orig_len * f * 0.15915494309189535;  // 1 / (2 pi)
+    double keep;  // share of the unscaled frequency
+    if (turns > r.beta_fast) keep = 1.0;
+    else if (turns < r.beta_slow) keep = 0.0;
+    else keep = (turns - r.beta_slow) / (r.beta_fast - r.beta_slow);
+    return f * keep + (f / r.factor) * (1.0 - keep);
+}
+
+// Rotates channels ch..ch+3 of a row at raw position pos when they fall in the
+// rotated tail (ch and dim multiples of 4, so a pair never straddles threads).
+__device__ __forceinline__ float4 rope4(float4 v, int ch, int64_t pos, const RopeArgs& r) {
+    const int first = kD - r.dim;
+    if (r.dim <= 0 || ch < first) return v;
+    const int i0 = (ch - first) >> 1;
+    double s0, c0, s1, c1;
+    sincos((double)pos * yarn_freq(i0, r), &s0, &c0);
+    sincos((double)pos * yarn_freq(i0 + 1, r), &s1, &c1);
+    const double x = v.x, y = v.y, z = v.z, w = v.w;
+    return make_float4((float)(x * c0 - y * s0), (float)(x * s0 + y * c0),
+                       (float)(z * c1 - w * s1), (float)(z * s1 + w * c1));
+}
+
 __device__ __forceinline__ uint32_t e4m3x4(float4 v) {
     uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(v.x, v.y), __NV_SATFINITE, __NV_E4M3);
     uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(v.z, v.w), __NV_SATFINITE, __NV_E4M3);
@@ -54,7 +89,7 @@ __global__ void __launch_bounds__(kThreads)
 k_compress_append(int n_new, const float* __restrict__ kv_new, const float* __restrict__ gate_new,
                   float* pend_kv, float* pend_gate, void* const* comp,
                   uint8_t* const* comp_scales, const int64_t* comp_cap, void* const* win,
-                  int32_t* n_tokens, int advance_here, int32_t* dev_status) {
+                  int32_t* n_tokens, int advance_here, RopeArgs rope, int32_t* dev_status) {
     const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
     trace_start(kTraceCompress);
     const int ch = 4 * tid;
@@ -97,6 +132,7 @@ k_compress_append(int n_new, const float* __restrict__ kv_new, const float* __re
                 v.z = pool1(k0.z, k1.z, g0.z, g1.z);
                 v.w = pool1(k0.w, k1.w, g0.w, g1.w);
             }
+            v = rope4(v, ch, (int64_t)kRatio * j, rope);  // row j sits at raw position ratio*j
             if (j >= cap) {
                 if (tid == 0) raise_status(dev_status, CSA2_DEV_BAD_LENGTH);
                 continue;
@@ -247,6 +283,19 @@ extern "C" int csa2_compress_append(const csa2_params* p, int B, int n_new,
         return fail(CSA2_ERR_INVALID_ARG, "compress_append: NVFP4 needs comp_scales");
     if (p->win_format != CSA2_E4M3 && p->win_format != CSA2_F32)
         return fail(CSA2_ERR_UNSUPPORTED, "compress_append: win_format must be E4M3 or F32");
+    if (p->rope_dim < 0 || p->rope_dim > kD || p->rope_dim % 4)
+        return fail(CSA2_ERR_UNSUPPORTED, "compress_append: rope_dim must be a multiple of 4 in [0, 512]");
+    if (p->rope_dim > 0 && !(p->rope_theta > 0.f && p->rope_factor > 0.f && p->rope_orig_len > 0.f &&
+                             p->rope_beta_fast > p->rope_beta_slow))
+        return fail(CSA2_ERR_INVALID_ARG,
+                    "compress_append: rope needs theta, factor, orig_len > 0 and beta_fast > beta_slow");
+    RopeArgs rope;
+    rope.dim = comp ? p->rope_dim : 0;
+    rope.base = p->rope_theta;
+    rope.factor = p->rope_factor;
+    rope.orig_len = p->rope_orig_len;
+    rope.beta_fast = p->rope_beta_fast;
+    rope.beta_slow = p->rope_beta_slow;
     if (!aligned16(kv_new) || (gate_new && !aligned16(gate_new)) ||
         (pend_kv && !aligned16(pend_kv)) || (pend_gate && !aligned16(pend_gate)))
         return fail(CSA2_ERR_ALIGN, "compress_append: fp32 buffers must be 16-byte aligned");
@@ -262,7 +311,7 @@ extern "C" int csa2_compress_append(const csa2_params* p, int B, int n_new,
     k_compress_append<R, NV, WE><<<grid, kThreads, 0, s>>>(n_new, kv_new, gate_new, pend_kv, \
                                                             pend_gate, comp, comp_scales,   \
                                                             comp_cap, win, n_tokens,        \
-                                                            advance_here, dev_status)
+                                                            advance_here, rope, dev_status)
     if (ratio == 2) {
         if (nvfp4 && we) CSA2_LAUNCH(2, true, true);
         else if (nvfp4) CSA2_LAUNCH(2, true, false);

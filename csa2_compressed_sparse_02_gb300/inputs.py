@@ -41,6 +41,7 @@ class DecodeConfig:
     T: int = 0          # context length (incl. the step's token) at step 0; 0 = ragged
     T_range: tuple = (4096, 1048576)
     ratio: int = 2      # raw tokens per compressed position: 2 (pooled) or 1 (1:1 layers)
+    rope: bool = False  # the Compressor rotates the last ROPE_DIM dims of each compressed row
 
     @property
     def seed(self) -> int:
@@ -83,6 +84,10 @@ CONFIGS = {
     7: DecodeConfig(7, "decode B=8 T=32768 1:1 layers (n_c = T) NVFP4, 1 group x 2 layers", B=8,
                     groups=1, readers=2, steps=1, quant=True, plants=16, kscale_pow2=True,
                     T=32768, ratio=1),
+    # the compressed KV rotated by the Compressor (YaRN, base 160000, factor 16, last 64 dims)
+    9: DecodeConfig(9, "decode B=8 T=65536 NVFP4, compressed-KV RoPE (YaRN x16, base 160000, "
+                       "last 64 dims)", B=8, groups=1, readers=1, steps=1, quant=True, plants=16,
+                    kscale_pow2=True, T=65536, rope=True),
     5: DecodeConfig(5, "decode B=32 ragged T in [4096, 1048576], 1 index source + 5 readers, "
                        "16 steps", B=32, groups=1, readers=6, steps=16, quant=True, plants=16,
                     kscale_pow2=True),
@@ -123,6 +128,7 @@ PREFILL = PrefillConfig(4, "prefill chunk of 8192 queries on a 262,144-token con
                         T0=262144, chunk=8192)
 
 D, H, HI, DI, W = 512, 64, 32, 128, 128
+ROPE_DIM = 64  # rotated width of the compressed KV (a reading; the pages give only the base)
 
 
 # =============================================================================== host side

@@ -10,7 +10,7 @@ from dataclasses import dataclass, field
 import numpy as np
 
 from . import synth
-from .inputs import CONFIGS, D, DI, H, HI, W, DecodeConfig, plants  # noqa: F401
+from .inputs import CONFIGS, D, DI, H, HI, ROPE_DIM, W, DecodeConfig, plants  # noqa: F401
 
 # =============================================================================== device side
 @dataclass
@@ -46,11 +46,12 @@ class DecodeRun:
         assert self.out_slots in (1, 2)
         if self.out_slots == 2:
             self.n_prep = max(2, self.n_prep - self.n_prep % 2)
+        rope = dict(rope_dim=ROPE_DIM) if cfg.rope else {}
         if cfg.quant:
-            self.params = api.default_params(compress_ratio=cfg.ratio)
+            self.params = api.default_params(compress_ratio=cfg.ratio, **rope)
         else:
             self.params = api.default_params(kv_format=api.F32, win_format=api.F32,
-                                             q_format=api.F32, compress_ratio=cfg.ratio)
+                                             q_format=api.F32, compress_ratio=cfg.ratio, **rope)
         last = [T + self.n_steps - 1 for T in self.T0]          # T after the last step
         rt = cfg.ratio
         self.comp_caps = [t // rt + 1 for t in last]

@@ -88,13 +88,35 @@ typedef struct csa2_params {
                              (csa2_index_scores, csa2_sparse_attn_layers); 0 = one
                              per SM. A caller that runs two of them concurrently on
                              different streams splits the SMs with it. */
+    /* Rotary embedding of the compressed KV, applied by csa2_compress_append
+     * ("CSA2稀疏注意力、384专家MoE与1M上下文" §2.2 compress_rope_theta, §四
+     * rope_scaling yarn; "DeepSeek-V4.1-Flash-NVFP4" §3.2). Compressed row j is
+     * rotated at raw position compress_ratio*j (its first raw token) after
+     * pooling and before quantising: its last rope_dim dims, in adjacent pairs
+     * (2i, 2i+1) -> (a cos - b sin, a sin + b cos) with angle pos*theta_i, where
+     * theta_i is the YaRN "NTK-by-parts" frequency (Peng et al. 2023) of the
+     * RoFormer frequency rope_theta^(-2i/rope_dim): with r_i = rope_orig_len *
+     * theta_i / (2 pi) rotations over the original context, pairs with r_i >
+     * rope_beta_fast keep theta_i, pairs with r_i < rope_beta_slow take
+     * theta_i / rope_factor, and in between the two blend linearly in r_i.
+     * Angles, sines and cosines in fp64; the rotated values are rounded to fp32.
+     * The window is not rotated here (its tokens arrive rotated). */
+    int rope_dim;         /* rotated dims: 0 (default: rows arrive rotated) or a
+                             multiple of 4 up to head_dim */
+    float rope_theta;     /* rotary base: 160000 */
+    float rope_factor;    /* YaRN factor: 16 (1 = plain RoPE) */
+    float rope_orig_len;  /* YaRN original context length: 65536 */
+    float rope_beta_fast; /* 32 */
+    float rope_beta_slow; /* 1 */
 } csa2_params;
 
 #define CSA2_WIN_RING 0
 #define CSA2_WIN_LINEAR 1
 
 /* Fills *p with the pages' configuration (64/512/32/128/128/8/2048/512/2,
- * NVFP4 cache, E4M3 window, bf16 query, 1/sqrt(512), ring window). */
+ * NVFP4 cache, E4M3 window, bf16 query, 1/sqrt(512), ring window; rotary base
+ * 160000, YaRN factor 16 over 65536 with betas 32/1, rope_dim 0 = rows arrive
+ * rotated). */
 void csa2_default_params(csa2_params* p);
 
 /*
@@ -138,6 +160,10 @@ const char* csa2_last_error(void);
  * With compress_ratio 1 (the 1:1 layers, "CSA2稀疏注意力、384专家MoE与1M上下文"
  * §2.2) pooling is skipped: new raw token p is written as compressed row p with
  * the same encoding, and gate_new / pend_kv / pend_gate are not used.
+ * With rope_dim > 0 each compressed row is rotated before it is encoded (see
+ * csa2_params); rope_dim must be a multiple of 4 up to D and the YaRN settings
+ * must have rope_theta > 0, rope_factor > 0, rope_orig_len > 0 and
+ * rope_beta_fast > rope_beta_slow (else CSA2_ERR_UNSUPPORTED / INVALID_ARG).
  *
  *   kv_new, gate_new  [B, n_new, D] fp32, device. gate_new may be NULL when
  *                     comp is NULL or compress_ratio is 1.

@@ -14,6 +14,7 @@ from __future__ import annotations
 
 import math
 import time
+from types import SimpleNamespace
 
 import numpy as np
 
@@ -37,14 +38,26 @@ def index_and_select(cfg, g: int, s: int, step: int):
 
 
 def compressed_rows(cfg, layer: int, s: int, positions):
-    """Compact cache whose row i is compressed position positions[i] of `layer`."""
+    """Compact cache whose row i is compressed position positions[i] of `layer`:
+    each row recomputed from its raw tokens (pooled at ratio 2, rotated at raw
+    position ratio*j when the configuration rotates the compressed KV)."""
     rt = cfg.ratio
-    st = orc.SeqState(cap_comp=max(1, len(positions)), D=I.D, W=I.W, comp_f32=not cfg.quant,
-                      win_f32=not cfg.quant, ratio=rt)
-    for j in positions:  # position j is raw tokens rt*j .. rt*j + rt - 1
+    rope = orc.rope_config(dim=I.ROPE_DIM) if getattr(cfg, "rope", False) else None
+    n = max(1, len(positions))
+    st = SimpleNamespace(comp_f32=None, comp_vals=None, comp_scales=None)
+    if cfg.quant:
+        st.comp_vals = np.zeros((n, I.D // 2), np.uint8)
+        st.comp_scales = np.zeros((n, I.D // 16), np.uint8)
+    else:
+        st.comp_f32 = np.zeros((n, I.D), np.float32)
+    for i, j in enumerate(positions):  # position j is raw tokens rt*j .. rt*j + rt - 1
         kv = I.host_kv(cfg, layer, s, rt * j, rt * j + rt)
         g = I.host_gate(cfg, layer, s, rt * j, rt * j + rt) if rt == 2 else None
-        st.append(kv, g)
+        row = orc.compress_row(j, kv, g, ratio=rt, rope=rope, f32=not cfg.quant)
+        if cfg.quant:
+            st.comp_vals[i], st.comp_scales[i] = row
+        else:
+            st.comp_f32[i] = row
     return st
 
 

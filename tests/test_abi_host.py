@@ -37,6 +37,10 @@ def test_defaults_are_the_pages_sizes(L):
             p.topk_blocks, p.topk_pos, p.compress_ratio) == (64, 512, 32, 128, 128, 8, 2048, 512, 2)
     assert abs(p.softmax_scale - 512 ** -0.5) < 1e-8
     assert (p.kv_format, p.win_format, p.q_format) == (api.NVFP4, api.E4M3, api.BF16)
+    # compressed-KV rotary setting: config walkthrough §2.2 (compress_rope_theta) and §四
+    # (YaRN factor 16 over 65536, beta_fast 32, beta_slow 1); off by default
+    assert (p.rope_dim, p.rope_theta, p.rope_factor, p.rope_orig_len, p.rope_beta_fast,
+            p.rope_beta_slow) == (0, 160000.0, 16.0, 65536.0, 32.0, 1.0)
 
 
 def test_workspace_size_covers_split_partials(L):
@@ -76,5 +80,13 @@ def test_host_side_rejections_without_launching(L):
     assert L.csa2_sparse_attn_layers_part(pp, 2, 4, 1, 0, *([None] * 10)) == 0  # empty range
     bad_ratio = api.default_params(compress_ratio=3)
     assert L.csa2_compress_append(ctypes.byref(bad_ratio), 1, 1, *([None] * 11)) == 4
+    # rotary settings the Compressor is not built for, rejected before any launch
+    # (the buffers are host memory, never dereferenced)
+    for over, code in ((dict(rope_dim=62), 4), (dict(rope_dim=1024), 4), (dict(rope_dim=-4), 4),
+                       (dict(rope_dim=64, rope_beta_fast=0.5), 1),
+                       (dict(rope_dim=64, rope_theta=0.0), 1)):
+        bp = api.default_params(**over)
+        assert L.csa2_compress_append(ctypes.byref(bp), 1, 1, al, None, None, None, None, None,
+                                      None, al, al, None, None) == code, over
     # nothing to do is not an error
     assert L.csa2_compress_append(pp, 0, 1, *([None] * 11)) == 0

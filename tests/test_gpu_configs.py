@@ -82,6 +82,20 @@ def test_config7_ratio_one_full():
         assert set(pos.tolist()) <= set(ref["idx"].tolist())
 
 
+def test_config9_compressed_kv_rope_full():
+    """Configuration 2 with the compressed KV rotated by the Compressor (YaRN, base
+    160000, factor 16, last 64 dims): every sequence's whole decode step."""
+    cfg = inputs.CONFIGS[9]
+    run = workloads.DecodeRun(cfg, n_steps=1)
+    assert run.params.rope_dim == inputs.ROPE_DIM
+    run.step()
+    torch.cuda.synchronize()
+    assert run.dev_status.item() == 0
+    for s in range(cfg.B):
+        ref = _check(run, 0, s, 0)
+        assert ref["n_sel"] == 512 and ref["attended"] == 640
+
+
 def test_config3_sampled():
     cfg = inputs.CONFIGS[3]
     run = workloads.DecodeRun(cfg, n_steps=1)

@@ -130,6 +130,95 @@ def test_compress_append_matches_oracle(f32):
                                               gv[j, 8 * gi:8 * gi + 8], gsc[j, gi]), (j, gi)
 
 
+@pytest.mark.parametrize("ratio,T0,f32", [(2, 0, False), (2, 1046528, False), (1, 1046528, False),
+                                          (2, 1046528, True)])
+def test_compress_append_rope_matches_oracle(ratio, T0, f32):
+    """Compressed-KV rotary embedding ("CSA2稀疏注意力、384专家MoE与1M上下文" §2.2, §四;
+    "DeepSeek-V4.1-Flash-NVFP4" §3.2): YaRN rotation of the last 64 dims of row j at
+    raw position ratio*j, after pooling and before quantising, near 0 and near 1M.
+    At ratio 1 the rotation sees identical fp32 inputs; the rotated value may differ
+    from the oracle's by one fp32 rounding (both fp64, rounded once), plus the fp32
+    pooling error of both pair members at ratio 2; a code may flip only where moving
+    the oracle's value by that bound crosses a rounding boundary."""
+    rng = np.random.default_rng(30 + ratio + (T0 > 0))
+    B = 2
+    rope = orc.rope_config(dim=64)
+    n_news = [1, 2, 7, 150, 1, 33] if ratio == 2 else [1, 2, 7, 150, 3]
+    total = sum(n_news)
+    cap = (T0 + total) // ratio + 1
+    over = dict(rope_dim=64, compress_ratio=ratio)
+    if f32:
+        over.update(kv_format=api.F32, win_format=api.F32, q_format=api.F32)
+    p = api.default_params(**over)
+    cache = api.LayerCache(B, [cap] * B, p)
+    cache.n_tokens.fill_(T0)
+    kvs, gs = [], []
+    for n in n_news:
+        kv = (rng.standard_normal((B, n, 512)) * 2).astype(np.float32)
+        g = (rng.standard_normal((B, n, 512)) * 3).astype(np.float32)
+        kvs.append(kv)
+        gs.append(g)
+        cache.append(t(kv), t(g) if ratio == 2 else None, dev_status=None)
+    torch.cuda.synchronize()
+    assert cache.n_tokens.cpu().tolist() == [T0 + total] * B
+    j_lo, j_hi = T0 // ratio, (T0 + total) // ratio
+    for b in range(B):
+        kv_all = np.concatenate([k[b] for k in kvs])
+        g_all = np.concatenate([g[b] for g in gs])
+        got_f = cache.comp[b][j_lo:j_hi].cpu().numpy() if f32 else None
+        gv = None if f32 else cache.comp[b][j_lo:j_hi].cpu().numpy()
+        gsc = None if f32 else cache.comp_scales[b][j_lo:j_hi].cpu().numpy()
+        flips = 0
+        for j in range(j_lo, j_hi):
+            t0 = ratio * j - T0
+            kvp = kv_all[t0:t0 + ratio]
+            gp = g_all[t0:t0 + 2] if ratio == 2 else None
+            ref = orc.compress_row(j, kvp, gp, ratio=ratio, rope=rope, f32=True)
+            if ratio == 2:
+                bound = _pool_error_bound(kvp[0], kvp[1]).astype(np.float64)
+            else:
+                bound = np.zeros(512)
+            tail = slice(512 - 64, 512)
+            pair_b = bound[tail].reshape(-1, 2).sum(1).repeat(2)  # both members feed each output
+            bound[tail] = pair_b + np.spacing(np.abs(ref[tail]).astype(np.float32) + np.float32(1e-30))
+            if f32:
+                err = np.abs(got_f[j - j_lo].astype(np.float64) - ref)
+                assert np.all(err <= bound), (b, j, (err / np.maximum(bound, 1e-30)).max())
+                continue
+            rv, rs = orc.nvfp4_quantize(ref)
+            for gi in range(32):
+                if rs[gi] == gsc[j - j_lo, gi] and np.array_equal(rv[8 * gi:8 * gi + 8],
+                                                                  gv[j - j_lo, 8 * gi:8 * gi + 8]):
+                    continue
+                flips += 1
+                assert _near_boundary_flip_ok(ref[16 * gi:16 * gi + 16], bound[16 * gi:16 * gi + 16],
+                                              gv[j - j_lo, 8 * gi:8 * gi + 8], gsc[j - j_lo, gi]), (b, j, gi)
+        assert flips <= max(2, (j_hi - j_lo) * 32 // 1000)
+    # the rotation is active: rows differ from the unrotated Compressor's
+    p0 = api.default_params(**dict(over, rope_dim=0))
+    flat = api.LayerCache(1, [cap], p0)
+    flat.n_tokens.fill_(T0)
+    for kv, g in zip(kvs, gs):
+        flat.append(t(kv[:1]), t(g[:1]) if ratio == 2 else None)
+    torch.cuda.synchronize()
+    a, z = cache.comp[0][j_lo + 1:j_hi].cpu().numpy(), flat.comp[0][j_lo + 1:j_hi].cpu().numpy()
+    head = slice(0, 448) if f32 else slice(0, 224)
+    assert np.array_equal(a[:, head], z[:, head]) and not np.array_equal(a, z)
+
+
+def test_compress_append_rope_rejects_bad_settings():
+    cache = api.LayerCache(1, [4], api.default_params())
+    kv = torch.zeros(1, 2, 512, device=DEV)
+    for over in (dict(rope_dim=62), dict(rope_dim=516), dict(rope_dim=64, rope_beta_fast=1.0)):
+        p = api.default_params(**over)
+        with pytest.raises(api.Csa2Error):
+            api.compress_append(p, kv, kv, cache.pend_kv, cache.pend_gate, cache.comp_ptrs,
+                                cache.comp_scale_ptrs, cache.comp_cap, cache.win_ptrs,
+                                cache.n_tokens)
+    torch.cuda.synchronize()
+    assert cache.n_tokens.item() == 0  # nothing was enqueued
+
+
 def test_compress_capacity_overflow_sets_status_and_writes_nothing_past_cap():
     p = api.default_params()
     cache = api.LayerCache(1, [2], p)
