@@ -50,6 +50,7 @@ SIGNATURES = {
     "csa2_select_topk": (I32, [PP, I32, I64, P, P, P, P, P, P, P]),
     "csa2_sparse_attn_workspace_size": (SZ, [PP, I32]),
     "csa2_sparse_attn": (I32, [PP, I32, P, P, P, P, P, P, P, P, P, SZ, P, P]),
+    "csa2_sparse_attn_mma": (I32, [PP, I32, P, P, P, P, P, P, P, P, P, SZ, P, P]),
     "csa2_sparse_attn_noalloc": (I32, [PP, I32, P, P, P, P, P, P, P, P, P, P]),
     "csa2_sparse_attn_layers": (I32, [PP, I32, I32, P, P, P, P, P, P, P, P, P, P]),
     "csa2_sparse_attn_layers_mma": (I32, [PP, I32, I32, P, P, P, P, P, P, P, P, P, P]),

@@ -141,13 +141,16 @@ def sparse_attn_workspace_size(params, B) -> int:
 
 
 def sparse_attn(params, q, sink, win_ptrs, n_tokens, comp_ptrs, comp_scale_ptrs, idx, out,
-                workspace, dev_status=None, stream=None):
+                workspace, dev_status=None, stream=None, mma_sync=False):
+    """One layer (csa2_sparse_attn: tcgen05 for the quantised formats); mma_sync=True
+    runs the legacy mma.sync split-KV implementation (csa2_sparse_attn_mma)."""
     B = n_tokens.numel()
-    check(lib().csa2_sparse_attn(
+    fn = lib().csa2_sparse_attn_mma if mma_sync else lib().csa2_sparse_attn
+    check(fn(
         ctypes.byref(params), B, _ptr(q), _ptr(sink), _ptr(win_ptrs), _ptr(n_tokens),
         _ptr(comp_ptrs), _ptr(comp_scale_ptrs), _ptr(idx), _ptr(out), _ptr(workspace),
         workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream)),
-        "sparse_attn")
+        "sparse_attn_mma" if mma_sync else "sparse_attn")
 
 
 def sparse_attn_layers_split_workspace(params, L, B, device="cuda"):

@@ -55,6 +55,17 @@ cudaError_t preload_select();
 cudaError_t preload_attn();
 cudaError_t preload_attn_tc();
 
+// Single-layer sparse attention (csa2_sparse_attn, quantised formats) on the
+// tcgen05 kernel of sparse_attn_tc.cu with the even split schedule; the
+// workspace holds that schedule's partial results (sparse_attn_tc_ws_bytes),
+// 256-byte aligned; its completion counts are zeroed on the stream first.
+size_t sparse_attn_tc_ws_bytes(const csa2_params* p, int B);
+int sparse_attn_tc_single(const char* name, const csa2_params* p, int B, const void* q,
+                          const float* sink, const void* const* win, const int32_t* n_tokens,
+                          const void* const* comp, const uint8_t* const* comp_scales,
+                          const int32_t* idx, void* out, void* workspace, size_t ws_bytes,
+                          int32_t* dev_status, void* stream);
+
 // ---- launch trace (diagnostics; off unless csa2_trace_attach set a record).
 // Every translation unit has its own copy of the record pointer. When set, CTA 0
 // thread 0 of the traced kernels writes {kernel id, launch number} into record

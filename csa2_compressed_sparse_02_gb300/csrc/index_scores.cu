@@ -214,6 +214,15 @@ __device__ __forceinline__ int64_t supers_of(int64_t n_c) {
 // sequence) for a role that visits increasing f: it reads each sequence's length
 // as it passes it, so no per-sequence table sits in shared memory and the batch
 // size is not bounded by it. f must be below the total.
+// Every role of every CTA must read the same n_tokens values that warp 0 summed
+// into the total: the loader, the MMA issuers and the epilogue each walk the
+// flat super-tiles with their own cursor, and a role that saw other lengths
+// would wait on barriers the others never complete (until the bounded wait
+// gives up). That holds because n_tokens does not change while the kernel runs:
+// it is launched in plain stream order after the Compressor's k_advance, which
+// writes n_tokens. A launch that could overlap that writer (a programmatic
+// launch behind it) must first wait for it (grid_dep_wait) before warp 0 reads
+// the lengths.
 struct SeqCursor {
     int b = -1;
     int64_t start = 0, end = 0;  // flat super-tiles [start, end) belong to sequence b
@@ -586,14 +595,8 @@ extern "C" int csa2_index_scores(const csa2_params* p, int B, int64_t max_ncomp,
                                     scores, block_max);
     if (rc != CSA2_OK) return rc < 0 ? CSA2_OK : rc;
     if (B > 65535) return fail(CSA2_ERR_UNSUPPORTED, "index_scores: at most 65535 sequences per call");
+    // loads the kernel and sets its shared-memory limit on this device, once per device
     if (const int rc = ensure_loaded()) return rc;
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(k_index_scores_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kTcSmem) != cudaSuccess)
-            return check_launch("index_scores: smem attribute");
-        attr = true;
-    }
     const int64_t tiles_max = (int64_t)B * ((max_ncomp + kTilesPerStage * kKeyTile - 1) / (kTilesPerStage * kKeyTile));
     int64_t ctas = num_sms();
     if (p->max_ctas > 0 && p->max_ctas < ctas) ctas = p->max_ctas;

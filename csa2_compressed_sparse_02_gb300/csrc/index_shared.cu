@@ -436,20 +436,8 @@ extern "C" int csa2_index_scores_shared(const csa2_params* p, int Q, int64_t max
     if (!aligned16(q_vals) || !aligned16(key_cache) || (reinterpret_cast<uintptr_t>(q_scales) & 7) ||
         (reinterpret_cast<uintptr_t>(w) & 3))
         return fail(CSA2_ERR_ALIGN, "index_scores_shared: q_vals, key_cache 16-byte, q_scales 8-byte aligned");
-    {
-        if (const int rc = ensure_loaded()) return rc;
-        static std::mutex mu;
-        static uint64_t attr_set = 0;
-        int dev = 0;
-        cudaGetDevice(&dev);
-        std::lock_guard<std::mutex> lk(mu);
-        if (dev >= 0 && dev < 64 && !((attr_set >> dev) & 1u)) {
-            if (cudaFuncSetAttribute(k_index_shared_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kShSmem) != cudaSuccess)
-                return check_launch("index_scores_shared: smem attribute");
-            attr_set |= 1ull << dev;
-        }
-    }
+    // loads the kernel and sets its shared-memory limit on this device, once per device
+    if (const int rc = ensure_loaded()) return rc;
     Work wk;
     wk.n_blocks = (Q + kQPerBlock - 1) / kQPerBlock;
     wk.st_per_block = (max_ncomp + kPosPerStage - 1) / kPosPerStage;

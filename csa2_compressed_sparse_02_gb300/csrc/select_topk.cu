@@ -490,15 +490,9 @@ extern "C" int csa2_select_topk(const csa2_params* p, int B, int64_t max_ncomp,
         return fail(CSA2_ERR_UNSUPPORTED, "select_topk: more than 2^31 positions");
     if (!scores || !block_max || !n_tokens || !idx)
         return fail(CSA2_ERR_INVALID_ARG, "select_topk: NULL buffer");
+    // loads the kernel and sets its shared-memory limit on this device, once per device
     if (const int rc = ensure_loaded()) return rc;
-    static bool attr_set = false;
     const int smem = (int)sizeof(SelShared);
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(k_select_topk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 smem) != cudaSuccess)
-            return check_launch("select_topk: smem attribute");
-        attr_set = true;
-    }
     k_select_topk<<<B, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(
         max_ncomp, p->compress_ratio, scores, block_max, n_tokens, idx, n_sel, dev_status);
     return check_launch("select_topk");

@@ -736,9 +736,12 @@ cudaError_t preload_attn() {
 using namespace csa2;
 
 extern "C" size_t csa2_sparse_attn_workspace_size(const csa2_params* p, int B) {
-    (void)p;
     if (B <= 0) return 0;
-    return ws_o_bytes(B) + ws_ml_bytes(B);
+    // the larger of the two schedules' needs: the CUDA-core and mma.sync split-KV
+    // passes (5 partials per sequence) and the tcgen05 kernel's cut units
+    const size_t kv = ws_o_bytes(B) + ws_ml_bytes(B);
+    const size_t tc = sparse_attn_tc_ws_bytes(p, B);
+    return kv > tc ? kv : tc;
 }
 
 extern "C" int csa2_sparse_attn_layers_mma(const csa2_params* p, int L, int B, const void* q,
@@ -759,14 +762,8 @@ extern "C" int csa2_sparse_attn_layers_mma(const csa2_params* p, int L, int B, c
     if (!aligned16(q) || !aligned16(out))
         return fail(CSA2_ERR_ALIGN, "sparse_attn_layers_mma: q, out must be 16-byte aligned");
     if (L > 65535 || B > 65535) return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn_layers_mma: grid too large");
+    // loads the kernel and sets its shared-memory limit on this device, once per device
     if (const int rc = ensure_loaded()) return rc;
-    static bool attr = false;
-    if (!attr) {
-        if (cudaFuncSetAttribute(k_sparse_attn_fd, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kSmemFd) != cudaSuccess)
-            return check_launch("sparse_attn_layers_mma: smem attribute");
-        attr = true;
-    }
     k_sparse_attn_fd<<<dim3(L, B), kFdThreads, kSmemFd, static_cast<cudaStream_t>(stream)>>>(
         B, static_cast<const __nv_bfloat16*>(q), sink, win, n_tokens, comp, comp_scales, idx,
         p->compress_ratio, p->softmax_scale * kLog2e, static_cast<__nv_bfloat16*>(out), dev_status,
@@ -774,73 +771,105 @@ extern "C" int csa2_sparse_attn_layers_mma(const csa2_params* p, int L, int B, c
     return check_launch("sparse_attn_layers_mma");
 }
 
-extern "C" int csa2_sparse_attn(const csa2_params* p, int B, const void* q, const float* sink,
-                                const void* const* win, const int32_t* n_tokens,
-                                const void* const* comp, const uint8_t* const* comp_scales,
-                                const int32_t* idx, void* out, void* workspace, size_t ws_bytes,
-                                int32_t* dev_status, void* stream) {
+namespace {
+// Host checks shared by csa2_sparse_attn and csa2_sparse_attn_mma. Returns
+// CSA2_OK with *quant set, -1 for an empty batch (nothing to do), or an error.
+int check_single(const char* name, const csa2_params* p, int B, const void* q, const float* sink,
+                 const void* const* win, const int32_t* n_tokens, const void* const* comp,
+                 const uint8_t* const* comp_scales, const int32_t* idx, void* out, void* workspace,
+                 size_t ws_bytes, bool* quant) {
+    const std::string n(name);
     CSA2_CHECK_PARAMS(p);
-    if (B < 0) return fail(CSA2_ERR_INVALID_ARG, "sparse_attn: negative batch");
-    if (B == 0) return CSA2_OK;
+    if (B < 0) return fail(CSA2_ERR_INVALID_ARG, n + ": negative batch");
+    if (B == 0) return -1;
     if (p->heads != kH || p->head_dim != kD || p->window != kW || p->topk_pos != kKp ||
         p->compress_ratio < 1)
-        return fail(CSA2_ERR_UNSUPPORTED, "sparse_attn: built for 64 heads x 512, W=128, k=512");
+        return fail(CSA2_ERR_UNSUPPORTED, n + ": built for 64 heads x 512, W=128, k=512");
     if (!q || !sink || !win || !n_tokens || !comp || !idx || !out || !workspace)
-        return fail(CSA2_ERR_INVALID_ARG, "sparse_attn: NULL buffer");
+        return fail(CSA2_ERR_INVALID_ARG, n + ": NULL buffer");
     if (ws_bytes < csa2_sparse_attn_workspace_size(p, B))
-        return fail(CSA2_ERR_SHAPE, "sparse_attn: workspace smaller than the size query");
+        return fail(CSA2_ERR_SHAPE, n + ": workspace smaller than the size query");
     if (!aligned16(q) || !aligned16(out) || !aligned16(workspace))
-        return fail(CSA2_ERR_ALIGN, "sparse_attn: q, out, workspace must be 16-byte aligned");
-    const bool quant = p->kv_format == CSA2_NVFP4 && p->win_format == CSA2_E4M3 &&
-                       p->q_format == CSA2_BF16;
+        return fail(CSA2_ERR_ALIGN, n + ": q, out, workspace must be 16-byte aligned");
+    *quant = p->kv_format == CSA2_NVFP4 && p->win_format == CSA2_E4M3 && p->q_format == CSA2_BF16;
     const bool plain = p->kv_format == CSA2_F32 && p->win_format == CSA2_F32 &&
                        p->q_format == CSA2_F32;
-    if (!quant && !plain)
+    if (!*quant && !plain)
         return fail(CSA2_ERR_UNSUPPORTED,
-                    "sparse_attn: formats must be (NVFP4, E4M3, BF16) or (F32, F32, F32)");
-    if (quant && !comp_scales) return fail(CSA2_ERR_INVALID_ARG, "sparse_attn: NVFP4 needs scales");
+                    n + ": formats must be (NVFP4, E4M3, BF16) or (F32, F32, F32)");
+    if (*quant && !comp_scales) return fail(CSA2_ERR_INVALID_ARG, n + ": NVFP4 needs scales");
+    return CSA2_OK;
+}
+
+// The split-KV passes (5 position splits per sequence, partials in the
+// workspace) and the log-sum-exp merge: fp32 on CUDA cores, or bf16 mma.sync.
+int launch_split_kv(const char* name, const csa2_params* p, int B, bool quant, const void* q,
+                    const float* sink, const void* const* win, const int32_t* n_tokens,
+                    const void* const* comp, const uint8_t* const* comp_scales,
+                    const int32_t* idx, void* out, void* workspace, int32_t* dev_status,
+                    void* stream) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float* ws_o = static_cast<float*>(workspace);
     float2* ws_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) + ws_o_bytes(B));
     const float scale_log2 = p->softmax_scale * kLog2e;
     const dim3 grid(kSplits, B);
+    // loads the kernels and sets their shared-memory limits on this device, once per device
     if (const int rc = ensure_loaded()) return rc;
-    static bool attr_bf16 = false, attr_f32 = false;
     if (quant) {
-        if (!attr_bf16) {
-            if (cudaFuncSetAttribute(k_sparse_attn_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kSmemBf16) != cudaSuccess)
-                return check_launch("sparse_attn: smem attribute");
-            attr_bf16 = true;
-        }
         k_sparse_attn_bf16<<<grid, kThreads, kSmemBf16, s>>>(
             static_cast<const __nv_bfloat16*>(q), win, n_tokens, comp, comp_scales, idx,
             p->compress_ratio, scale_log2, ws_o, ws_ml, dev_status, p->win_layout == CSA2_WIN_LINEAR);
         k_sparse_attn_merge<true><<<dim3(kH, B), 128, 0, s>>>(sink, ws_o, ws_ml, out);
     } else {
-        if (!attr_f32) {
-            if (cudaFuncSetAttribute(k_sparse_attn_f32, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kSmemF32) != cudaSuccess)
-                return check_launch("sparse_attn: smem attribute");
-            attr_f32 = true;
-        }
         k_sparse_attn_f32<<<grid, kF32Threads, kSmemF32, s>>>(
             static_cast<const float*>(q), win, n_tokens, comp, idx, p->compress_ratio, scale_log2,
             ws_o, ws_ml, dev_status, p->win_layout == CSA2_WIN_LINEAR);
         k_sparse_attn_merge<false><<<dim3(kH, B), 128, 0, s>>>(sink, ws_o, ws_ml, out);
     }
-    return check_launch("sparse_attn");
+    return check_launch(name);
+}
+}  // namespace
+
+extern "C" int csa2_sparse_attn(const csa2_params* p, int B, const void* q, const float* sink,
+                                const void* const* win, const int32_t* n_tokens,
+                                const void* const* comp, const uint8_t* const* comp_scales,
+                                const int32_t* idx, void* out, void* workspace, size_t ws_bytes,
+                                int32_t* dev_status, void* stream) {
+    bool quant = false;
+    const int rc = check_single("sparse_attn", p, B, q, sink, win, n_tokens, comp, comp_scales, idx,
+                                out, workspace, ws_bytes, &quant);
+    if (rc != CSA2_OK) return rc < 0 ? CSA2_OK : rc;
+    if (quant)  // tcgen05, the fused kernel of sparse_attn_tc.cu with one layer
+        return sparse_attn_tc_single("sparse_attn", p, B, q, sink, win, n_tokens, comp, comp_scales,
+                                     idx, out, workspace, ws_bytes, dev_status, stream);
+    return launch_split_kv("sparse_attn", p, B, false, q, sink, win, n_tokens, comp, comp_scales,
+                           idx, out, workspace, dev_status, stream);
+}
+
+extern "C" int csa2_sparse_attn_mma(const csa2_params* p, int B, const void* q, const float* sink,
+                                    const void* const* win, const int32_t* n_tokens,
+                                    const void* const* comp, const uint8_t* const* comp_scales,
+                                    const int32_t* idx, void* out, void* workspace, size_t ws_bytes,
+                                    int32_t* dev_status, void* stream) {
+    bool quant = false;
+    const int rc = check_single("sparse_attn_mma", p, B, q, sink, win, n_tokens, comp, comp_scales,
+                                idx, out, workspace, ws_bytes, &quant);
+    if (rc != CSA2_OK) return rc < 0 ? CSA2_OK : rc;
+    return launch_split_kv("sparse_attn_mma", p, B, quant, q, sink, win, n_tokens, comp,
+                           comp_scales, idx, out, workspace, dev_status, stream);
 }
 
 // ---------------------------------------------------------------------------
-// No-allocation variant. Its split-KV scratch lives in this file-scope device
-// array, so the caller passes no workspace. Some callers cannot allocate device
-// memory at all: a serving engine that has already handed the free HBM to its
-// own pool (the KV cache is sized to fill it), or a latency-critical path where
-// a cudaMalloc/cudaFree would synchronise the device. The array holds the
-// partial outputs of at most kNoAllocMaxBatch sequences (the pages' serving
-// batch, max-num-seqs 32): 32 x 657,920 B = 21,053,440 B, held by every GPU that
-// loads the library until the process exits.
+// No-allocation variant. Its scratch (the partial results of csa2_sparse_attn's
+// schedules) lives in this file-scope device array, so the caller passes no
+// workspace. Some callers cannot allocate device memory at all: a serving engine
+// that has already handed the free HBM to its own pool (the KV cache is sized to
+// fill it), or a latency-critical path where a cudaMalloc/cudaFree would
+// synchronise the device. The array holds the partials of at most
+// kNoAllocMaxBatch sequences (the pages' serving batch, max-num-seqs 32): the
+// fp32 split-KV passes need 32 x 657,920 B = 21,053,440 B, the tcgen05
+// schedule of the quantised formats at most 31 cut units x 263,168 B + counts,
+// and every GPU that loads the library holds the array until the process exits.
 // ---------------------------------------------------------------------------
 #include <mutex>
 
@@ -853,6 +882,12 @@ std::mutex g_noalloc_mu;
 void* g_noalloc_ptr[kMaxDevices] = {};
 }  // namespace
 
+// the tcgen05 schedule's need for B <= 32: at most 31 boundary slots of two
+// partials (64 x 512 outputs + 64 maxima + 64 sums, fp32) after 256 B of counts
+static_assert(256 + 31 * 2 * (csa2::kH * csa2::kD + 2 * csa2::kH) * sizeof(float) <=
+                  kNoAllocScratchBytes,
+              "no-allocation scratch too small for the tcgen05 schedule");
+
 static __device__ __align__(256) unsigned char g_sparse_attn_scratch[kNoAllocScratchBytes];
 
 extern "C" int csa2_sparse_attn_noalloc(const csa2_params* p, int B, const void* q,
@@ -860,6 +895,8 @@ extern "C" int csa2_sparse_attn_noalloc(const csa2_params* p, int B, const void*
                                         const int32_t* n_tokens, const void* const* comp,
                                         const uint8_t* const* comp_scales, const int32_t* idx,
                                         void* out, int32_t* dev_status, void* stream) {
+    CSA2_CHECK_PARAMS(p);
+    if (B < 0) return fail(CSA2_ERR_INVALID_ARG, "sparse_attn_noalloc: negative batch");
     if (B > kNoAllocMaxBatch)
         return fail(CSA2_ERR_UNSUPPORTED,
                     "sparse_attn_noalloc: at most 32 sequences per call (the built-in scratch "

@@ -804,17 +804,6 @@ int launch_layers(const char* name, const csa2_params* p, int L, int B, int b0, 
         if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
             return fail(CSA2_ERR_ALIGN, n + ": workspace must be 256-byte aligned");
     }
-    {
-        static std::mutex mu;
-        static uint64_t attr_set = 0;
-        std::lock_guard<std::mutex> g(mu);
-        if (dev >= 0 && dev < 64 && !((attr_set >> dev) & 1u)) {
-            if (cudaFuncSetAttribute(k_sparse_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kAttnSmem) != cudaSuccess)
-                return check_launch((n + ": smem attribute").c_str());
-            attr_set |= 1ull << dev;
-        }
-    }
     UnitArgs a;
     a.L = L;
     a.B = B;
@@ -863,6 +852,36 @@ int launch_layers(const char* name, const csa2_params* p, int L, int B, int b0, 
 }  // namespace
 
 CSA2_TRACE_SETTER(trace_set_attn_tc)
+
+size_t sparse_attn_tc_ws_bytes(const csa2_params* p, int B) {
+    int dev = 0;
+    if (!p || B <= 0 || cudaGetDevice(&dev) != cudaSuccess) return 0;
+    return split_ws_bytes(split_slots(p, B, dev));
+}
+
+int sparse_attn_tc_single(const char* name, const csa2_params* p, int B, const void* q,
+                          const float* sink, const void* const* win, const int32_t* n_tokens,
+                          const void* const* comp, const uint8_t* const* comp_scales,
+                          const int32_t* idx, void* out, void* workspace, size_t ws_bytes,
+                          int32_t* dev_status, void* stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return check_launch(name);
+    const int64_t slots = split_slots(p, B, dev);
+    if (ws_bytes < split_ws_bytes(slots) || (slots > 0 && !workspace))
+        return fail(CSA2_ERR_SHAPE, std::string(name) + ": workspace smaller than the size query");
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(CSA2_ERR_ALIGN, std::string(name) + ": workspace must be 256-byte aligned");
+    if ((int64_t)B > (int64_t)1 << 28)
+        return fail(CSA2_ERR_UNSUPPORTED, std::string(name) + ": too many sequences");
+    if (const int rc = ensure_loaded()) return rc;
+    // the completion counts of the cut units start at zero on every call, so the
+    // caller's workspace needs no initialisation
+    if (slots > 0 && cudaMemsetAsync(workspace, 0, (size_t)slots * sizeof(int32_t),
+                                     static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return check_launch(name);
+    return launch_layers(name, p, 1, B, 0, B, q, sink, win, n_tokens, comp, comp_scales, idx, out,
+                         workspace, ws_bytes, true, dev_status, stream);
+}
 
 cudaError_t preload_attn_tc() { return preload_kernel(k_sparse_attn_tc, kAttnSmem); }
 

@@ -340,7 +340,13 @@ size_t csa2_sparse_attn_workspace_size(const csa2_params* p, int B);
  *   idx  [B, topk_pos] int32 (-1 = empty); an idx >= T/compress_ratio is
  *        skipped and sets CSA2_DEV_BAD_INDEX.
  *   workspace: device scratch of at least csa2_sparse_attn_workspace_size(p, B)
- *   bytes (partial outputs of the split-KV passes); contents need no init.
+ *   bytes, 256-byte aligned (partial results of the schedule below); contents
+ *   need no initialisation (the call clears what must start at zero, on the
+ *   stream). Calls that share a workspace must be ordered (one stream or events).
+ * Quantised formats (NVFP4 cache, E4M3 window, bf16 q/out) run on the tcgen05
+ * tensor cores: the kernel of csa2_sparse_attn_layers_split with one layer
+ * (f16 operands decoded exactly, fp32 accumulation in TMEM). The fp32 formats
+ * run on CUDA cores in 5 position splits per sequence merged by log-sum-exp.
  * Constraints: H == 64, D == 512, W == 128, topk_pos == 512.
  */
 int csa2_sparse_attn(const csa2_params* p, int B,
@@ -350,6 +356,21 @@ int csa2_sparse_attn(const csa2_params* p, int B,
                      const int32_t* idx, void* out,
                      void* workspace, size_t ws_bytes,
                      int32_t* dev_status, void* stream);
+
+/*
+ * csa2_sparse_attn_mma — csa2_sparse_attn on the legacy warp-level tensor-core
+ * path for the quantised formats (mma.sync bf16: 5 position splits per sequence
+ * with partials in the workspace, then a log-sum-exp merge; P rounded to bf16).
+ * Same arguments, workspace and results; kept as a second, independent
+ * implementation and ablation of the tcgen05 path. fp32 formats as csa2_sparse_attn.
+ */
+int csa2_sparse_attn_mma(const csa2_params* p, int B,
+                         const void* q, const float* sink,
+                         const void* const* win, const int32_t* n_tokens,
+                         const void* const* comp, const uint8_t* const* comp_scales,
+                         const int32_t* idx, void* out,
+                         void* workspace, size_t ws_bytes,
+                         int32_t* dev_status, void* stream);
 
 /*
  * csa2_sparse_attn_layers — csa2_sparse_attn for L layers that share one
@@ -452,8 +473,8 @@ int csa2_sparse_attn_layers_mma(const csa2_params* p, int L, int B,
  * latency-critical path where cudaMalloc/cudaFree would synchronise the device.
  * This entry point allocates nothing: its scratch is a fixed array inside the
  * library (21,053,440 bytes, enough for 32 sequences), held on every GPU that
- * loads the library until the process exits. Arguments and results are those
- * of csa2_sparse_attn, minus workspace/ws_bytes.
+ * loads the library until the process exits. Arguments, results and kernels are
+ * those of csa2_sparse_attn, minus workspace/ws_bytes.
  *   - B > 32 returns CSA2_ERR_UNSUPPORTED (nothing enqueued): split the batch.
  *   - The first call on a device looks up the array's device address (with that
  *     device current) and caches it; make that first call before any stream

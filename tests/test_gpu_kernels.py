@@ -473,21 +473,36 @@ def _attn_case(rng, Ts, f32, n_idx_valid):
     return p, cache, st, idx, q_dev, q64, sink
 
 
-@pytest.mark.parametrize("f32", [False, True])
-def test_sparse_attn_matches_oracle(f32):
+# csa2_sparse_attn's paths: (fp32 formats, mma_sync ablation entry, max_ctas). The
+# quantised formats run on tcgen05; with 3 CTAs the even split cuts 2 of the 8
+# units, whose pieces merge by log-sum-exp through the workspace.
+SINGLE_MODES = {
+    "tcgen05": (False, False, 0),
+    "tcgen05_3ctas": (False, False, 3),
+    "mma_sync": (False, True, 0),
+    "f32": (True, False, 0),
+}
+
+
+@pytest.mark.parametrize("mode", list(SINGLE_MODES))
+def test_sparse_attn_matches_oracle(mode):
+    f32, mma_sync, max_ctas = SINGLE_MODES[mode]
     rng = np.random.default_rng(7 if f32 else 8)
     Ts = [1, 50, 127, 128, 129, 1000, 4096, 1025]
     valid = [512, 512, 512, 100, 512, 512, 512, 0]
     p, cache, st, idx, q_dev, q64, sink = _attn_case(rng, Ts, f32, 512)
+    p.max_ctas = max_ctas
     for b, v in enumerate(valid):
         if v < 512:
             idx[b, rng.choice(512, 512 - v, replace=False)] = -1
     B = len(Ts)
     out = torch.empty(B, 64, 512, dtype=torch.float32 if f32 else torch.bfloat16, device=DEV)
-    ws = torch.empty(api.sparse_attn_workspace_size(p, B), dtype=torch.uint8, device=DEV)
+    # garbage in the workspace: the call must not depend on its contents
+    ws = torch.full((api.sparse_attn_workspace_size(p, B),), 0x5A, dtype=torch.uint8, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    api.sparse_attn(p, q_dev, t(sink), cache.win_ptrs, cache.n_tokens, cache.comp_ptrs,
-                    cache.comp_scale_ptrs, t(idx), out, ws, status)
+    for _ in range(2):  # twice: the cut units' counts are left clean for the next call
+        api.sparse_attn(p, q_dev, t(sink), cache.win_ptrs, cache.n_tokens, cache.comp_ptrs,
+                        cache.comp_scale_ptrs, t(idx), out, ws, status, mma_sync=mma_sync)
     torch.cuda.synchronize()
     assert status.item() == 0
     got = out.float().cpu().numpy().astype(np.float64)
