@@ -83,3 +83,58 @@ def test_planted_high_scores_are_selected_and_the_block_cut_binds():
     idx, m = orc.select(s, 8, 2048, 512)
     assert m == 512 and set(plants) <= set(idx.tolist())
     assert len(set(int(t) // 8 for t in idx)) <= 2048
+
+
+def flat_top(scores, Kp):
+    """The Kp best positions by (score desc, position asc), ascending."""
+    order = np.lexsort((np.arange(len(scores)), -scores.astype(np.float64)))
+    return np.sort(order[:Kp])
+
+
+def top_within_top_blocks(scores, blk, Kp):
+    """The Kp best positions among the positions of the Kp best blocks (blocks by
+    (block max desc, block asc)), ascending."""
+    n = len(scores)
+    nb = -(-n // blk)
+    bm = np.array([scores[b * blk:(b + 1) * blk].max() for b in range(nb)], np.float64)
+    blocks = np.lexsort((np.arange(nb), -bm))[:Kp]
+    cand = np.concatenate([np.arange(b * blk, min(n, b * blk + blk)) for b in np.sort(blocks)])
+    order = np.lexsort((cand, -scores[cand].astype(np.float64)))
+    return np.sort(cand[order[:Kp]])
+
+
+def test_two_levels_equal_the_flat_top_when_blocks_outnumber_positions():
+    # With the block score the maximum of its positions' scores and more blocks kept
+    # than positions (Kb - 1 >= Kp; the pages' 2047 >= 512), the two-level rule returns
+    # the Kp best positions overall, and those lie among the positions of the Kp best
+    # blocks: a best position's block ranks at least as high as that position, and
+    # the blocks of the Kp best positions form a top set of the block order, so the
+    # Kb - 1 best blocks other than the newest already contain them. The newest
+    # block, kept regardless, changes nothing then. (With Kb = Kp it can: the
+    # brute-force test above covers that regime.)
+    rng = np.random.default_rng(3)
+    for trial in range(300):
+        n = int(rng.integers(1, 200))
+        blk = int(rng.integers(1, 5))
+        Kp = int(rng.integers(1, 12))
+        Kb = Kp + 1 + int(rng.integers(0, 6))
+        s = rng.integers(0, int(rng.integers(1, 7)), n).astype(np.float32)
+        if trial % 3 == 0:
+            s[(n - 1) // blk * blk:] = -9.0  # the newest block is the worst
+        idx, m = orc.select(s, blk, Kb, Kp)
+        ref = flat_top(s, Kp)
+        assert m == len(ref) and np.array_equal(idx[:m], ref), (trial, n, blk, Kb, Kp)
+        assert np.array_equal(top_within_top_blocks(s, blk, Kp), ref), trial
+
+
+def test_two_levels_equal_the_flat_top_at_the_pages_sizes():
+    rng = np.random.default_rng(4)
+    for n in (16385, 20011, 65536):  # 2,049 to 8,192 blocks of 8
+        for levels in (3, 50, 0):
+            s = (rng.integers(0, levels, n).astype(np.float32) if levels
+                 else rng.standard_normal(n).astype(np.float32))
+            s[(n - 1) // 8 * 8:] = -100.0  # newest block last
+            idx, m = orc.select(s, 8, 2048, 512)
+            ref = flat_top(s, 512)
+            assert m == 512 and np.array_equal(idx, ref), (n, levels)
+            assert np.array_equal(top_within_top_blocks(s, 8, 512), ref), (n, levels)
