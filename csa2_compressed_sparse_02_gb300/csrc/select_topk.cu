@@ -4,6 +4,12 @@
 // blocks kept with the block of the newest position always kept; then the
 // top-512 positions inside the kept blocks.
 //
+// With the block score the best position's score and 2,047 > 512, that rule
+// returns the 512 best positions of the sequence, and they lie in the 512 best
+// blocks (see k_select_topk). So level 1 here keeps the 512 best blocks and
+// level 2 selects among their at most 4,096 positions: the same positions,
+// found with a quarter of the block keys kept and of the scores gathered.
+//
 // One CTA of 1024 threads per sequence. Each level is an exact radix select
 // on order-preserving u32 keys (four 8-bit digit passes with a shared-memory
 // histogram, the digit found by one warp's scan), then an ordered pass that
@@ -11,13 +17,15 @@
 // the candidate keys in shared memory; its candidate list is ascending by
 // position, so the output comes out ascending by construction.
 //
-// Level 1 keeps 2,047 of up to 65,535 blocks, so it first narrows the field:
+// Level 1 keeps 512 of up to 131,072 blocks, so it first narrows the field:
 // a threshold estimated from a strided sample of 2,048 block maxima, one pass
 // that keeps the blocks at or above it (in index order, in shared memory), and
-// the exact select among those. The answer is unchanged because the top 2,047
-// all lie at or above any threshold that at least 2,047 blocks reach; when the
-// count falls outside [2,047, kMaxFiltered] the threshold moves, and after a
-// few tries the exact select runs over all blocks in global memory.
+// the exact select among those. The answer is unchanged because the top 512
+// all lie at or above any threshold that at least 512 blocks reach; when the
+// count falls outside [512, kMaxFiltered] the threshold moves, and after a
+// few tries the exact select runs over all blocks in global memory. Level 2
+// keeps the positions at or above the 512th block's maximum (the kept blocks'
+// own maxima already reach it, so the 512 best do) before its exact select.
 #include "common.cuh"
 #include "sm100.cuh"
 
@@ -31,8 +39,7 @@ constexpr int kMaxCand = kKb * kBlk;  // 16384
 
 constexpr int kSample = 2048;
 constexpr int kMaxFiltered = 8192;
-constexpr int kSample2 = 1024;       // level 2 sample (stored at the end of cand_idx)
-constexpr int kMaxFiltered2 = 4096;
+constexpr int kMaxFiltered2 = kKp * kBlk;  // level 2: every candidate of the kKp kept blocks
 constexpr int kStagePerWarp = 256;   // kept pairs a warp stages during the vector filter's pass
 
 struct SelShared {
@@ -147,7 +154,7 @@ __device__ uint32_t warp_excl_scan(uint32_t v, SelShared& sh, uint32_t* total) {
 // contiguous range of indices and walks it 32 at a time (coalesced), so tie
 // ranks and output ranks follow index order via ballots.
 template <class KeyAt, class Emit>
-__device__ void select_top(int n, int K, KeyAt key_at, Emit emit, SelShared& sh) {
+__device__ uint32_t select_top(int n, int K, KeyAt key_at, Emit emit, SelShared& sh) {
     int need_eq;
     const uint32_t kth = radix_kth(n, K, key_at, sh, &need_eq);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -178,6 +185,7 @@ __device__ void select_top(int n, int K, KeyAt key_at, Emit emit, SelShared& sh)
         r_eq += __popc(eqm);
     }
     __syncthreads();
+    return kth;
 }
 
 
@@ -346,21 +354,30 @@ k_select_topk(int64_t max_ncomp, int ratio, const float* __restrict__ scores,
     int32_t* out = idx + (int64_t)b * kKp;
     const int n_b = (n_c + kBlk - 1) / kBlk;
 
-    // ---- level 1: kept blocks, ascending ----
+    // The two levels' result is the kKp best positions of the sequence by (score
+    // desc, position asc): a best position's block ranks at least as high as the
+    // position itself (its block maximum is at least its score, ties going to the
+    // lower block as to the lower position), so the blocks holding the kKp best
+    // positions are the top of the block order, and the kKb - 1 best blocks other
+    // than the newest (kKb - 1 >= kKp) hold all of them whatever the newest block
+    // scores. The kernel therefore keeps the kKp best blocks (over all blocks) and
+    // selects among their at most 8 kKp positions, which gives the same positions
+    // as keeping kKb blocks and selecting among 8 kKb.
+    // ---- level 1: the kKp best blocks, ascending ----
     int n_kept;
-    if (n_b <= kKb) {
+    uint32_t thr2 = 0u;  // a key the kKp-th best position reaches
+    if (n_b <= kKp) {
         for (int i = tid; i < n_b; i += kThreads) sh.kept[i] = i;
         n_kept = n_b;
     } else {
-        // best K_b - 1 among blocks [0, n_b - 1), then the newest block n_b - 1
-        const int n1 = n_b - 1, K1 = kKb - 1;
+        const int K1 = kKp;
         const bool vec_ok = (reinterpret_cast<uintptr_t>(bm) & 15u) == 0;
         // (a) threshold from a strided sample: the r-th largest sample key, r chosen so
-        //     that about 1.5 K1 blocks of all n1 reach it
+        //     that about 1.5 K1 blocks of all n_b reach it
         for (int i = tid; i < kSample; i += kThreads)
-            sh.cand[kMaxCand - kSample + i] = score_key(bm[(int64_t)i * n1 / kSample]);
+            sh.cand[kMaxCand - kSample + i] = score_key(bm[(int64_t)i * n_b / kSample]);
         __syncthreads();
-        int r = (int)(1.5f * K1 * kSample / n1) + 1;
+        int r = (int)(1.5f * K1 * kSample / n_b) + 1;
         bool done = false;
         for (int attempt = 0; attempt < 4 && !done; ++attempt) {
             r = max(1, min(kSample, r));
@@ -368,10 +385,10 @@ k_select_topk(int64_t max_ncomp, int ratio, const float* __restrict__ scores,
             // the top 16 bits of the r-th largest sample key: a slightly lower threshold
             const uint32_t thr = radix_kth(kSample, r, [&](int i) { return sh.cand[kMaxCand - kSample + i]; },
                                            sh, &unused, 2);
-            int total = vec_ok ? filter_ge_vec(n1, thr, bm, sh.cand, sh.cand_idx, kMaxFiltered, sh) : -1;
+            int total = vec_ok ? filter_ge_vec(n_b, thr, bm, sh.cand, sh.cand_idx, kMaxFiltered, sh) : -1;
             if (total < 0)
                 total = filter_ge(
-                    n1, thr, [&](int i) { return score_key(bm[i]); }, sh.cand, sh.cand_idx,
+                    n_b, thr, [&](int i) { return score_key(bm[i]); }, sh.cand, sh.cand_idx,
                     kMaxFiltered, sh);
             if (total < K1) {          // threshold too high: take a lower sample rank
                 r = r * 2 + 8;
@@ -382,25 +399,25 @@ k_select_topk(int64_t max_ncomp, int ratio, const float* __restrict__ scores,
                 r = r / 2;
                 continue;
             }
-            select_top(
+            thr2 = select_top(
                 total, K1, [&](int i) { return sh.cand[i]; },
                 [&](uint32_t rank, int i) { sh.kept[rank] = sh.cand_idx[i]; }, sh);
             done = true;
         }
         if (!done) {  // exact select over every block, read from global memory
             __syncthreads();
-            select_top(
-                n1, K1, [&](int i) { return score_key(bm[i]); },
+            thr2 = select_top(
+                n_b, K1, [&](int i) { return score_key(bm[i]); },
                 [&](uint32_t rank, int i) { sh.kept[rank] = i; }, sh);
         }
-        if (tid == 0) sh.kept[kKb - 1] = n_b - 1;
-        n_kept = kKb;
+        n_kept = K1;
     }
     __syncthreads();
 
-    // ---- level 2: positions of the kept blocks ----
-    // the last kept block is block n_b - 1, the only one that may be partial
-    const int n_cand = n_kept == 0 ? 0 : (n_kept - 1) * kBlk + (n_c - (n_b - 1) * kBlk);
+    // ---- level 2: positions of the kept blocks (block n_b - 1, the only one that
+    // may be partial, comes last when kept) ----
+    const int n_cand = n_kept == 0 ? 0
+                                   : n_kept * kBlk - (sh.kept[n_kept - 1] == n_b - 1 ? n_b * kBlk - n_c : 0);
     if ((reinterpret_cast<uintptr_t>(sc) & 15u) == 0) {
         // blocks are 8 consecutive scores (32 bytes): two 16-byte loads per block
         for (int q = tid; q < 2 * n_kept; q += kThreads) {
@@ -424,43 +441,14 @@ k_select_topk(int64_t max_ncomp, int ratio, const float* __restrict__ scores,
     if (n_cand <= kKp) {
         for (int i = tid; i < n_cand; i += kThreads) out[i] = pos_of(i);
     } else {
-        // sample -> threshold -> filter -> exact select, as at level 1
-        bool done = false;
-        if (n_cand > 2 * kSample2) {
-            uint32_t* sample = reinterpret_cast<uint32_t*>(sh.cand_idx) + kMaxFiltered - kSample2;
-            for (int i = tid; i < kSample2; i += kThreads)
-                sample[i] = sh.cand[(int64_t)i * n_cand / kSample2];
-            __syncthreads();
-            int r = (int)(1.5f * kKp * kSample2 / n_cand) + 1;
-            for (int attempt = 0; attempt < 4 && !done; ++attempt) {
-                r = max(1, min(kSample2, r));
-                int unused;
-                const uint32_t thr = radix_kth(kSample2, r, [&](int i) { return sample[i]; }, sh,
-                                               &unused, 2);
-                const int total = filter_ge(
-                    n_cand, thr, [&](int i) { return sh.cand[i]; }, sh.cand2, sh.cand_idx,
-                    kMaxFiltered2, sh);
-                if (total < kKp) {
-                    r = r * 2 + 8;
-                    continue;
-                }
-                if (total > kMaxFiltered2) {
-                    if (r <= 1) break;
-                    r = r / 2;
-                    continue;
-                }
-                select_top(
-                    total, kKp, [&](int i) { return sh.cand2[i]; },
-                    [&](uint32_t rank, int i) { out[rank] = pos_of(sh.cand_idx[i]); }, sh);
-                done = true;
-            }
-        }
-        if (!done) {
-            __syncthreads();
-            select_top(
-                n_cand, kKp, [&](int i) { return sh.cand[i]; },
-                [&](uint32_t rank, int i) { out[rank] = pos_of(i); }, sh);
-        }
+        // at least kKp positions reach the kKp-th best block's maximum (the kept
+        // blocks' own maxima), so the kKp best all sit at or above it; the
+        // candidates (at most 8 kKp) always fit the filter's capacity
+        const int total = filter_ge(
+            n_cand, thr2, [&](int i) { return sh.cand[i]; }, sh.cand2, sh.cand_idx, kMaxFiltered2, sh);
+        select_top(
+            total, kKp, [&](int i) { return sh.cand2[i]; },
+            [&](uint32_t rank, int i) { out[rank] = pos_of(sh.cand_idx[i]); }, sh);
     }
     if (tid == 0 && n_sel_out) n_sel_out[b] = min(n_cand, kKp);
     trace_end(kTraceSelect);
