@@ -10,7 +10,10 @@
 // level 2 selects among their at most 4,096 positions: the same positions,
 // found with a quarter of the block keys kept and of the scores gathered.
 //
-// One CTA of 1024 threads per sequence. Each level is an exact radix select
+// One CTA of 1024 threads per sequence, or, for a small batch, a cluster of 4
+// CTAs per sequence whose level-1 pass over the block maxima is split in
+// quarters (counts and candidates exchanged through distributed shared memory,
+// every wait bounded), CTA 0 finishing alone. Each level is an exact radix select
 // on order-preserving u32 keys (four 8-bit digit passes with a shared-memory
 // histogram, the digit found by one warp's scan), then an ordered pass that
 // takes the tied elements with the lowest indices. Level 2 works on a copy of
@@ -35,23 +38,30 @@ using namespace sm100;
 
 constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxCand = kKb * kBlk;  // 16384
 
 constexpr int kSample = 2048;
 constexpr int kMaxFiltered = 8192;
 constexpr int kMaxFiltered2 = kKp * kBlk;  // level 2: every candidate of the kKp kept blocks
+constexpr int kMaxCand = kMaxFiltered + kSample;  // level 1: filtered keys, sample at the end
 constexpr int kStagePerWarp = 256;   // kept pairs a warp stages during the vector filter's pass
+constexpr int kClMax = 4;            // CTAs of one sequence in the cluster launch
+constexpr int kAttempts = 4;         // thresholds tried before the exact select over every block
 
 struct SelShared {
     uint32_t hist[256];
     uint32_t warp_sum[kWarps];
     int32_t bcast[4];
-    int32_t kept[kKb];
-    uint32_t cand[kMaxCand];        // level 2 keys; level 1: filtered keys, sample at the end
-    int32_t cand_idx[kMaxFiltered];  // index of each filtered key; level 2 sample at the end
+    int32_t kept[kKp];
+    uint32_t cand[kMaxCand];        // level 1: filtered keys (sample at the end); level 2 keys
+    int32_t cand_idx[kMaxFiltered];  // index of each filtered key
     uint32_t cand2[kMaxFiltered2];   // level 2 filtered keys
     uint32_t stage_key[kWarps * kStagePerWarp];  // level 1 filter: kept pairs per warp, in order
     int32_t stage_idx[kWarps * kStagePerWarp];
+    // cluster launch: each CTA's level-1 candidate count, per attempt, written into
+    // every CTA of the cluster; cnt_bar completes a phase per attempt once all CTAs
+    // wrote theirs, gat_bar (CTA 0) once the others copied their candidates in
+    uint32_t cl_cnt[kAttempts][kClMax];
+    uint64_t cnt_bar, gat_bar;
 };
 
 __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
@@ -332,16 +342,31 @@ __device__ int filter_ge_vec(int n, uint32_t thr, const float* __restrict__ bm, 
     return (int)total;
 }
 
+// ncl CTAs per sequence (1, or kClMax in a cluster launch): with a cluster, every
+// CTA filters a quarter of the block maxima at level 1 and CTA 0 (rank 0 of the
+// cluster) finishes the sequence alone once the others have copied their
+// candidates into its shared memory.
 __global__ void __launch_bounds__(kThreads, 1)
 k_select_topk(int64_t max_ncomp, int ratio, const float* __restrict__ scores,
               const float* __restrict__ block_max, const int32_t* __restrict__ n_tokens,
-              int32_t* idx, int32_t* n_sel_out, int32_t* dev_status) {
+              int32_t* idx, int32_t* n_sel_out, int32_t* dev_status, int ncl) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
     SelShared& sh = *reinterpret_cast<SelShared*>(smem_raw);
-    const int b = blockIdx.x, tid = threadIdx.x;
+    const int b = blockIdx.x / ncl, tid = threadIdx.x;
+    const int rank = ncl > 1 ? (int)cluster_ctarank() : 0;
     trace_start(kTraceSelect);
     // the attention after it may be scheduled now (it waits for this grid first)
     grid_dep_launch_dependents();
+    if (ncl > 1) {
+        if (tid == 0) {
+            mbar_init(&sh.cnt_bar, (uint32_t)ncl);
+            mbar_init(&sh.gat_bar, (uint32_t)(ncl - 1));
+            fence_mbar_init();
+        }
+        // every CTA of the cluster has started and initialised its barriers before
+        // any of them touches another's shared memory
+        cluster_sync_all();
+    }
     int64_t n_c64 = n_tokens[b] / ratio;
     if (n_c64 > max_ncomp || n_c64 < 0) {
         if (tid == 0) raise_status(dev_status, CSA2_DEV_BAD_LENGTH);
@@ -367,29 +392,55 @@ k_select_topk(int64_t max_ncomp, int ratio, const float* __restrict__ scores,
     int n_kept;
     uint32_t thr2 = 0u;  // a key the kKp-th best position reaches
     if (n_b <= kKp) {
+        if (rank > 0) return;  // the cluster's other CTAs have nothing to do
         for (int i = tid; i < n_b; i += kThreads) sh.kept[i] = i;
         n_kept = n_b;
     } else {
         const int K1 = kKp;
+        // this CTA's blocks [lo, hi): whole 128-block chunks, so bm + lo stays 16-byte aligned
+        const int span = ((n_b + ncl - 1) / ncl + 127) / 128 * 128;
+        const int lo = min(n_b, rank * span), hi = min(n_b, lo + span);
         const bool vec_ok = (reinterpret_cast<uintptr_t>(bm) & 15u) == 0;
-        // (a) threshold from a strided sample: the r-th largest sample key, r chosen so
-        //     that about 1.5 K1 blocks of all n_b reach it
+        // (a) threshold from a strided sample of all n_b blocks: the r-th largest sample
+        //     key, r chosen so that about 1.5 K1 blocks reach it (every CTA of a cluster
+        //     computes the same one)
         for (int i = tid; i < kSample; i += kThreads)
             sh.cand[kMaxCand - kSample + i] = score_key(bm[(int64_t)i * n_b / kSample]);
         __syncthreads();
         int r = (int)(1.5f * K1 * kSample / n_b) + 1;
         bool done = false;
-        for (int attempt = 0; attempt < 4 && !done; ++attempt) {
+        for (int attempt = 0; attempt < kAttempts && !done; ++attempt) {
             r = max(1, min(kSample, r));
             int unused;
             // the top 16 bits of the r-th largest sample key: a slightly lower threshold
             const uint32_t thr = radix_kth(kSample, r, [&](int i) { return sh.cand[kMaxCand - kSample + i]; },
                                            sh, &unused, 2);
-            int total = vec_ok ? filter_ge_vec(n_b, thr, bm, sh.cand, sh.cand_idx, kMaxFiltered, sh) : -1;
-            if (total < 0)
-                total = filter_ge(
-                    n_b, thr, [&](int i) { return score_key(bm[i]); }, sh.cand, sh.cand_idx,
+            // (b) this CTA's blocks at or above it, in index order (indices from lo)
+            const float* bml = bm + lo;
+            int mine = vec_ok ? filter_ge_vec(hi - lo, thr, bml, sh.cand, sh.cand_idx, kMaxFiltered, sh) : -1;
+            if (mine < 0)
+                mine = filter_ge(
+                    hi - lo, thr, [&](int i) { return score_key(bml[i]); }, sh.cand, sh.cand_idx,
                     kMaxFiltered, sh);
+            // (c) the count over the cluster, the same in every CTA
+            int total = mine, before = 0;
+            if (ncl > 1) {
+                if (tid == 0) {
+                    const uint32_t slot = smem_u32(&sh.cl_cnt[attempt][rank]);
+                    for (int m = 0; m < ncl; ++m) st_cluster_u32(mapa_shared(slot, (uint32_t)m), (uint32_t)mine);
+                    for (int m = 0; m < ncl; ++m) mbar_arrive_cluster(mapa_shared(smem_u32(&sh.cnt_bar), (uint32_t)m));
+                }
+                if (!mbar_wait_cluster(&sh.cnt_bar, (uint32_t)(attempt & 1))) {
+                    if (tid == 0) raise_status(dev_status, CSA2_DEV_TIMEOUT);
+                    return;
+                }
+                total = 0;
+                for (int m = 0; m < ncl; ++m) {
+                    const int c = (int)sh.cl_cnt[attempt][m];
+                    if (m < rank) before += c;
+                    total += c;
+                }
+            }
             if (total < K1) {          // threshold too high: take a lower sample rank
                 r = r * 2 + 8;
                 continue;
@@ -399,16 +450,36 @@ k_select_topk(int64_t max_ncomp, int ratio, const float* __restrict__ scores,
                 r = r / 2;
                 continue;
             }
+            if (ncl > 1) {
+                // (d) the candidates of CTA k go to CTA 0 at the count of CTAs < k (CTA 0's
+                //     own are in place), in index order
+                if (rank > 0) {
+                    for (int i = tid; i < mine; i += kThreads) {
+                        st_cluster_u32(mapa_shared(smem_u32(&sh.cand[before + i]), 0u), sh.cand[i]);
+                        st_cluster_u32(mapa_shared(smem_u32(&sh.cand_idx[before + i]), 0u),
+                                       (uint32_t)(sh.cand_idx[i] + lo));
+                    }
+                    asm volatile("fence.acq_rel.cluster;\n" ::: "memory");
+                    __syncthreads();
+                    if (tid == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&sh.gat_bar), 0u));
+                    return;
+                }
+                if (!mbar_wait_cluster(&sh.gat_bar, 0u)) {
+                    if (tid == 0) raise_status(dev_status, CSA2_DEV_TIMEOUT);
+                    return;
+                }
+            }
             thr2 = select_top(
                 total, K1, [&](int i) { return sh.cand[i]; },
-                [&](uint32_t rank, int i) { sh.kept[rank] = sh.cand_idx[i]; }, sh);
+                [&](uint32_t rank_, int i) { sh.kept[rank_] = sh.cand_idx[i]; }, sh);
             done = true;
         }
-        if (!done) {  // exact select over every block, read from global memory
+        if (!done) {  // exact select over every block, read from global memory (CTA 0)
+            if (rank > 0) return;
             __syncthreads();
             thr2 = select_top(
                 n_b, K1, [&](int i) { return score_key(bm[i]); },
-                [&](uint32_t rank, int i) { sh.kept[rank] = i; }, sh);
+                [&](uint32_t rank_, int i) { sh.kept[rank_] = i; }, sh);
         }
         n_kept = K1;
     }
@@ -481,7 +552,29 @@ extern "C" int csa2_select_topk(const csa2_params* p, int B, int64_t max_ncomp,
     // loads the kernel and sets its shared-memory limit on this device, once per device
     if (const int rc = ensure_loaded()) return rc;
     const int smem = (int)sizeof(SelShared);
-    k_select_topk<<<B, kThreads, smem, static_cast<cudaStream_t>(stream)>>>(
-        max_ncomp, p->compress_ratio, scores, block_max, n_tokens, idx, n_sel, dev_status);
+    // A small batch leaves most SMs idle with one CTA per sequence: then each
+    // sequence's level-1 pass over its block maxima is spread over a cluster of
+    // kClMax CTAs, when the grid stays within p->max_ctas (0: two waves of the SMs).
+    int dev = 0, sms = 1;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return check_launch("select_topk: device");
+    const int64_t cta_cap = p->max_ctas > 0 ? p->max_ctas : 2 * (int64_t)sms;
+    const int ncl = (int64_t)B * kClMax <= cta_cap ? kClMax : 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(B * ncl));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)ncl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, k_select_topk, max_ncomp, p->compress_ratio, scores, block_max,
+                           n_tokens, idx, n_sel, dev_status, ncl) != cudaSuccess)
+        return check_launch("select_topk");
     return check_launch("select_topk");
 }

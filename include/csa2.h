@@ -87,7 +87,9 @@ typedef struct csa2_params {
     int max_ctas;         /* upper bound on the CTAs of the persistent kernels
                              (csa2_index_scores, csa2_sparse_attn_layers); 0 = one
                              per SM. A caller that runs two of them concurrently on
-                             different streams splits the SMs with it. */
+                             different streams splits the SMs with it. Also
+                             csa2_select_topk spreads each sequence over a cluster
+                             of 4 CTAs only when 4 B <= max_ctas (0: 2 x SMs). */
     /* Rotary embedding of the compressed KV, applied by csa2_compress_append
      * ("CSA2稀疏注意力、384专家MoE与1M上下文" §2.2 compress_rope_theta, §四
      * rope_scaling yarn; "DeepSeek-V4.1-Flash-NVFP4" §3.2). Compressed row j is
@@ -320,6 +322,11 @@ int csa2_index_scores_cuda_cores(const csa2_params* p, int B, int64_t max_ncomp,
  *   idx   [B, topk_pos] int32 out: kept positions ascending, then -1 padding.
  *   n_sel [B] int32 out: number of valid entries (may be NULL).
  * Scores compare as fp32 values (-0 == +0). Ties are resolved exactly.
+ * Because the block score is its best position's and topk_blocks - 1 >=
+ * topk_pos, the result is the topk_pos best positions of the sequence; the
+ * kernel finds them among the positions of the topk_pos best blocks. A small
+ * batch (4 B <= max_ctas, or 2 x SMs) runs each sequence on a cluster of 4 CTAs
+ * that share the pass over the block maxima through distributed shared memory.
  */
 int csa2_select_topk(const csa2_params* p, int B, int64_t max_ncomp,
                      const float* scores, const float* block_max, const int32_t* n_tokens,

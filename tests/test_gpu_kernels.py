@@ -397,10 +397,13 @@ def test_index_scores_clip_and_status_when_length_exceeds_max():
 
 
 # --------------------------------------------------------------------------- selection
+@pytest.mark.parametrize("cluster", [True, False], ids=["cluster4", "one_cta"])
 @pytest.mark.parametrize("levels,pad", [(3, 0), (50, 0), (0, 0), (0, 4)])
-def test_select_topk_exact_with_ties(levels, pad):
+def test_select_topk_exact_with_ties(levels, pad, cluster):
     """pad = 0: every row 16-byte aligned (vector loads where a sequence has at most
-    65,536 blocks); pad = 4: odd rows misaligned (scalar loads)."""
+    65,536 blocks); pad = 4: odd rows misaligned (scalar loads). cluster: each
+    sequence on a cluster of 4 CTAs (the small-batch launch), else on one CTA
+    (max_ctas below 4 B forces it)."""
     rng = np.random.default_rng(levels + 5)
     n_cs = [0, 1, 5, 511, 512, 513, 4095, 16384, 16385, 20000, 70001, 524288, 600000]
     B, max_nc = len(n_cs), max(n_cs) + pad
@@ -418,12 +421,15 @@ def test_select_topk_exact_with_ties(levels, pad):
         pad = np.full(math.ceil(n / 8) * 8, -np.inf, np.float32)
         pad[:n] = scores[b, :n]
         bm[b, :len(pad) // 8] = pad.reshape(-1, 8).max(1) if n else bm[b, :0]
-    p = api.default_params()
+    p = api.default_params(max_ctas=0 if cluster else B)
     idx = torch.full((B, 512), 123, dtype=torch.int32, device=DEV)
     n_sel = torch.zeros(B, dtype=torch.int32, device=DEV)
-    api.select_topk(p, max_nc, t(scores), t(bm), t(np.array([2 * n for n in n_cs], np.int32)),
-                    idx, n_sel)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    for _ in range(2):  # twice: the launch leaves nothing behind that the next one reads
+        api.select_topk(p, max_nc, t(scores), t(bm), t(np.array([2 * n for n in n_cs], np.int32)),
+                        idx, n_sel, status)
     torch.cuda.synchronize()
+    assert status.item() == 0
     gi, gn = idx.cpu().numpy(), n_sel.cpu().numpy()
     for b, n in enumerate(n_cs):
         ref, m = orc.select(scores[b, :n], 8, 2048, 512)
