@@ -182,7 +182,7 @@ def cpu_threads():
 
 
 def cpu_baseline(cfg, budget_units=None):
-    threads = max(1, min(cpu_threads(), 16))
+    threads = cpu_threads()  # every host core this process may run on
     n = budget_units or threads
     units = [(i % cfg.groups, (7 * i) % cfg.B) for i in range(n)]
     secs, cores = oracle_units(cfg, units, threads)
@@ -190,7 +190,7 @@ def cpu_baseline(cfg, budget_units=None):
     units_per_step = cfg.B * cfg.groups
     # `cores` units run concurrently, one per core
     value = cfg.B * cores / (per_unit * units_per_step)
-    return {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+    return {"value": value, "unit": UNIT, "cores": cores, "nproc": os.cpu_count(), "kind": "oracle",
             "sample": "%d (group, sequence) units of step 0 (Indexer over all %d compressed "
                       "positions, selection, compressed rows of the 512 selected, %d attention "
                       "layers), %d in parallel; mean %.2f s per unit; scaled to %d units per step"
@@ -201,7 +201,7 @@ def cpu_baseline(cfg, budget_units=None):
 def run_reference(args, cfg, rank):
     if rank != 0:
         return
-    threads = max(1, min(cpu_threads(), 8))
+    threads = cpu_threads()  # every host core this process may run on, as the GPU arm's baseline
     per = []
     for _ in range(args.warmup):
         oracle_units(cfg, [(0, 0)], 1)
@@ -220,7 +220,12 @@ def run_reference(args, cfg, rank):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": cfg.workload, "B": cfg.B,
                                             "T": cfg.first_lengths()[0]},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "ms_per_step_extrapolated": True,
+            "extrapolation": "each timed step runs %d (group, sequence) units of the %d a step "
+                             "has, one per core; ms_per_step and value scale the mean unit time "
+                             "to the whole step" % (threads, cfg.B * cfg.groups),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "nproc": os.cpu_count(),
+                             "kind": "oracle",
                              "sample": "per step %d (group, sequence) units in parallel; "
                                        "scaled to %d units per step" % (threads, cfg.B * cfg.groups)},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -237,6 +242,8 @@ def main():
     ap.add_argument("--config", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the FP4 MMA rate, prefill chunk and ragged-run keys")
     ap.add_argument("--nvtx", action="store_true", help="mark the timed steps with an NVTX range")
     ap.add_argument("--eager", action="store_true", help="launch kernels one by one (no CUDA graph)")
     ap.add_argument("--whole-unit-attn", action="store_true",
@@ -419,6 +426,17 @@ def main():
     }
     if e2e:
         line["e2e"] = e2e
+    if rank == 0 and not args.no_extras:
+        # secondary workloads, after the timed region: the FP4 tensor rate, the
+        # prefill chunk (configuration 4) and the ragged 16-step run (configuration 5)
+        del run
+        torch.cuda.empty_cache()
+        phase("FP4 MMA rate")
+        line["fp4_peak"] = fp4_peak(torch)
+        phase("prefill chunk (configuration 4)")
+        line["prefill"] = prefill_summary(torch, line["fp4_peak"]["tflops"])
+        phase("ragged decode, 16 steps (configuration 5)")
+        line["config5"] = config5_summary(torch)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         phase("oracle baseline on the host cores")
         line["cpu_baseline"] = cpu_baseline(cfg)
@@ -474,6 +492,102 @@ def prefill_main(args):
         "ms_per_step_by_call": {c: sum(a.elapsed_time(b) for a, b in evs) / K
                                 for c, evs in timers.items()},
         "clocks": clk.summary(), "gpu_launches": None}), flush=True)
+
+
+def fp4_peak(torch, iters=20000, launches=4):
+    """The block-scaled FP4 MMA rate (csa2_fp4_mma_peak: the prefill Indexer's
+    instruction, M = N = 128, K = 64, one CTA per SM), timed with CUDA events."""
+    from csa2_compressed_sparse_02_gb300 import api
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.fp4_mma_peak(sms, 1000, st)  # warm-up
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(launches):
+        api.fp4_mma_peak(sms, iters, st)
+    b.record()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0, "fp4_mma_peak status %d" % int(st.item())
+    flops = launches * sms * iters * 2.0 * 128 * 128 * 128
+    tflops = flops / (a.elapsed_time(b) / 1e3) / 1e12
+    return {"tflops": tflops, "shape": "tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X, "
+            "M=128 N=128 K=64, operands in shared memory, one CTA per SM, back to back",
+            "ctas": sms, "iters": iters, "source": "measured in this run"}
+
+
+def prefill_summary(torch, peak_tflops, chunks=3):
+    """Configuration 4 (8,192 prefill queries on a 262,144-token context), timed
+    after the decode line: chunk tokens/s, the per-call split, and the Indexer's
+    FP4 contraction rate against the measured FP4 MMA rate."""
+    from csa2_compressed_sparse_02_gb300 import workloads
+    from csa2_compressed_sparse_02_gb300.inputs import DI, HI, PREFILL
+    run = workloads.PrefillRun(PREFILL)
+    for _ in range(2):
+        run.reset()
+        run.run()
+    torch.cuda.synchronize()
+    timers = {}
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(chunks):
+        run.reset()
+        run.run(timers)
+    b.record()
+    torch.cuda.synchronize()
+    assert int(run.dev_status.item()) == 0, "device status %d" % int(run.dev_status.item())
+    per_chunk = a.elapsed_time(b) / 1e3 / chunks
+    split = {c: sum(x.elapsed_time(y) for x, y in evs) / chunks for c, evs in timers.items()}
+    # FP4 contraction of the Indexer: 32 heads x 128 dims per visible compressed position
+    n = PREFILL.chunk
+    visible = sum((PREFILL.T0 + i + 1) // PREFILL.ratio for i in range(n))
+    idx_flop = 2.0 * HI * DI * visible
+    idx_tflops = idx_flop / (split["index"] / 1e3) / 1e12
+    out = {"workload": PREFILL.workload, "value": n / per_chunk, "unit": "tok/s",
+           "ms_per_chunk": 1e3 * per_chunk, "ms_per_chunk_by_call": split,
+           "indexer": {"flop_per_chunk": idx_flop, "tflops": idx_tflops,
+                       "fp4_peak_tflops": peak_tflops,
+                       "frac": idx_tflops / peak_tflops if peak_tflops else None,
+                       "peak_source": "fp4_peak of this line (measured)"}}
+    del run
+    torch.cuda.empty_cache()
+    return out
+
+
+def config5_summary(torch, warmup=3, steps=16):
+    """Configuration 5 (32 sequences, context lengths log-uniform in [4,096,
+    1,048,576], ragged caches, 1 index source + 5 readers): 16 consecutive decode
+    steps as CUDA graphs, query-tok/s."""
+    from csa2_compressed_sparse_02_gb300 import workloads
+    from csa2_compressed_sparse_02_gb300.inputs import CONFIGS
+    cfg = CONFIGS[5]
+    run = workloads.DecodeRun(cfg, n_steps=warmup + 2 + steps)
+    for _ in range(warmup):
+        run.step()
+    torch.cuda.synchronize()
+    graphs = run.capture()
+    if graphs:
+        for _ in range(2):
+            run.step_graph()
+    else:
+        for _ in range(2):
+            run.step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        run.step_graph() if graphs else run.step()
+    b.record()
+    torch.cuda.synchronize()
+    assert int(run.dev_status.item()) == 0, "device status %d" % int(run.dev_status.item())
+    el = a.elapsed_time(b) / 1e3
+    lens = cfg.first_lengths()
+    out = {"workload": cfg.workload, "value": cfg.B * steps / el, "unit": UNIT,
+           "ms_per_step": 1e3 * el / steps, "steps": steps,
+           "launch_mode": "cuda-graph" if graphs else "eager",
+           "context_tokens": {"min": min(lens), "max": max(lens), "mean": sum(lens) / len(lens)}}
+    del run
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(run, K, stream, barrier, over_ranks=lambda x: x, world=1):

@@ -57,6 +57,7 @@ SIGNATURES = {
     "csa2_sparse_attn_layers_part": (I32, [PP, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P, P]),
     "csa2_sparse_attn_layers_split": (I32, [PP, I32, I32, P, P, P, P, P, P, P, P, P, SZ, P, P]),
     "csa2_sparse_attn_layers_split_workspace_size": (SZ, [PP, I32, I32]),
+    "csa2_fp4_mma_peak": (I32, [I32, I32, P, P]),
 }
 
 

@@ -206,6 +206,13 @@ def sparse_attn_noalloc(params, q, sink, win_ptrs, n_tokens, comp_ptrs, comp_sca
         _stream(stream)), "sparse_attn_noalloc")
 
 
+def fp4_mma_peak(ctas, iters, dev_status=None, stream=None):
+    """Enqueue the FP4 tensor-core rate measurement (csa2_fp4_mma_peak): ctas x iters
+    MMA pairs of 2 x 128 x 128 x 128 flop each. The caller times it."""
+    check(lib().csa2_fp4_mma_peak(int(ctas), int(iters), _ptr(dev_status), _stream(stream)),
+          "fp4_mma_peak")
+
+
 # --------------------------------------------------------------------------- buffers
 @dataclass
 class LayerCache:

@@ -31,7 +31,7 @@ int ensure_loaded() {
     std::lock_guard<std::mutex> g(mu);
     if ((done >> dev) & 1u) return CSA2_OK;
     cudaError_t (*lists[])() = {preload_compress, preload_index, preload_index_shared,
-                                preload_select, preload_attn, preload_attn_tc};
+                                preload_select, preload_attn, preload_attn_tc, preload_peak};
     for (auto f : lists) {
         const cudaError_t e = f();
         if (e != cudaSuccess) {

@@ -54,6 +54,7 @@ cudaError_t preload_index_shared();
 cudaError_t preload_select();
 cudaError_t preload_attn();
 cudaError_t preload_attn_tc();
+cudaError_t preload_peak();
 
 // Single-layer sparse attention (csa2_sparse_attn, quantised formats) on the
 // tcgen05 kernel of sparse_attn_tc.cu with the even split schedule; the

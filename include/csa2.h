@@ -498,6 +498,20 @@ int csa2_sparse_attn_noalloc(const csa2_params* p, int B,
                              const int32_t* idx, void* out,
                              int32_t* dev_status, void* stream);
 
+/*
+ * csa2_fp4_mma_peak — measurement aid, no counterpart in the pages: the rate of
+ * the block-scaled FP4 tensor-core MMA that csa2_index_scores_shared issues, so
+ * its throughput can be quoted as a fraction of what the GPU reaches with the
+ * same instruction. Launches `ctas` CTAs; each issues `iters` pairs of
+ * tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X (M = N = 128, K = 64 each)
+ * back to back from shared-memory operands into one TMEM accumulator:
+ * 2 x 128 x 128 x 128 flop per pair and CTA. The caller times the launch (CUDA
+ * events on `stream`). Nothing is read or written outside the kernel except
+ * dev_status (CSA2_DEV_TIMEOUT if the completion wait gave up; may be NULL).
+ * Requires 1 <= ctas <= 65535, 1 <= iters <= 2^22 (else CSA2_ERR_INVALID_ARG).
+ */
+int csa2_fp4_mma_peak(int ctas, int iters, int32_t* dev_status, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -88,5 +88,9 @@ def test_host_side_rejections_without_launching(L):
         bp = api.default_params(**over)
         assert L.csa2_compress_append(ctypes.byref(bp), 1, 1, al, None, None, None, None, None,
                                       None, al, al, None, None) == code, over
+    # the FP4 MMA rate measurement rejects empty or oversized launches on the host
+    assert L.csa2_fp4_mma_peak(0, 10, None, None) == 1
+    assert L.csa2_fp4_mma_peak(4, 0, None, None) == 1
+    assert L.csa2_fp4_mma_peak(4, (1 << 22) + 1, None, None) == 1
     # nothing to do is not an error
     assert L.csa2_compress_append(pp, 0, 1, *([None] * 11)) == 0

@@ -715,6 +715,17 @@ def test_sparse_attn_layers_rescale_and_many_units(mode):
             assert ok, (l, b, T, e)
 
 
+def test_fp4_mma_peak_completes_with_a_clean_status():
+    """The FP4 tensor-core rate measurement (the prefill Indexer's MMA issued back to
+    back) completes, twice, more CTAs than SMs included."""
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    api.fp4_mma_peak(3, 50, st)
+    api.fp4_mma_peak(2 * sms + 1, 200, st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+
+
 def test_launch_trace_names_the_last_launch():
     """csa2_trace_attach: after a selection launch the host-mapped record names it
     (started and first-CTA-finished), without a synchronising read of device
