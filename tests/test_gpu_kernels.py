@@ -570,10 +570,14 @@ def _run_layers(mode, p, L, B, *args, repeat=1):
     return ws
 
 
+@pytest.mark.parametrize("sinks", ["normal", "extreme"])
 @pytest.mark.parametrize("mode", list(LAYER_MODES))
-def test_sparse_attn_layers_matches_oracle_per_layer(mode):
+def test_sparse_attn_layers_matches_oracle_per_layer(mode, sinks):
     """L layers share one compressed cache and one selection; each has its own
-    window ring, query and sink (the KV-sharing readers of a source layer)."""
+    window ring, query and sink (the KV-sharing readers of a source layer).
+    sinks = "extreme": per head +30 (the sink outweighs every position, output near
+    0), -30, -inf (a plain softmax), 0 and 5, across the running maximum, the sink
+    term of the denominator and, in the split modes, the merge of cut units."""
     rng = np.random.default_rng(31)
     L = 3
     Ts = [1, 70, 128, 129, 900, 4096, 2001]
@@ -608,6 +612,9 @@ def test_sparse_attn_layers_matches_oracle_per_layer(mode):
     qb = synth.bf16_bits_rne(q)
     q_dev = torch.from_numpy(qb.view(np.int16)).to(DEV).view(torch.bfloat16)
     sink = rng.standard_normal((L, 64)).astype(np.float32)
+    if sinks == "extreme":
+        prof = np.array([30.0, -30.0, -np.inf, 0.0, 5.0], np.float32)
+        sink = prof[(np.arange(L)[:, None] + np.arange(64)[None, :]) % len(prof)]
     win_all = torch.cat([src.win_ptrs] + [w.win_ptrs for w in wins])
     out = torch.empty(L, B, 64, 512, dtype=torch.bfloat16, device=DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
