@@ -11,10 +11,11 @@
 // D[128 x 128] = K . Q^T takes two tcgen05.mma.kind::mxf4nvf4 (K = 64 each). A
 // persistent CTA walks a contiguous range of (query block of 16, key super-tile
 // of 4 tiles) items: each 36 KB super-tile is loaded once per 16 queries. The
-// epilogue (8 warps: one TMEM lane quarter x two queries of the group each) reads
-// one key per lane, applies ReLU and the head weights,
-// mask positions past each query's own length, and write the score and the
-// block maximum (8 adjacent lanes). Every wait is bounded.
+// epilogue is 16 warps, one per (TMEM lane quarter, query of the group): each reads
+// its query's 32 head columns for 32 keys (one per lane), applies ReLU and the head
+// weights in packed FP32 pairs, masks positions past the query's own causal
+// length, and writes the score and the block maximum (8 adjacent lanes). Every
+// wait is bounded.
 #include <mutex>
 
 #include "common.cuh"
@@ -35,20 +36,15 @@ constexpr int kTilesPerStage = 4;
 constexpr int kStageBytes = kTilesPerStage * kKeyTileBytes;  // 36,864
 constexpr int kPosPerStage = kTilesPerStage * kKeyTile;      // 512
 constexpr int kStages = 4;
-constexpr int kQPerWarp = 2;                        // queries of a group per epilogue warp
-constexpr int kEpiWarps = 4 * kQPerGroup / kQPerWarp;  // 8: lane quarter x query pair
+constexpr int kEpiWarps = 4 * kQPerGroup;           // 16: TMEM lane quarter x query of the group
 constexpr int kAcc = 3;                             // accumulators in flight
 constexpr int kLoadWarp = kEpiWarps, kMmaWarp = kLoadWarp + 1;
-constexpr int kThreadsSh = 32 * (kMmaWarp + 1);     // 320
+constexpr int kThreadsSh = 32 * (kMmaWarp + 1);     // 576
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColD = 0;                       // kAcc x 128 columns
 constexpr uint32_t kColSFA = kN * kAcc;             // 2 super-tile slots x kTilesPerStage x 8
 constexpr uint32_t kColSFB = kColSFA + 2 * kTilesPerStage * 8;  // 2 query slots x kGroups x 8
 static_assert(kColSFB + 2 * kGroups * 8 <= kTmemCols, "TMEM columns");
-// heads [0, kHRelu) take ReLU as a max on the ALU pipe; the rest as
-// (w/2) d + (w/2) |d| on the FMA pipe, which balances the two pipes
-constexpr int kHRelu = 20;
-static_assert(kHRelu % 4 == 0 && kHRelu <= kHi, "head split");
 // kind::mxf4nvf4, A and B E2M1, K-major, dense, N = 128 (N>>3 in bits 17..22),
 // UE4M3 scales, M = 128 (M>>4 in bits 24..28).
 constexpr uint32_t kIdesc = (1u << 7) | (1u << 10) | ((uint32_t)(kN >> 3) << 17) | ((128u >> 4) << 24);
@@ -81,28 +77,41 @@ __device__ __forceinline__ int tiles_in(int64_t g, int32_t ncmax) {
     return left <= 0 ? 0 : (left < kTilesPerStage ? (int)left : kTilesPerStage);
 }
 
-// sum over heads of w ReLU(d): a max and an FMA for the first kHRelu heads, (w/2) d
-// + (w/2) |d| (two FMAs, the weights stored halved) for the rest; four independent
-// chains. Every partial sum is exact when the products are (power-of-two scales),
-// so the order of the chains does not change the result there.
-__device__ __forceinline__ float head_sum(const float (&w)[kHi], const uint32_t* r) {
-    float c0 = 0.0f, c1 = 0.0f, c2 = 0.0f, c3 = 0.0f;
+// Packed FP32 pairs: fma.rn.f32x2 rounds each half exactly as fma.rn.f32 does, and
+// one instruction covers two heads.
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    uint64_t v;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "f"(lo), "f"(hi));
+    return v;
+}
+__device__ __forceinline__ void unpack2(uint64_t v, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// sum over heads of w ReLU(d) (w2[i] = the weights of heads 2i, 2i + 1): ReLU as a
+// max, the products and sums in packed pairs, eight independent partial sums. Every
+// partial sum is exact when the products are (power-of-two scales), so the order of
+// the chains does not change the result there.
+__device__ __forceinline__ float head_sum(const uint64_t (&w2)[kHi / 2], const uint32_t (&r)[kHi]) {
+    uint64_t c2[4] = {0ull, 0ull, 0ull, 0ull};  // +0.0f in both halves
 #pragma unroll
-    for (int h = 0; h < kHRelu; h += 4) {
-        c0 = __fmaf_rn(w[h], fmaxf(__uint_as_float(r[h]), 0.0f), c0);
-        c1 = __fmaf_rn(w[h + 1], fmaxf(__uint_as_float(r[h + 1]), 0.0f), c1);
-        c2 = __fmaf_rn(w[h + 2], fmaxf(__uint_as_float(r[h + 2]), 0.0f), c2);
-        c3 = __fmaf_rn(w[h + 3], fmaxf(__uint_as_float(r[h + 3]), 0.0f), c3);
-    }
+    for (int h = 0; h < kHi; h += 8) {
 #pragma unroll
-    for (int h = kHRelu; h < kHi; h += 2) {
-        const float d0 = __uint_as_float(r[h]), d1 = __uint_as_float(r[h + 1]);
-        c0 = __fmaf_rn(w[h], d0, c0);
-        c1 = __fmaf_rn(w[h], fabsf(d0), c1);
-        c2 = __fmaf_rn(w[h + 1], d1, c2);
-        c3 = __fmaf_rn(w[h + 1], fabsf(d1), c3);
+        for (int u = 0; u < 4; ++u) {
+            const float d0 = fmaxf(__uint_as_float(r[h + 2 * u]), 0.0f);
+            const float d1 = fmaxf(__uint_as_float(r[h + 2 * u + 1]), 0.0f);
+            c2[u] = fma2(w2[h / 2 + u], pack2(d0, d1), c2[u]);
+        }
     }
-    return (c0 + c1) + (c2 + c3);
+    float v[8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) unpack2(c2[u], v[2 * u], v[2 * u + 1]);
+    return ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
 }
 
 __global__ void __launch_bounds__(kThreadsSh, 1)
@@ -187,7 +196,7 @@ k_index_shared_tc(int Q, Work wk, int64_t max_ncomp, int ratio, const uint8_t* _
                     // scale-factor atoms: row n & 31 = h, bytes 4 qi .. 4 qi + 3
                     *reinterpret_cast<uint32_t*>(&sh.sfb[qs][gi][lane * 16 + 4 * (qb % kQPerGroup)]) = sc.x;
                     *reinterpret_cast<uint32_t*>(&sh.sfb[qs][gi][512 + lane * 16 + 4 * (qb % kQPerGroup)]) = sc.y;
-                    sh.w[qs][qb][lane] = lane < kHRelu ? wv : 0.5f * wv;
+                    sh.w[qs][qb][lane] = wv;
                     if (lane == 0) sh.nc[qs][qb] = nc;
                     mx = max(mx, nc);
                 }
@@ -314,11 +323,11 @@ k_index_shared_tc(int Q, Work wk, int64_t max_ncomp, int ratio, const uint8_t* _
             if (mbar_try_wait(&sh.done, 0)) break;
     } else {
         // ---------------- epilogue: warp (qp, wq) reads TMEM lanes 32 wq.. (positions
-        // 32 wq.. of the tile) for queries 2 qp and 2 qp + 1 of the item's group
+        // 32 wq.. of each tile) and the 32 columns of query qp of the item's group; it
+        // releases the accumulator as soon as its columns are in registers.
         const int wq = warp & 3, qp = warp >> 2;
         const uint32_t accf0 = smem_u32(&sh.accf[0]), acce0 = smem_u32(&sh.acce[0]);
-        const uint32_t tmem_lane = tmem + ((uint32_t)(32 * wq) << 16) + kColD + kHi * kQPerWarp * qp;
-        const int ncomp32 = (int)max_ncomp, ldbm32 = (int)ld_bm;  // both below 2^31
+        const uint32_t tmem_lane = tmem + ((uint32_t)(32 * wq) << 16) + kColD + kHi * qp;
         const bool blk_lead = (lane & (kBlk - 1)) == 0;
         int seg = -1, prev_k = -1;
         int a = 0;         // accumulator slot of the next item
@@ -339,46 +348,43 @@ k_index_shared_tc(int Q, Work wk, int64_t max_ncomp, int ratio, const uint8_t* _
             }
             const int qs = seg & 1;
             const int nt = tiles_in(g, sh.ncmax[qs]);
+            // group-major, as the MMA issuer runs: the query's weights stay in registers
+            // across the super-tile's tiles
             for (int gi = 0; gi < kGroups && ok; ++gi) {
-                const int qb = gi * kQPerGroup + kQPerWarp * qp;  // queries qb and qb + 1
-                const int32_t nc0 = sh.nc[qs][qb], nc1 = sh.nc[qs][qb + 1];
+                const int qb = gi * kQPerGroup + qp;  // this warp's query of group gi
+                const int32_t nc0 = sh.nc[qs][qb];
                 const int64_t qq = (int64_t)(k * kQPerBlock + qb);
                 float* srow0 = scores + qq * max_ncomp;
                 float* brow0 = block_max + qq * ld_bm;
-                float w0[kHi], w1[kHi];
+                uint64_t w0[kHi / 2];
 #pragma unroll
                 for (int h4 = 0; h4 < kHi / 4; ++h4) {
-                    const float4 v0 = reinterpret_cast<const float4*>(sh.w[qs][qb])[h4];
-                    const float4 v1 = reinterpret_cast<const float4*>(sh.w[qs][qb + 1])[h4];
-                    w0[4 * h4] = v0.x, w0[4 * h4 + 1] = v0.y, w0[4 * h4 + 2] = v0.z, w0[4 * h4 + 3] = v0.w;
-                    w1[4 * h4] = v1.x, w1[4 * h4 + 1] = v1.y, w1[4 * h4 + 2] = v1.z, w1[4 * h4 + 3] = v1.w;
+                    const ulonglong2 v0 = reinterpret_cast<const ulonglong2*>(sh.w[qs][qb])[h4];
+                    w0[2 * h4] = v0.x, w0[2 * h4 + 1] = v0.y;
                 }
                 int tl = g * kPosPerStage + 32 * wq + lane;  // this lane's position in tile j
-                for (int j = 0; j < nt; ++j, tl += kKeyTile) {
+                float* sp = srow0 + tl;  // its score and block-maximum slots, stepped per tile
+                float* bp = brow0 + (tl >> 3);
+                for (int j = 0; j < nt; ++j, tl += kKeyTile, sp += kKeyTile, bp += kKeyTile / kBlk) {
                     if (!mbar_wait_sleep_at(accf0 + 8u * a, ph, abort)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    uint32_t r[2 * kHi];
-                    tmem_ld_32x32b_x64_nowait(tmem_lane + kN * a, r);
-                    tmem_wait_ld();
+                    uint32_t r[kHi];
+                    tmem_ld_32x32b_x32_nowait(tmem_lane + kN * a, r);
+                    tmem_wait_ld_regs32(r);
                     tc_fence_before();
                     mbar_arrive_at(acce0 + 8u * a);  // this thread's part of the accumulator is read
                     a = (a + 1 == kAcc) ? 0 : a + 1;
                     ph ^= (a == 0) ? 1u : 0u;
-                    const float sc0 = head_sum(w0, r), sc1 = head_sum(w1, r + kHi);
-                    const bool v0 = tl < nc0, v1 = tl < nc1;
-                    float m0 = v0 ? sc0 : -INFINITY, m1 = v1 ? sc1 : -INFINITY;
+                    const float sc = head_sum(w0, r);
+                    const bool v = tl < nc0;
+                    float m = v ? sc : -INFINITY;
 #pragma unroll
-                    for (int o = 1; o < kBlk; o <<= 1) {
-                        m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-                        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
-                    }
-                    st_global_if(srow0 + tl, sc0, v0);
-                    st_global_if(srow0 + (ncomp32 + tl), sc1, v1);
-                    st_global_if(brow0 + (tl >> 3), m0, v0 && blk_lead);
-                    st_global_if(brow0 + (ldbm32 + (tl >> 3)), m1, v1 && blk_lead);
+                    for (int o = 1; o < kBlk; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                    st_global_if(sp, sc, v);
+                    st_global_if(bp, m, v && blk_lead);
                 }
             }
         }
