@@ -21,14 +21,19 @@
 // position, so the output comes out ascending by construction.
 //
 // Level 1 keeps 512 of up to 131,072 blocks, so it first narrows the field:
-// a threshold estimated from a strided sample of 2,048 block maxima, one pass
-// that keeps the blocks at or above it (in index order, in shared memory), and
-// the exact select among those. The answer is unchanged because the top 512
-// all lie at or above any threshold that at least 512 blocks reach; when the
-// count falls outside [512, kMaxFiltered] the threshold moves, and after a
-// few tries the exact select runs over all blocks in global memory. Level 2
-// keeps the positions at or above the 512th block's maximum (the kept blocks'
-// own maxima already reach it, so the 512 best do) before its exact select.
+// a threshold estimated from a strided sample of 2,048 block maxima and one pass
+// that keeps the blocks at or above it (in index order, in shared memory). The
+// top 512 blocks all lie at or above any threshold that at least 512 blocks
+// reach, and so do the 512 best positions (each scores at least the 512th best
+// block maximum). So the common path goes flat from there: the positions of at
+// most 2,048 candidate blocks are gathered into shared memory, those at or above
+// the threshold kept (usually a few hundred more than 512), and one exact select
+// of 512 runs among them. When the count falls outside [512, kMaxFiltered] the
+// threshold moves, and after a few tries the exact select runs over all blocks
+// in global memory; with more than 2,048 candidate blocks, or more than 4,096
+// tied positions at or above the threshold, the 512 best candidate blocks are
+// selected first and level 2 keeps the positions at or above the 512th block's
+// maximum before its exact select.
 #include "common.cuh"
 #include "sm100.cuh"
 
@@ -46,6 +51,8 @@ constexpr int kMaxCand = kMaxFiltered + kSample;  // level 1: filtered keys, sam
 constexpr int kStagePerWarp = 256;   // kept pairs a warp stages during the vector filter's pass
 constexpr int kClMax = 4;            // CTAs of one sequence in the cluster launch
 constexpr int kAttempts = 4;         // thresholds tried before the exact select over every block
+constexpr int kStage = kWarps * kStagePerWarp;  // pairs the level-1 filter can stage
+constexpr int kFlatCap = 2 * kStage;  // positions the flat pass gathers (the whole stage area)
 
 struct SelShared {
     uint32_t hist[256];
@@ -55,8 +62,9 @@ struct SelShared {
     uint32_t cand[kMaxCand];        // level 1: filtered keys (sample at the end); level 2 keys
     int32_t cand_idx[kMaxFiltered];  // index of each filtered key
     uint32_t cand2[kMaxFiltered2];   // level 2 filtered keys
-    uint32_t stage_key[kWarps * kStagePerWarp];  // level 1 filter: kept pairs per warp, in order
-    int32_t stage_idx[kWarps * kStagePerWarp];
+    // level 1 filter: kept (key, index) pairs per warp, in order (keys in
+    // [0, kStage), indices in [kStage, 2 kStage)); the flat pass: position keys
+    uint32_t stage[2 * kStage];
     // cluster launch: each CTA's level-1 candidate count, per attempt, written into
     // every CTA of the cluster; cnt_bar completes a phase per attempt once all CTAs
     // wrote theirs, gat_bar (CTA 0) once the others copied their candidates in
@@ -265,8 +273,8 @@ __device__ int filter_ge_vec(int n, uint32_t thr, const float* __restrict__ bm, 
     const int chunks = (n + 127) / 128;
     const int R = (chunks + kWarps - 1) / kWarps;
     const int c0 = min(chunks, warp * R), c1 = min(chunks, c0 + R);
-    uint32_t* skey = sh.stage_key + warp * kStagePerWarp;
-    int32_t* sidx = sh.stage_idx + warp * kStagePerWarp;
+    uint32_t* skey = sh.stage + warp * kStagePerWarp;
+    int32_t* sidx = reinterpret_cast<int32_t*>(sh.stage + kStage) + warp * kStagePerWarp;
     // the value whose key is thr: key >= thr <=> value >= thr_f (keys are monotone)
     const uint32_t tb = (thr & 0x80000000u) ? (thr & 0x7fffffffu) : ~thr;
     const float thr_f = __uint_as_float(tb);
@@ -469,6 +477,49 @@ k_select_topk(int64_t max_ncomp, int ratio, const float* __restrict__ scores,
                     return;
                 }
             }
+            // (e) flat: the candidate blocks hold every position of the kKp best (those
+            //     score at least the kKp-th best block maximum, which is at least thr), so
+            //     the kKp best of their positions at or above thr are the answer. Slot i =
+            //     position i % 8 of candidate block i / 8, ascending by position; positions
+            //     past n_c take the lowest key, and thr is above it.
+            __syncthreads();
+            auto vpos = [&](int i) { return sh.cand_idx[i >> 3] * kBlk + (i & (kBlk - 1)); };
+            if (thr > 0u && total * kBlk <= kFlatCap) {
+                const int nv = total * kBlk;
+                if ((reinterpret_cast<uintptr_t>(sc) & 15u) == 0) {
+                    // a block is 8 consecutive scores (32 bytes): two 16-byte loads
+                    for (int q = tid; q < 2 * total; q += kThreads) {
+                        const int i = 4 * q, pos = vpos(i);
+                        if (pos + 3 < n_c) {
+                            const float4 v = __ldg(reinterpret_cast<const float4*>(sc + pos));
+                            *reinterpret_cast<uint4*>(&sh.stage[i]) =
+                                make_uint4(score_key(v.x), score_key(v.y), score_key(v.z), score_key(v.w));
+                        } else {
+                            for (int c = 0; c < 4; ++c) sh.stage[i + c] = pos + c < n_c ? score_key(sc[pos + c]) : 0u;
+                        }
+                    }
+                } else {
+                    for (int i = tid; i < nv; i += kThreads) {
+                        const int pos = vpos(i);
+                        sh.stage[i] = pos < n_c ? score_key(sc[pos]) : 0u;
+                    }
+                }
+                __syncthreads();
+                // kept keys to cand2, their slots to the block keys' array (not needed on
+                // this path; untouched when the filter overflows)
+                int32_t* slot = reinterpret_cast<int32_t*>(sh.cand);
+                const int n2 = filter_ge(
+                    nv, thr, [&](int i) { return sh.stage[i]; }, sh.cand2, slot, kMaxFiltered2, sh);
+                if (n2 <= kMaxFiltered2) {  // at least total >= kKp: each candidate block's maximum
+                    select_top(
+                        n2, kKp, [&](int i) { return sh.cand2[i]; },
+                        [&](uint32_t rank_, int i) { out[rank_] = vpos(slot[i]); }, sh);
+                    if (tid == 0 && n_sel_out) n_sel_out[b] = kKp;
+                    trace_end(kTraceSelect);
+                    return;
+                }
+            }
+            // too many positions at or above thr (ties): the kKp best blocks first
             thr2 = select_top(
                 total, K1, [&](int i) { return sh.cand[i]; },
                 [&](uint32_t rank_, int i) { sh.kept[rank_] = sh.cand_idx[i]; }, sh);

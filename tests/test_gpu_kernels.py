@@ -398,14 +398,20 @@ def test_index_scores_clip_and_status_when_length_exceeds_max():
 
 # --------------------------------------------------------------------------- selection
 @pytest.mark.parametrize("cluster", [True, False], ids=["cluster4", "one_cta"])
-@pytest.mark.parametrize("levels,pad", [(3, 0), (50, 0), (0, 0), (0, 4)])
+@pytest.mark.parametrize("levels,pad", [(1, 0), (3, 0), (50, 0), (0, 0), (0, 4)])
 def test_select_topk_exact_with_ties(levels, pad, cluster):
     """pad = 0: every row 16-byte aligned (vector loads where a sequence has at most
     65,536 blocks); pad = 4: odd rows misaligned (scalar loads). cluster: each
     sequence on a cluster of 4 CTAs (the small-batch launch), else on one CTA
-    (max_ctas below 4 B forces it)."""
+    (max_ctas below 4 B forces it). Paths: up to 2,048 candidate blocks go flat
+    (positions at or above the level-1 threshold, one exact select); with 1 level
+    8,000 positions put all 1,000 blocks and 8,000 positions at the threshold, and
+    with 3 levels 16,384 positions about 1,970 blocks and 5,500 positions: more than
+    the flat pass's 4,096, so the 512 best blocks are selected first, as they are
+    for 20,000..40,000 positions (2,400..4,800 candidate blocks). 70,001 and more
+    with few levels put over 8,192 blocks there: the exact select over every block."""
     rng = np.random.default_rng(levels + 5)
-    n_cs = [0, 1, 5, 511, 512, 513, 4095, 16384, 16385, 20000, 70001, 524288, 600000]
+    n_cs = [0, 1, 5, 511, 512, 513, 4095, 8000, 16384, 16385, 20000, 40000, 70001, 524288, 600000]
     B, max_nc = len(n_cs), max(n_cs) + pad
     scores = np.zeros((B, max_nc), np.float32)
     for b, n in enumerate(n_cs):
