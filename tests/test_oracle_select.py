@@ -138,3 +138,54 @@ def test_two_levels_equal_the_flat_top_at_the_pages_sizes():
             ref = flat_top(s, 512)
             assert m == 512 and np.array_equal(idx, ref), (n, levels)
             assert np.array_equal(top_within_top_blocks(s, 8, 512), ref), (n, levels)
+
+
+def top_above_threshold(scores, blk, Kp, t):
+    """The Kp best positions by (score desc, position asc), ascending, among the
+    positions at or above t of the blocks whose maximum is at or above t."""
+    n = len(scores)
+    nb = -(-n // blk)
+    bm = np.array([scores[b * blk:(b + 1) * blk].max() for b in range(nb)], np.float64)
+    blocks = np.nonzero(bm >= t)[0]
+    cand = np.concatenate([np.arange(b * blk, min(n, b * blk + blk)) for b in blocks])
+    cand = cand[scores[cand] >= t]
+    order = np.lexsort((cand, -scores[cand].astype(np.float64)))
+    return np.sort(cand[order[:Kp]])
+
+
+def test_any_threshold_that_kp_blocks_reach_keeps_the_answer():
+    # The selection kernel's candidates: for any t that at least Kp block maxima
+    # reach, the Kp best positions all score at least t (each of the Kp best blocks
+    # holds a position at or above the Kp-th best block maximum, which is at least
+    # t), so they lie among the positions at or above t of the blocks whose maximum
+    # reaches t, and the Kp best of those are the rule's answer. Thresholds from the
+    # largest one (the Kp-th best block maximum) down to below every score, with
+    # ties, partial newest blocks and Kb - 1 >= Kp.
+    rng = np.random.default_rng(9)
+    for trial in range(400):
+        blk = int(rng.integers(1, 9))
+        Kp = int(rng.integers(1, 40))
+        Kb = Kp + 1 + int(rng.integers(0, 8))
+        n = int(rng.integers(1, 600))
+        levels = int(rng.integers(0, 8))
+        s = (rng.integers(0, levels, n).astype(np.float32) if levels
+             else rng.standard_normal(n).astype(np.float32))
+        idx, m = orc.select(s, blk, Kb, Kp)
+        nb = -(-n // blk)
+        bm = np.sort(np.array([s[b * blk:(b + 1) * blk].max() for b in range(nb)], np.float64))[::-1]
+        if nb < Kp:
+            continue  # every block is a candidate: nothing to choose
+        t_max = bm[Kp - 1]
+        for t in (t_max, t_max - 0.5, bm[-1], bm[-1] - 1.0, float(rng.uniform(bm[-1] - 1.0, t_max))):
+            assert (bm >= t).sum() >= Kp
+            got = top_above_threshold(s, blk, Kp, t)
+            assert len(got) == m and np.array_equal(got, idx[:m]), (trial, n, blk, Kp, t)
+
+
+def test_a_threshold_above_the_kp_th_block_maximum_can_lose_positions():
+    # The bound is tight: above the Kp-th best block maximum fewer than Kp blocks
+    # remain and the answer is not kept (the kernel never uses such a threshold).
+    s = np.array([5, 0, 0, 0, 4, 0, 0, 0, 3, 0, 0, 0], np.float32)
+    idx, m = orc.select(s, 4, 3, 2)
+    assert list(idx[:m]) == [0, 4]
+    assert list(top_above_threshold(s, 4, 2, 4.5)) == [0]
