@@ -9,6 +9,7 @@
 // at decode (one token per sequence); at prefill the pairs are spread over
 // CTAs of 16 pairs each.
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace csa2 {
 namespace {
@@ -92,6 +93,9 @@ k_compress_append(int n_new, const float* __restrict__ kv_new, const float* __re
                   int32_t* n_tokens, int advance_here, RopeArgs rope, int32_t* dev_status) {
     const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
     trace_start(kTraceCompress);
+    // a kernel launched programmatically behind this one (the Indexer) may be placed
+    // now; it waits for this grid before reading anything it writes
+    sm100::grid_dep_launch_dependents();
     const int ch = 4 * tid;
     const int64_t T = n_tokens[b];
     if (T < 0) {

@@ -219,10 +219,10 @@ __device__ __forceinline__ int64_t supers_of(int64_t n_c) {
 // flat super-tiles with their own cursor, and a role that saw other lengths
 // would wait on barriers the others never complete (until the bounded wait
 // gives up). That holds because n_tokens does not change while the kernel runs:
-// it is launched in plain stream order after the Compressor's k_advance, which
-// writes n_tokens. A launch that could overlap that writer (a programmatic
-// launch behind it) must first wait for it (grid_dep_wait) before warp 0 reads
-// the lengths.
+// the kernel is launched programmatically behind the Compressor (which writes
+// n_tokens), so its CTAs may be placed and set up their barriers and TMEM while
+// that kernel still runs, but nothing global is read before grid_dep_wait(),
+// i.e. before the kernels ahead of it on the stream have completed.
 struct SeqCursor {
     int b = -1;
     int64_t start = 0, end = 0;  // flat super-tiles [start, end) belong to sequence b
@@ -316,6 +316,9 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
         sh.abort = 0;
         fence_mbar_init();
     }
+    // launched programmatically: nothing global is read before the kernels ahead of
+    // it on the stream (the Compressor writes the lengths) have completed
+    grid_dep_wait();
     if (warp == 0) {  // super-tiles of all sequences (CTA 0 flags bad lengths)
         int64_t local = 0;
         for (int b = lane; b < B; b += 32)
@@ -601,8 +604,20 @@ extern "C" int csa2_index_scores(const csa2_params* p, int B, int64_t max_ncomp,
     int64_t ctas = num_sms();
     if (p->max_ctas > 0 && p->max_ctas < ctas) ctas = p->max_ctas;
     const int grid = (int)std::min<int64_t>(tiles_max, ctas);
-    k_index_scores_tc<<<grid, kTcThreads, kTcSmem, static_cast<cudaStream_t>(stream)>>>(
-        B, max_ncomp, p->compress_ratio, q_vals, q_scales, w, key_cache, n_tokens, scores,
-        block_max, dev_status);
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)grid);
+        cfg.blockDim = dim3(kTcThreads);
+        cfg.dynamicSmemBytes = kTcSmem;
+        cfg.stream = static_cast<cudaStream_t>(stream);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, k_index_scores_tc, B, max_ncomp, p->compress_ratio, q_vals, q_scales, w,
+                               key_cache, n_tokens, scores, block_max, dev_status) != cudaSuccess)
+            return check_launch("index_scores");
+    }
     return check_launch("index_scores");
 }
