@@ -93,9 +93,12 @@ k_compress_append(int n_new, const float* __restrict__ kv_new, const float* __re
                   int32_t* n_tokens, int advance_here, RopeArgs rope, int32_t* dev_status) {
     const int b = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
     trace_start(kTraceCompress);
-    // a kernel launched programmatically behind this one (the Indexer) may be placed
-    // now; it waits for this grid before reading anything it writes
+    // A kernel launched programmatically behind this one (the next append, the
+    // Indexer) may be placed now; it waits for this grid before touching its data.
+    // This one is launched the same way: nothing is read or written before the
+    // kernels ahead of it on the stream have completed.
     sm100::grid_dep_launch_dependents();
+    sm100::grid_dep_wait();
     const int ch = 4 * tid;
     const int64_t T = n_tokens[b];
     if (T < 0) {
@@ -311,11 +314,24 @@ extern "C" int csa2_compress_append(const csa2_params* p, int B, int n_new,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool we = p->win_format == CSA2_E4M3;
     if (const int rc = ensure_loaded()) return rc;
-#define CSA2_LAUNCH(R, NV, WE)                                                              \
-    k_compress_append<R, NV, WE><<<grid, kThreads, 0, s>>>(n_new, kv_new, gate_new, pend_kv, \
-                                                            pend_gate, comp, comp_scales,   \
-                                                            comp_cap, win, n_tokens,        \
-                                                            advance_here, rope, dev_status)
+    // programmatic launch: the CTAs may be placed while the kernel ahead still runs
+    // (they wait for it first), which hides the launch gap between back-to-back appends
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+#define CSA2_LAUNCH(R, NV, WE)                                                                       \
+    do {                                                                                             \
+        if (cudaLaunchKernelEx(&cfg, k_compress_append<R, NV, WE>, n_new, kv_new, gate_new, pend_kv, \
+                               pend_gate, comp, comp_scales, comp_cap, win, n_tokens, advance_here,  \
+                               rope, dev_status) != cudaSuccess)                                     \
+            return check_launch("compress_append");                                                  \
+    } while (0)
     if (ratio == 2) {
         if (nvfp4 && we) CSA2_LAUNCH(2, true, true);
         else if (nvfp4) CSA2_LAUNCH(2, true, false);
