@@ -353,6 +353,18 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
             cur.advance(f, n_tokens, ratio, max_ncomp);
             b = cur.b;
             const int64_t g = f - cur.start;
+            // the key copy first: it does not need the query, whose staging costs a
+            // memory round trip at every sequence change
+            const int s = (int)(i % kStages);
+            if (!mbar_wait(&sh.empty[s], (uint32_t)((i / kStages) & 1) ^ 1, abort)) break;
+            if (lane == 0) {
+                const uint32_t bytes = (uint32_t)tiles_in(g, cur.n_c) * kKeyTileBytes;
+                mbar_arrive_expect_tx(&sh.full[s], bytes);
+                bulk_g2s_hint(sh.stage[s], key_cache[b] + g * kStageBytes, bytes, &sh.full[s],
+                              key_policy);
+            }
+            __syncwarp();
+            issued = i + 1;
             if (b != prev_b) {
                 ++seg;
                 const int qs = seg & 1;
@@ -373,16 +385,6 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
                 if (lane == 0) mbar_arrive(&sh.qfull[qs]);
                 prev_b = b;
             }
-            const int s = (int)(i % kStages);
-            if (!mbar_wait(&sh.empty[s], (uint32_t)((i / kStages) & 1) ^ 1, abort)) break;
-            if (lane == 0) {
-                const uint32_t bytes = (uint32_t)tiles_in(g, cur.n_c) * kKeyTileBytes;
-                mbar_arrive_expect_tx(&sh.full[s], bytes);
-                bulk_g2s_hint(sh.stage[s], key_cache[b] + g * kStageBytes, bytes, &sh.full[s],
-                              key_policy);
-            }
-            __syncwarp();
-            issued = i + 1;
         }
         // copies still in flight land before the CTA can exit
         for (int64_t j = issued > kStages ? issued - kStages : 0; j < issued; ++j) {
@@ -394,6 +396,10 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
         // i % kIssuers == e (a single thread each); every issuer copies the query
         // scale factors of every sequence segment into its own TMEM slots.
         const int e = warp - kMmaWarp;
+        // descriptors built once; a stage, a tile or a query slot moves the start-address field
+        const uint64_t dA0 = smem_desc(smem_u32(sh.stage[0]), 16, 512, kLayoutSw64);
+        const uint64_t dS0 = smem_desc(smem_u32(sh.stage[0]) + kKeyValBytes, 128, 128, kLayoutNone);
+        const uint64_t dQ0 = smem_desc(smem_u32(sh.q[0]), 16, 512, kLayoutSw64);
         if (lane == 0) {
             int seg = -1, b = 0, prev_b = -1;
             SeqCursor cur;
@@ -419,19 +425,20 @@ k_index_scores_tc(int B, int64_t max_ncomp, int ratio, const uint8_t* __restrict
                 if (!mbar_wait(&sh.acce[a], (uint32_t)((i / kAcc) & 1) ^ 1, abort)) break;
                 tc_fence_after();
                 const int qs = seg & 1;
-                const uint32_t qa = smem_u32(sh.q[qs]);
                 const uint32_t sfb = tmem + kColSFB + 16 * e + 8 * qs;
                 const int nt = tiles_in(f - cur.start, cur.n_c);
-                for (int j = 0; j < nt; ++j) {
-                    const uint32_t st = smem_u32(sh.stage[s]) + j * kKeyTileBytes;
-                    const uint32_t sfa = tmem + kColSFA + 8 * (a * kTilesPerStage + j);
-                    const uint32_t d = tmem + kColD + 32 * (a * kTilesPerStage + j);
-                    tmem_cp_32x128b_x4(sfa, smem_desc(st + kKeyValBytes, 128, 128, kLayoutNone));
-                    tmem_cp_32x128b_x4(sfa + 4, smem_desc(st + kKeyValBytes + 512, 128, 128, kLayoutNone));
-                    mma_mxf4nvf4(d, smem_desc(st, 16, 512, kLayoutSw64),
-                                 smem_desc(qa, 16, 512, kLayoutSw64), kIdesc, sfa, sfb, 0);
-                    mma_mxf4nvf4(d, smem_desc(st + 32, 16, 512, kLayoutSw64),
-                                 smem_desc(qa + 32, 16, 512, kLayoutSw64), kIdesc, sfa + 4, sfb + 4, 1);
+                // descriptors advance by (byte offset >> 4) in their start-address field
+                // (shared addresses stay below 256 KB: no carry out of the field)
+                const uint64_t dQ = dQ0 + (uint64_t)((uint32_t)(qs * kHi * (kDi / 2)) >> 4);
+                uint64_t dA = dA0 + (uint64_t)((uint32_t)(s * kStageBytes) >> 4);
+                uint64_t dS = dS0 + (uint64_t)((uint32_t)(s * kStageBytes) >> 4);
+                uint32_t sfa = tmem + kColSFA + 8 * (a * kTilesPerStage);
+                uint32_t d = tmem + kColD + 32 * (a * kTilesPerStage);
+                for (int j = 0; j < nt; ++j, dA += kKeyTileBytes >> 4, dS += kKeyTileBytes >> 4, sfa += 8, d += 32) {
+                    tmem_cp_32x128b_x4(sfa, dS);
+                    tmem_cp_32x128b_x4(sfa + 4, dS + (512 >> 4));
+                    mma_mxf4nvf4(d, dA, dQ, kIdesc, sfa, sfb, 0);
+                    mma_mxf4nvf4(d, dA + 2, dQ + 2, kIdesc, sfa + 4, sfb + 4, 1);  // K 64..127
                 }
                 tc_commit(&sh.empty[s]);
                 tc_commit(&sh.accf[a]);
