@@ -23,7 +23,11 @@
  *  - Per-sequence caches are reached through device arrays of per-sequence
  *    base pointers (ragged batches need no common stride).
  *  - `stream` is a cudaStream_t passed as void*. Every call only enqueues work
- *    on it and returns; nothing synchronises.
+ *    on it and returns; nothing synchronises. Stream order holds as usual: some
+ *    kernels (the appends, the tensor-core Indexer, the fused attention) are
+ *    programmatic launches whose blocks may be placed while the kernel ahead on
+ *    the stream still runs, but they read and write nothing before it has
+ *    completed.
  *  - Return value: CSA2_OK or a CSA2_ERR_* code for errors found on the host
  *    (bad arguments, unsupported sizes, launch failures; text in
  *    csa2_last_error(), per calling thread). Nothing is enqueued on error.
