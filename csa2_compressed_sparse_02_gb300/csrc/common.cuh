@@ -72,7 +72,9 @@ int sparse_attn_tc_single(const char* name, const csa2_params* p, int B, const v
 // thread 0 of the traced kernels writes {kernel id, launch number} into record
 // words 0-1 at its start and into words 2-3 when it finishes: plain posted stores
 // to host-mapped memory (no fence: nothing waits for them), which the host can
-// read after an error has ended the context.
+// read after an error has ended the context. Kernels launched programmatically may
+// start while the one ahead still runs: the record then holds whichever wrote last,
+// and the launch number (a plain increment) may repeat across such a pair.
 enum TraceKernel { kTraceCompress = 1, kTraceIndex = 2, kTraceSelect = 3, kTraceAttn = 4 };
 namespace {
 __device__ int32_t* g_trace = nullptr;
