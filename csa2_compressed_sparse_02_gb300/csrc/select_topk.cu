@@ -41,30 +41,50 @@ namespace csa2 {
 namespace {
 using namespace sm100;
 
-constexpr int kThreads = 1024;
-constexpr int kWarps = kThreads / 32;
-
 constexpr int kSample = 2048;
-constexpr int kMaxFiltered = 8192;
 constexpr int kMaxFiltered2 = kKp * kBlk;  // level 2: every candidate of the kKp kept blocks
-constexpr int kMaxCand = kMaxFiltered + kSample;  // level 1: filtered keys, sample at the end
 constexpr int kStagePerWarp = 256;   // kept pairs a warp stages during the vector filter's pass
 constexpr int kClMax = 4;            // CTAs of one sequence in the cluster launch
 constexpr int kAttempts = 4;         // thresholds tried before the exact select over every block
-constexpr int kStage = kWarps * kStagePerWarp;  // pairs the level-1 filter can stage
-constexpr int kFlatCap = 2 * kStage;  // positions the flat pass gathers (the whole stage area)
 
+// Two builds: 1,024 threads and up to 8,192 level-1 candidates (159 KB of shared
+// memory: one CTA per SM) for the cluster launch and batches that fill one wave;
+// 512 threads and up to 4,096 candidates (91 KB: two CTAs per SM, so that one CTA's
+// barriers and memory round trips overlap the other's work) for larger batches.
+template <int NT, int MF>
+struct SelCfg {
+    static constexpr int kThreads = NT;
+    static constexpr int kWarps = NT / 32;
+    static constexpr int kMaxFiltered = MF;
+    static constexpr int kMaxCand = MF + kSample;  // level 1: filtered keys, sample at the end
+    static constexpr int kStage = kWarps * kStagePerWarp;  // pairs the level-1 filter can stage
+    static constexpr int kFlatCap = 2 * kStage;  // positions the flat pass gathers (the whole stage area)
+};
+using SelWide = SelCfg<1024, 8192>;
+using SelHalf = SelCfg<512, 4096>;
+
+// the configuration's sizes under their short names, in every function below
+#define SEL_CFG_NAMES                                      \
+    constexpr int kThreads = C::kThreads;                  \
+    constexpr int kWarps = C::kWarps;                      \
+    constexpr int kMaxFiltered = C::kMaxFiltered;          \
+    constexpr int kMaxCand = C::kMaxCand;                  \
+    constexpr int kStage = C::kStage;                      \
+    constexpr int kFlatCap = C::kFlatCap;                  \
+    (void)kThreads, (void)kWarps, (void)kMaxFiltered, (void)kMaxCand, (void)kStage, (void)kFlatCap
+
+template <class C>
 struct SelShared {
     uint32_t hist[256];
-    uint32_t warp_sum[kWarps];
+    uint32_t warp_sum[C::kWarps];
     int32_t bcast[4];
     int32_t kept[kKp];
-    uint32_t cand[kMaxCand];        // level 1: filtered keys (sample at the end); level 2 keys
-    int32_t cand_idx[kMaxFiltered];  // index of each filtered key
+    uint32_t cand[C::kMaxCand];        // level 1: filtered keys (sample at the end); level 2 keys
+    int32_t cand_idx[C::kMaxFiltered];  // index of each filtered key
     uint32_t cand2[kMaxFiltered2];   // level 2 filtered keys
     // level 1 filter: kept (key, index) pairs per warp, in order (keys in
     // [0, kStage), indices in [kStage, 2 kStage)); the flat pass: position keys
-    uint32_t stage[2 * kStage];
+    uint32_t stage[2 * C::kStage];
     // cluster launch: each CTA's level-1 candidate count, per attempt, written into
     // every CTA of the cluster; cnt_bar completes a phase per attempt once all CTAs
     // wrote theirs, gat_bar (CTA 0) once the others copied their candidates in
@@ -87,9 +107,10 @@ __device__ __forceinline__ uint32_t warp_incl_scan(uint32_t v) {
 // With digits < 4 only the top 8*digits bits are resolved: the result is the
 // K-th largest key with its low bits cleared, a lower bound that at least K keys
 // reach (used as a filter threshold).
-template <class KeyAt>
-__device__ uint32_t radix_kth(int n, int K, KeyAt key_at, SelShared& sh, int* need_eq,
+template <class C, class KeyAt>
+__device__ uint32_t radix_kth(int n, int K, KeyAt key_at, SelShared<C>& sh, int* need_eq,
                               int digits = 4) {
+    SEL_CFG_NAMES;
     const int tid = threadIdx.x, lane = tid & 31;
     uint32_t prefix = 0, mask = 0;
     int remaining = K;
@@ -150,14 +171,16 @@ __device__ __forceinline__ uint32_t lanemask_lt() {
 
 // Exclusive scan of one value per warp (lane 0 holds it) over the CTA's warps;
 // every lane of warp w receives the sum over warps < w. *total gets the sum.
-__device__ uint32_t warp_excl_scan(uint32_t v, SelShared& sh, uint32_t* total) {
+template <class C>
+__device__ uint32_t warp_excl_scan(uint32_t v, SelShared<C>& sh, uint32_t* total) {
+    SEL_CFG_NAMES;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (lane == 0) sh.warp_sum[warp] = v;
     __syncthreads();
-    if (warp == 0) {
-        const uint32_t x = sh.warp_sum[lane];
+    if (warp == 0) {  // lanes past the CTA's warp count add nothing
+        const uint32_t x = lane < kWarps ? sh.warp_sum[lane] : 0u;
         const uint32_t xi = warp_incl_scan(x);
-        sh.warp_sum[lane] = xi - x;
+        if (lane < kWarps) sh.warp_sum[lane] = xi - x;
         if (lane == 31) sh.bcast[3] = (int)xi;
     }
     __syncthreads();
@@ -171,8 +194,9 @@ __device__ uint32_t warp_excl_scan(uint32_t v, SelShared& sh, uint32_t* total) {
 // indices, in ascending order, through emit(rank, i). Each warp owns a
 // contiguous range of indices and walks it 32 at a time (coalesced), so tie
 // ranks and output ranks follow index order via ballots.
-template <class KeyAt, class Emit>
-__device__ uint32_t select_top(int n, int K, KeyAt key_at, Emit emit, SelShared& sh) {
+template <class C, class KeyAt, class Emit>
+__device__ uint32_t select_top(int n, int K, KeyAt key_at, Emit emit, SelShared<C>& sh) {
+    SEL_CFG_NAMES;
     int need_eq;
     const uint32_t kth = radix_kth(n, K, key_at, sh, &need_eq);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -211,9 +235,10 @@ __device__ uint32_t select_top(int n, int K, KeyAt key_at, Emit emit, SelShared&
 // pairs written to keys_out/idx_out (capacity cap). Each warp walks its own
 // contiguous range, 8 x 32 elements per round with the loads issued first.
 // Returns the count (which may exceed cap: then nothing was written).
-template <class KeyAt>
+template <class C, class KeyAt>
 __device__ int filter_ge(int n, uint32_t thr, KeyAt key_at, uint32_t* keys_out, int32_t* idx_out,
-                         int cap, SelShared& sh) {
+                         int cap, SelShared<C>& sh) {
+    SEL_CFG_NAMES;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t lt = lanemask_lt();
     const int R = (n + kWarps - 1) / kWarps;
@@ -267,8 +292,10 @@ __device__ int filter_ge(int n, uint32_t thr, KeyAt key_at, uint32_t* keys_out, 
 // counts then places every slot. Returns -1 when a slot overflowed (the caller
 // then uses filter_ge), else the count (which may exceed cap: then nothing was
 // written).
+template <class C>
 __device__ int filter_ge_vec(int n, uint32_t thr, const float* __restrict__ bm, uint32_t* keys_out,
-                             int32_t* idx_out, int cap, SelShared& sh) {
+                             int32_t* idx_out, int cap, SelShared<C>& sh) {
+    SEL_CFG_NAMES;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int chunks = (n + 127) / 128;
     const int R = (chunks + kWarps - 1) / kWarps;
@@ -354,12 +381,14 @@ __device__ int filter_ge_vec(int n, uint32_t thr, const float* __restrict__ bm, 
 // CTA filters a quarter of the block maxima at level 1 and CTA 0 (rank 0 of the
 // cluster) finishes the sequence alone once the others have copied their
 // candidates into its shared memory.
-__global__ void __launch_bounds__(kThreads, 1)
+template <class C>
+__global__ void __launch_bounds__(C::kThreads, 1024 / C::kThreads)
 k_select_topk(int64_t max_ncomp, int ratio, const float* __restrict__ scores,
               const float* __restrict__ block_max, const int32_t* __restrict__ n_tokens,
               int32_t* idx, int32_t* n_sel_out, int32_t* dev_status, int ncl) {
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    SelShared& sh = *reinterpret_cast<SelShared*>(smem_raw);
+    SEL_CFG_NAMES;
+    SelShared<C>& sh = *reinterpret_cast<SelShared<C>*>(smem_raw);
     const int b = blockIdx.x / ncl, tid = threadIdx.x;
     const int rank = ncl > 1 ? (int)cluster_ctarank() : 0;
     trace_start(kTraceSelect);
@@ -580,7 +609,10 @@ k_select_topk(int64_t max_ncomp, int ratio, const float* __restrict__ scores,
 
 CSA2_TRACE_SETTER(trace_set_select)
 
-cudaError_t preload_select() { return preload_kernel(k_select_topk, (int)sizeof(SelShared)); }
+cudaError_t preload_select() {
+    const cudaError_t e = preload_kernel(k_select_topk<SelWide>, (int)sizeof(SelShared<SelWide>));
+    return e != cudaSuccess ? e : preload_kernel(k_select_topk<SelHalf>, (int)sizeof(SelShared<SelHalf>));
+}
 
 }  // namespace csa2
 
@@ -602,20 +634,21 @@ extern "C" int csa2_select_topk(const csa2_params* p, int B, int64_t max_ncomp,
         return fail(CSA2_ERR_INVALID_ARG, "select_topk: NULL buffer");
     // loads the kernel and sets its shared-memory limit on this device, once per device
     if (const int rc = ensure_loaded()) return rc;
-    const int smem = (int)sizeof(SelShared);
     // A small batch leaves most SMs idle with one CTA per sequence: then each
     // sequence's level-1 pass over its block maxima is spread over a cluster of
     // kClMax CTAs, when the grid stays within p->max_ctas (0: two waves of the SMs).
+    // A batch of more sequences than SMs runs the 512-thread build, two CTAs per SM.
     int dev = 0, sms = 1;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return check_launch("select_topk: device");
     const int64_t cta_cap = p->max_ctas > 0 ? p->max_ctas : 2 * (int64_t)sms;
     const int ncl = (int64_t)B * kClMax <= cta_cap ? kClMax : 1;
+    const bool half = ncl == 1 && B > sms;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(B * ncl));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
+    cfg.blockDim = dim3(half ? SelHalf::kThreads : SelWide::kThreads);
+    cfg.dynamicSmemBytes = half ? (int)sizeof(SelShared<SelHalf>) : (int)sizeof(SelShared<SelWide>);
     cfg.stream = static_cast<cudaStream_t>(stream);
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -624,8 +657,11 @@ extern "C" int csa2_select_topk(const csa2_params* p, int B, int64_t max_ncomp,
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, k_select_topk, max_ncomp, p->compress_ratio, scores, block_max,
-                           n_tokens, idx, n_sel, dev_status, ncl) != cudaSuccess)
-        return check_launch("select_topk");
+    const cudaError_t e =
+        half ? cudaLaunchKernelEx(&cfg, k_select_topk<SelHalf>, max_ncomp, p->compress_ratio, scores,
+                                  block_max, n_tokens, idx, n_sel, dev_status, ncl)
+             : cudaLaunchKernelEx(&cfg, k_select_topk<SelWide>, max_ncomp, p->compress_ratio, scores,
+                                  block_max, n_tokens, idx, n_sel, dev_status, ncl);
+    if (e != cudaSuccess) return check_launch("select_topk");
     return check_launch("select_topk");
 }

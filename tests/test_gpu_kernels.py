@@ -443,6 +443,46 @@ def test_select_topk_exact_with_ties(levels, pad, cluster):
         assert np.array_equal(gi[b], ref), (b, n, np.nonzero(gi[b] != ref)[0][:5])
 
 
+@pytest.mark.parametrize("levels", [3, 0], ids=["ties", "continuous"])
+def test_select_topk_many_sequences_half_build(levels):
+    """More sequences than SMs (one CTA each, the 512-thread build with two CTAs per
+    SM): every sequence exact, over ragged lengths from empty to 70,001 positions,
+    with tied and continuous scores and planted maxima."""
+    rng = np.random.default_rng(31 + levels)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    base = [0, 1, 5, 511, 512, 513, 4095, 8000, 16384, 16385, 20000, 40000, 70001]
+    B = sms + 48
+    n_cs = base + [int(x) for x in rng.integers(0, 30000, B - len(base))]
+    max_nc = max(n_cs)
+    scores = np.zeros((B, max_nc), np.float32)
+    for b, n in enumerate(n_cs):
+        if levels:
+            scores[b, :n] = rng.integers(0, levels, n).astype(np.float32) * 0.25
+        else:
+            scores[b, :n] = rng.standard_normal(n).astype(np.float32)
+        if n > 100:
+            scores[b, rng.choice(n, 16, replace=False)] = 1e4
+    nb = math.ceil(max_nc / 8)
+    bm = np.full((B, nb), -np.inf, np.float32)
+    for b, n in enumerate(n_cs):
+        padded = np.full(math.ceil(n / 8) * 8, -np.inf, np.float32)
+        padded[:n] = scores[b, :n]
+        bm[b, :len(padded) // 8] = padded.reshape(-1, 8).max(1) if n else bm[b, :0]
+    p = api.default_params()
+    idx = torch.full((B, 512), 123, dtype=torch.int32, device=DEV)
+    n_sel = torch.zeros(B, dtype=torch.int32, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    api.select_topk(p, max_nc, t(scores), t(bm), t(np.array([2 * n for n in n_cs], np.int32)),
+                    idx, n_sel, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    gi, gn = idx.cpu().numpy(), n_sel.cpu().numpy()
+    for b, n in enumerate(n_cs):
+        ref, m = orc.select(scores[b, :n], 8, 2048, 512)
+        assert gn[b] == m, (b, n)
+        assert np.array_equal(gi[b], ref), (b, n, np.nonzero(gi[b] != ref)[0][:5])
+
+
 # --------------------------------------------------------------------------- attention
 def _attn_case(rng, Ts, f32, n_idx_valid):
     B = len(Ts)
