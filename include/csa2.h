@@ -328,9 +328,11 @@ int csa2_index_scores_cuda_cores(const csa2_params* p, int B, int64_t max_ncomp,
  * Scores compare as fp32 values (-0 == +0). Ties are resolved exactly.
  * Because the block score is its best position's and topk_blocks - 1 >=
  * topk_pos, the result is the topk_pos best positions of the sequence; the
- * kernel finds them among the positions of the topk_pos best blocks. A small
- * batch (4 B <= max_ctas, or 2 x SMs) runs each sequence on a cluster of 4 CTAs
- * that share the pass over the block maxima through distributed shared memory.
+ * kernel finds them among the positions of the blocks whose maximum reaches a
+ * sampled threshold that at least topk_pos block maxima reach. A small batch
+ * (4 B <= max_ctas, or 2 x SMs) runs each sequence on a cluster of 4 CTAs that
+ * share the pass over the block maxima through distributed shared memory; a
+ * batch of more sequences than SMs runs a 512-thread build, two CTAs per SM.
  */
 int csa2_select_topk(const csa2_params* p, int B, int64_t max_ncomp,
                      const float* scores, const float* block_max, const int32_t* n_tokens,
